@@ -1,0 +1,323 @@
+"""Benchmark of one MoE layer over an 8-token verify block (MXFP4 experts).
+
+`python bench.py [--gpus N] [--steps K] [--warmup W] [--workload large] [--impl reference]`
+
+A step is one forward of the whole layer (routing, grouping, expert FFN,
+combine) on seeded synthetic inputs resident in HBM.  The metric is
+microseconds per MoE layer per verify block (lower is better), reported with
+the achieved HBM bandwidth over the layer's algorithmic bytes (the routed
+experts' nibbles and scales, router weights, x read, y written) and its
+fraction of the measured copy bandwidth.  L2 is flushed (a 256 MiB write)
+between timed steps, outside the per-step events.  Prints one JSON line.
+
+`--impl reference` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload and prints the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+# the CPU oracle legs run single-threaded (BLAS included), so "cores" is 1
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+ACCEPTANCE_LENGTH = 6.30   # coding-task average accepted tokens per verify (page 3, "DFlash")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    return ws, rank
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: one verify block's layer output
+    for a bounded sample of its routed experts, scaled to the whole layer."""
+    ws, rank = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    from mxfp4_moe_expert_gb300.synth import WORKLOADS, expert_weight, make_inputs
+    from oracle import moe_oracle as O
+
+    wl = WORKLOADS[args.workload]
+    inputs = make_inputs(wl)
+    xf = O.bf16_to_f64(inputs.x.view(torch.int16).numpy().view(np.uint16))
+    wr = O.bf16_to_f64(inputs.layers[0].router_w.view(torch.int16).numpy().view(np.uint16))
+    b = inputs.layers[0].router_b.double().numpy()
+    logits = O.router_logits(xf, wr, b)
+    idx, gate = O.topk_gates(logits, wl.k)
+    counts, offsets, perm = O.assignment(idx, wl.E)
+    active = [int(e) for e in np.nonzero(counts)[0]]
+    n_sample = min(len(active), args.ref_experts)
+    # encoded bytes of the sampled experts (prepared outside the timed region)
+    enc = {}
+    for e in active[:n_sample]:
+        enc[e] = {m: O.quantize(expert_weight(wl, 0, e, m).numpy()) for m in ("gate", "up", "down")}
+
+    def one_step():
+        t0 = time.perf_counter()
+        lg = O.router_logits(xf, wr, b)
+        O.topk_gates(lg, wl.k)
+        for e in active[:n_sample]:
+            m = O.ExpertMatrices(*enc[e]["gate"], *enc[e]["up"], *enc[e]["down"])
+            for p in perm[offsets[e]:offsets[e + 1]]:
+                m.ffn(xf[int(p) // wl.k])
+        dt = time.perf_counter() - t0
+        return dt * len(active) / n_sample   # scaled to every routed expert of the block
+
+    for _ in range(args.warmup):
+        one_step()
+    times = [one_step() for _ in range(args.steps)]
+    us = statistics.mean(times) * 1e6
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
+    sample = f"{n_sample} of {len(active)} routed experts of one {wl.T}-token verify block, scaled by {len(active)}/{n_sample}"
+    line = {
+        "impl": "reference", "metric": "us_per_moe_layer_per_verify_block", "value": round(us, 1), "unit": "us",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import mxfp4_moe_expert_gb300 as pkg
+    from mxfp4_moe_expert_gb300.synth import WORKLOADS
+    from mxfp4_moe_expert_gb300.workload import device_layers, touched_bytes
+
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not os.path.exists(pkg.LIB_PATH):
+        from mxfp4_moe_expert_gb300 import build
+        build.build()
+
+    wl = WORKLOADS[args.workload]
+    inputs, layers = device_layers(wl, device=dev)
+    flags = pkg.MOE_FLAG_NORM if wl.norm else 0
+    moe = pkg.MoeLayers(hidden=wl.H, inter=wl.I, num_experts=wl.E, top_k=wl.k, max_tokens=wl.T, layers=layers,
+                        flags=flags, rms_eps=wl.rms_eps)
+    x = inputs.x.to(dev)
+    y = torch.empty((wl.T, wl.H), dtype=torch.float32, device=dev)
+    wsp = moe.new_workspace(wl.T, dev)
+    stream = torch.cuda.current_stream(dev)
+    st = stream.cuda_stream
+
+    # routing of this input: the algorithmic bytes of one step
+    bufs, dbg = moe.debug_buffers(wl.T, dev)
+    moe.forward(x, y, wsp, st, dbg, check=True)
+    counts = bufs["expert_counts"].cpu()
+    alg_bytes = touched_bytes(wl, [counts[l] for l in range(wl.layers)])
+    n_active = [int((counts[l] > 0).sum()) for l in range(wl.layers)]
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        moe.forward(x, y, wsp, st)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.__enter__()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        moe.forward(x, y, wsp, st)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if ws > 1:
+        torch.distributed.barrier()
+    if sampler:
+        sampler.__exit__()
+    per = [a.elapsed_time(b) * 1e3 for a, b in ev]   # us
+    us = statistics.mean(per)
+    st_code = pkg.moe_mxfp4_check(moe.handle, wsp.data_ptr(), st)
+    if st_code != 0:
+        raise pkg.MoeError(st_code, "forward")
+    if ws > 1:
+        t = torch.tensor([us], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        us = float(t.item())
+
+    # end to end: host buffers through the C ABI, copies inside the timed region
+    xh = inputs.x.clone().pin_memory()
+    yh = torch.empty((wl.T, wl.H), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        moe.forward_host(xh, yh, wsp)
+    e2e = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        moe.forward_host(xh, yh, wsp)
+        e2e.append((time.perf_counter() - t0) * 1e6)
+    e2e_us = statistics.mean(e2e)
+
+    if rank != 0:
+        return
+    peak, peak_kind = _peaks()
+    gbs = alg_bytes / (us * 1e-6) / 1e9
+    launches_per_step = 1 + 5 * wl.layers + (wl.layers if wl.norm else 0)
+    clocks = sampler.summary() if sampler else None
+    line = {
+        "metric": "us_per_moe_layer_per_verify_block", "value": round(us / wl.layers, 2), "unit": "us",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (MXFP4 weights)",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "layers": wl.layers, "routed_experts": n_active, "algorithmic_bytes": alg_bytes,
+                   "l2": "flushed between steps (256 MiB write outside the per-step events)",
+                   "parallelism": f"replicas{ws}"},
+        "hbm_gbs": round(gbs, 1),
+        "implied_tokens_per_s": round(ACCEPTANCE_LENGTH / (us * 1e-6), 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "whole forward (all phases)"},
+        "e2e": {"value": round(e2e_us / wl.layers, 2), "unit": "us", "h2d_bytes_per_step": wl.T * wl.H * 2,
+                "d2h_bytes_per_step": wl.T * wl.H * 4},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s": round(wall, 4),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line))
+
+
+def cpu_baseline(wl):
+    """The oracle on the host cores, on a bounded sample (a few routed experts)."""
+    import numpy as np
+    import torch
+
+    from mxfp4_moe_expert_gb300.synth import expert_weight, make_inputs
+    from oracle import moe_oracle as O
+
+    inputs = make_inputs(wl)
+    xf = O.bf16_to_f64(inputs.x.view(torch.int16).numpy().view(np.uint16))
+    wr = O.bf16_to_f64(inputs.layers[0].router_w.view(torch.int16).numpy().view(np.uint16))
+    b = inputs.layers[0].router_b.double().numpy()
+    if wl.norm:
+        xf = O.rmsnorm(xf, O.bf16_to_f64(inputs.layers[0].norm_w.view(torch.int16).numpy().view(np.uint16)),
+                       wl.rms_eps)
+    idx, _ = O.topk_gates(O.router_logits(xf, wr, b), wl.k)
+    counts, offsets, perm = O.assignment(idx, wl.E)
+    active = [int(e) for e in np.nonzero(counts)[0]]
+    n = min(3, len(active))
+    enc = {e: {m: O.quantize(expert_weight(wl, 0, e, m).numpy()) for m in ("gate", "up", "down")}
+           for e in active[:n]}
+    t0 = time.perf_counter()
+    O.topk_gates(O.router_logits(xf, wr, b), wl.k)
+    for e in active[:n]:
+        m = O.ExpertMatrices(*enc[e]["gate"], *enc[e]["up"], *enc[e]["down"])
+        for p in perm[offsets[e]:offsets[e + 1]]:
+            m.ffn(xf[int(p) // wl.k])
+    dt = (time.perf_counter() - t0) * len(active) / n * wl.layers
+    return {"value": round(dt * 1e6 / wl.layers, 1), "unit": "us", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {len(active)} routed experts of layer 0, scaled to all routed experts"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="large", choices=["tiny", "mid", "large", "batched", "stack"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-experts", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * moe_mxfp4.h -- C ABI of the MXFP4 Mixture-of-Experts expert layer for GB300 (sm_103a).
+ *
+ * One call runs one MoE layer (or a stack of pre-norm MoE layers) over a
+ * speculative-decoding verify block: router GEMM, softmax over the top-k
+ * logits, token-to-expert grouping, per-expert SwiGLU FFN on MXFP4 weights
+ * that are dequantised in registers, and the gate-weighted combine.
+ *
+ * Where the operation comes from (page title, section):
+ *  - "MiMo x TileRT" (blog.hypho.cn), "第一层：FP4 选择性量化": only the MoE
+ *    expert weights are stored in OCP Microscaling FP4 (MXFP4); the router keeps
+ *    higher precision.  "万亿参数推理为什么特别难": decode speed is bounded by
+ *    HBM bandwidth / bytes read per token, so the layer is judged on bytes moved.
+ *  - "MiMo 把 1T 模型推到每秒千 token" (vatt-ghern), "FP4：只量化 MoE expert":
+ *    blocks of weights share one scale, elements are FP4; the router's top-k is
+ *    precision-sensitive.  "DFlash：block-level masked 並行草稿": one target
+ *    forward verifies 8 drafted positions.  "persistent engine kernel 與 warp
+ *    specialization": one resident launch instead of one launch per operator.
+ *  - Implementation guide (shengyayun), "关键实现细节" items 1 and 3: expert
+ *    linears gate_proj / up_proj / down_proj; per-launch gaps of 5-10 us.
+ *  - OCP Microscaling Formats v1.0 (cited by the pages): E2M1 elements, E8M0
+ *    scales 2^(b-127) with 0xFF = NaN, 32 elements per scale.
+ *
+ * Conventions
+ *  - Every pointer named *_dev is a device pointer owned by the caller; the
+ *    library never allocates device memory (the caller provides a workspace
+ *    whose size moe_mxfp4_workspace_bytes reports) and never frees caller memory.
+ *  - Weights are BORROWED at create time: they must stay allocated and unchanged
+ *    until moe_mxfp4_destroy.  No copy or repack is made.
+ *  - Calls are asynchronous on the given stream (a cudaStream_t passed as void*,
+ *    NULL = legacy default stream) unless stated otherwise.  Errors the host can
+ *    see are returned at once; errors found on the device (a NaN scale byte, a
+ *    device wait that timed out) are written to a status word in the workspace
+ *    and returned by moe_mxfp4_check.  No call aborts or throws.
+ *  - One handle + one workspace may be used by one stream at a time.
+ *
+ * Layouts (row-major, contraction dimension contiguous):
+ *  - x: bf16 [T, H].   y: fp32 [T, H] (bf16 with MOE_FLAG_OUT_BF16).
+ *  - router_w: bf16 [E, H];  router_b: fp32 [E] (may be NULL = zero).
+ *  - gate_q, up_q: uint8 [E, I, H/2];  gate_s, up_s: uint8 [E, I, H/32].
+ *  - down_q: uint8 [E, H, I/2];        down_s: uint8 [E, H, I/32].
+ *    Element 2j of a row is the LOW nibble of byte j; a nibble is an E2M1 code
+ *    (bit 3 sign, bits 2..1 exponent with bias 1, bit 0 mantissa).  Scale byte
+ *    S[r, c/32] multiplies elements c of row r by 2^(S - 127).
+ *  - norm_w: bf16 [H] (required with MOE_FLAG_NORM).
+ *  Every base pointer must be 16-byte aligned; H and I must be multiples of 128.
+ *
+ * What a layer computes (per token t):
+ *   logit[e] = sum_h x[t,h] Wr[e,h] + b[e]
+ *   (idx, gate) = top-k by (logit desc, expert asc); gate = softmax(selected logits)
+ *   for slot j: e = idx[j]; a = silu(Wg_e x_t) * (Wu_e x_t); d_j = Wd_e a
+ *   y[t] = sum_j gate[j] d_j  (slot order j = 0..k-1)
+ * With MOE_FLAG_NORM the call runs num_layers layers r <- r + MoE_l(RMSNorm_l(r))
+ * with RMSNorm(r) = r * w / sqrt(mean(r^2) + eps), r_0 = x, and y = r_L.
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define MOE_OK               0
+#define MOE_ERR_INVALID_ARG (-1) /* bad size, NULL or misaligned pointer, T > max_tokens */
+#define MOE_ERR_UNSUPPORTED (-2) /* no sm_103 device current, or a shape outside the limits */
+#define MOE_ERR_CUDA        (-3) /* a CUDA runtime call failed */
+#define MOE_ERR_TIMEOUT     (-4) /* a device-side wait gave up (grid barrier / expert counter) */
+#define MOE_ERR_BAD_SCALE   (-5) /* an E8M0 scale byte of a routed expert is 0xFF (NaN) */
+#define MOE_ERR_WORKSPACE   (-6) /* workspace NULL, misaligned (256 B) or too small */
+
+/* ---- config flags ------------------------------------------------------- */
+#define MOE_FLAG_NORM         (1u << 0) /* pre-norm residual stack (see above) */
+#define MOE_FLAG_OUT_BF16     (1u << 1) /* y is bf16 instead of fp32 */
+#define MOE_FLAG_MULTI_KERNEL (1u << 2) /* one launch per phase (comparison path) */
+#define MOE_FLAG_NO_DENSE     (1u << 3) /* never use the tensor-core expert path */
+
+typedef struct moe_mxfp4_handle moe_mxfp4_handle; /* opaque, host-side */
+
+typedef struct {
+    int32_t num_layers;   /* >= 1; > 1 requires MOE_FLAG_NORM */
+    int32_t hidden;       /* H, multiple of 128, <= 16384 */
+    int32_t inter;        /* I, multiple of 128, <= 16384 */
+    int32_t num_experts;  /* E, 1..1024 */
+    int32_t top_k;        /* k, 1..min(E, 32) */
+    int32_t max_tokens;   /* largest T a forward will get, 1..4096 */
+    float rms_eps;        /* RMSNorm epsilon (used with MOE_FLAG_NORM) */
+    uint32_t flags;       /* MOE_FLAG_* */
+    int32_t expert_begin; /* experts [expert_begin, expert_end) are computed here; */
+    int32_t expert_end;   /* tokens routed elsewhere contribute 0 (expert-parallel shard). 0,0 = all */
+    int32_t dense_threshold; /* tokens per expert from which the tensor-core path runs; 0 = default */
+    int32_t timeout_us;   /* bound of every device-side wait in microseconds; 0 = default (200000) */
+} moe_mxfp4_config;
+
+typedef struct {
+    const void* router_w_dev;   /* bf16 [E, H] */
+    const float* router_b_dev;  /* fp32 [E] or NULL */
+    const uint8_t* gate_q_dev;  /* [E, I, H/2] */
+    const uint8_t* gate_s_dev;  /* [E, I, H/32] */
+    const uint8_t* up_q_dev;    /* [E, I, H/2] */
+    const uint8_t* up_s_dev;    /* [E, I, H/32] */
+    const uint8_t* down_q_dev;  /* [E, H, I/2] */
+    const uint8_t* down_s_dev;  /* [E, H, I/32] */
+    const void* norm_w_dev;     /* bf16 [H] or NULL */
+} moe_mxfp4_layer;
+
+/* Optional copies of the routing of every layer, written by a forward when the
+ * pointers are non-NULL (device memory, caller-owned):
+ *   topk_idx int32 [L, T, k], topk_gate fp32 [L, T, k], expert_counts int32 [L, E],
+ *   expert_offsets int32 [L, E+1], perm int32 [L, T*k] (pair ids t*k+j grouped by
+ *   expert, ascending by (t, j) inside an expert). */
+typedef struct {
+    int32_t* topk_idx_dev;
+    float* topk_gate_dev;
+    int32_t* expert_counts_dev;
+    int32_t* expert_offsets_dev;
+    int32_t* perm_dev;
+} moe_mxfp4_debug;
+
+/* Validates the config and the layer pointers (alignment, device), and checks
+ * that the current device is an sm_103 GPU.  layers points to num_layers
+ * descriptors (host memory, copied).  On success *out receives a handle. */
+int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
+                     moe_mxfp4_handle** out);
+
+/* Bytes of device workspace a forward over num_tokens tokens needs. */
+int moe_mxfp4_workspace_bytes(const moe_mxfp4_handle* h, int32_t num_tokens, size_t* bytes);
+
+/* Runs the layer (stack) on num_tokens rows of x_dev into y_dev.  workspace_dev
+ * must be 256-byte aligned and at least moe_mxfp4_workspace_bytes long; its
+ * contents need no initialisation and are overwritten.  x_dev and y_dev may not
+ * alias each other or the workspace.  num_tokens == 0 is a no-op.  dbg may be NULL. */
+int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens, void* y_dev,
+                      void* workspace_dev, size_t workspace_bytes, void* stream,
+                      const moe_mxfp4_debug* dbg);
+
+/* The same forward on HOST buffers: copies x_host (bf16 [T, H]) into the
+ * workspace, runs the forward, copies y back to y_host (fp32 or bf16 [T, H])
+ * and synchronises the stream.  Pinned host memory makes the copies
+ * asynchronous.  Returns the device status (as moe_mxfp4_check). */
+int moe_mxfp4_forward_host(moe_mxfp4_handle* h, const void* x_host, int32_t num_tokens, void* y_host,
+                           void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/* Synchronises the stream and returns the device status word of the last
+ * forward that used this workspace (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_BAD_SCALE). */
+int moe_mxfp4_check(moe_mxfp4_handle* h, const void* workspace_dev, void* stream);
+
+/* Frees the handle (host memory only).  NULL is ignored. */
+void moe_mxfp4_destroy(moe_mxfp4_handle* h);
+
+/* Static description of a status code. */
+const char* moe_mxfp4_status_string(int status);
+
+/* MXFP4 conversion of an fp32 matrix w_dev [rows, cols] (cols a multiple of 32)
+ * into nibbles q_dev [rows, cols/2] and E8M0 scales s_dev [rows, cols/32], by the
+ * OCP MX v1.0 rule: per block of 32, X = 2^(floor(log2 amax) - 2) (byte clamped to
+ * [0, 254]; an all-zero block gets byte 127); elements w/X rounded to the nearest
+ * E2M1 value, ties to even, saturating at +-6; the sign bit is the sign of w.
+ * NaN inputs are not supported.  Device pointers (w_dev and q_dev 16-byte
+ * aligned), asynchronous on stream. */
+int moe_mxfp4_quantize(const float* w_dev, int64_t rows, int64_t cols, uint8_t* q_dev, uint8_t* s_dev,
+                       void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_MXFP4_H */

@@ -1,0 +1,256 @@
+// Host side of the C ABI declared in include/moe_mxfp4.h: validation, the
+// workspace contract, and the launch sequence of a forward.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "expert_simple.cuh"
+#include "layer_ops.cuh"
+#include "route.cuh"
+
+struct moe_mxfp4_handle {
+    moe_mxfp4_config cfg;
+    std::vector<moe_mxfp4_layer> layers;
+    int device = 0;
+    int sm_count = 0;
+    int e_begin = 0, e_end = 0;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kDefaultTimeoutUs = 200000;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// Byte offsets of the workspace sections for T tokens.
+struct WsLayout {
+    size_t status, xstage, ystage, act, resid, logits, idx, gate, counts, offsets, perm, active, hbuf, partial, total;
+};
+
+WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
+    WsLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
+    const size_t H = (size_t)c.hidden, I = (size_t)c.inter, E = (size_t)c.num_experts, k = (size_t)c.top_k;
+    L.status = take(64);
+    L.xstage = take((size_t)T * H * 2);
+    L.ystage = take((size_t)T * H * 4);
+    L.act = take((size_t)T * H * 4);
+    L.resid = take((size_t)T * H * 4);
+    L.logits = take((size_t)T * E * 4);
+    L.idx = take((size_t)T * k * 4);
+    L.gate = take((size_t)T * k * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm = take((size_t)T * k * 4);
+    L.active = take((E + 1) * 4);
+    L.hbuf = take((size_t)T * k * I * 4);
+    L.partial = take((size_t)T * k * H * 4);
+    L.total = o;
+    return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool is_device_ptr(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+int check_layer(const moe_mxfp4_config& c, const moe_mxfp4_layer& l) {
+    const void* req[] = {l.router_w_dev, l.gate_q_dev, l.gate_s_dev, l.up_q_dev, l.up_s_dev, l.down_q_dev, l.down_s_dev};
+    for (const void* p : req)
+        if (!p || !aligned16(p) || !is_device_ptr(p)) return MOE_ERR_INVALID_ARG;
+    if (l.router_b_dev && ((reinterpret_cast<uintptr_t>(l.router_b_dev) & 3) || !is_device_ptr(l.router_b_dev)))
+        return MOE_ERR_INVALID_ARG;
+    if (c.flags & MOE_FLAG_NORM) {
+        if (!l.norm_w_dev || !aligned16(l.norm_w_dev) || !is_device_ptr(l.norm_w_dev)) return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+moe::RouteBufs route_bufs(char* ws, const WsLayout& L) {
+    moe::RouteBufs rb;
+    rb.logits = reinterpret_cast<float*>(ws + L.logits);
+    rb.idx = reinterpret_cast<int*>(ws + L.idx);
+    rb.gate = reinterpret_cast<float*>(ws + L.gate);
+    rb.counts = reinterpret_cast<int*>(ws + L.counts);
+    rb.offsets = reinterpret_cast<int*>(ws + L.offsets);
+    rb.perm = reinterpret_cast<int*>(ws + L.perm);
+    rb.active = reinterpret_cast<int*>(ws + L.active);
+    return rb;
+}
+
+void copy_debug(const moe_mxfp4_debug* dbg, int l, int T, int E, int k, const moe::RouteBufs& rb, cudaStream_t st) {
+    if (!dbg) return;
+    auto cp = [&](void* dst, size_t per_layer, const void* src) {
+        if (dst)
+            cudaMemcpyAsync(static_cast<char*>(dst) + per_layer * l, src, per_layer, cudaMemcpyDeviceToDevice, st);
+    };
+    cp(dbg->topk_idx_dev, (size_t)T * k * 4, rb.idx);
+    cp(dbg->topk_gate_dev, (size_t)T * k * 4, rb.gate);
+    cp(dbg->expert_counts_dev, (size_t)E * 4, rb.counts);
+    cp(dbg->expert_offsets_dev, (size_t)(E + 1) * 4, rb.offsets);
+    cp(dbg->perm_dev, (size_t)T * k * 4, rb.perm);
+}
+
+// Multi-kernel forward: one launch per phase and per layer.
+int forward_multi_kernel(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, const WsLayout& L,
+                         cudaStream_t st, const moe_mxfp4_debug* dbg) {
+    const moe_mxfp4_config& c = h->cfg;
+    const int H = c.hidden, I = c.inter, E = c.num_experts, k = c.top_k;
+    const bool norm = (c.flags & MOE_FLAG_NORM) != 0;
+    const int y_bf16 = (c.flags & MOE_FLAG_OUT_BF16) ? 1 : 0;
+    int* status = reinterpret_cast<int*>(ws + L.status);
+    float* act = reinterpret_cast<float*>(ws + L.act);
+    float* resid = norm ? reinterpret_cast<float*>(ws + L.resid) : nullptr;
+    float* hbuf = reinterpret_cast<float*>(ws + L.hbuf);
+    float* partial = reinterpret_cast<float*>(ws + L.partial);
+    const moe::RouteBufs rb = route_bufs(ws, L);
+    const int max_active = std::min(E, T * k);
+    const int n = T * H;
+
+    moe::prep_input_kernel<<<std::min((n + 255) / 256, 4 * h->sm_count), 256, 0, st>>>(
+        reinterpret_cast<const __nv_bfloat16*>(x), n, act, resid);
+    const size_t sel_smem = (size_t)(33 * E + 64) * sizeof(int);
+    for (int l = 0; l < c.num_layers; ++l) {
+        const moe_mxfp4_layer& ly = h->layers[l];
+        if (norm)
+            moe::rmsnorm_kernel<<<T, 256, 0, st>>>(resid, reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev), H,
+                                                   c.rms_eps, act);
+        moe::route_logits_kernel<<<(E + 7) / 8, 256, 0, st>>>(
+            act, T, H, reinterpret_cast<const __nv_bfloat16*>(ly.router_w_dev), ly.router_b_dev, E, rb.logits);
+        moe::route_select_kernel<<<1, 1024, sel_smem, st>>>(rb.logits, T, E, k, h->e_begin, h->e_end, rb);
+        const moe::ExpertWeights w{ly.gate_q_dev, ly.gate_s_dev, ly.up_q_dev, ly.up_s_dev, ly.down_q_dev, ly.down_s_dev};
+        moe::gateup_simple_kernel<<<dim3(I / 32, max_active), 256, 0, st>>>(act, H, I, k, w, rb, hbuf, status, l);
+        moe::down_simple_kernel<<<dim3(H / 32, max_active), 256, 0, st>>>(hbuf, H, I, w, rb, partial, status, l);
+        const bool last = l == c.num_layers - 1;
+        moe::combine_kernel<<<dim3(T, (H + 1023) / 1024), 256, 0, st>>>(partial, rb, H, k, h->e_begin, h->e_end,
+                                                                        resid, last ? y : nullptr, y_bf16);
+        copy_debug(dbg, l, T, E, k, rb, st);
+    }
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_mxfp4_status_string(int s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported device or shape";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+        case MOE_ERR_BAD_SCALE: return "E8M0 scale byte 0xFF (NaN) in a routed expert";
+        case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        default: return "unknown status";
+    }
+}
+
+int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers, moe_mxfp4_handle** out) {
+    if (!cfg || !layers || !out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    const moe_mxfp4_config& c = *cfg;
+    if (c.num_layers < 1 || (c.num_layers > 1 && !(c.flags & MOE_FLAG_NORM))) return MOE_ERR_INVALID_ARG;
+    if (c.hidden <= 0 || c.hidden % 128 || c.hidden > 16384) return MOE_ERR_INVALID_ARG;
+    if (c.inter <= 0 || c.inter % 128 || c.inter > 16384) return MOE_ERR_INVALID_ARG;
+    if (c.num_experts < 1 || c.num_experts > moe::kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (c.top_k < 1 || c.top_k > c.num_experts || c.top_k > moe::kMaxTopK) return MOE_ERR_INVALID_ARG;
+    if (c.max_tokens < 1 || c.max_tokens > 4096) return MOE_ERR_INVALID_ARG;
+    if ((c.flags & MOE_FLAG_NORM) && !(c.rms_eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (c.timeout_us < 0 || c.dense_threshold < 0) return MOE_ERR_INVALID_ARG;
+    int eb = c.expert_begin, ee = c.expert_end;
+    if (eb == 0 && ee == 0) ee = c.num_experts;
+    if (eb < 0 || ee > c.num_experts || eb >= ee) return MOE_ERR_INVALID_ARG;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;
+    for (int l = 0; l < c.num_layers; ++l) {
+        const int r = check_layer(c, layers[l]);
+        if (r != MOE_OK) return r;
+    }
+    const size_t sel_smem = (size_t)(33 * c.num_experts + 64) * sizeof(int);
+    if (cudaFuncSetAttribute(moe::route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    moe_mxfp4_handle* h = new (std::nothrow) moe_mxfp4_handle();
+    if (!h) return MOE_ERR_INVALID_ARG;
+    h->cfg = c;
+    if (h->cfg.timeout_us == 0) h->cfg.timeout_us = kDefaultTimeoutUs;
+    h->layers.assign(layers, layers + c.num_layers);
+    h->device = dev;
+    h->sm_count = prop.multiProcessorCount;
+    h->e_begin = eb;
+    h->e_end = ee;
+    *out = h;
+    return MOE_OK;
+}
+
+int moe_mxfp4_workspace_bytes(const moe_mxfp4_handle* h, int32_t num_tokens, size_t* bytes) {
+    if (!h || !bytes || num_tokens < 0 || num_tokens > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    *bytes = ws_layout(h->cfg, num_tokens).total;
+    return MOE_OK;
+}
+
+int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens, void* y_dev, void* workspace_dev,
+                      size_t workspace_bytes, void* stream, const moe_mxfp4_debug* dbg) {
+    if (!h || num_tokens < 0 || num_tokens > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (num_tokens == 0) return MOE_OK;
+    if (!x_dev || !y_dev || !aligned16(x_dev) || !aligned16(y_dev)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(h->cfg, num_tokens);
+    if (!workspace_dev || (reinterpret_cast<uintptr_t>(workspace_dev) % kAlign) || workspace_bytes < L.total)
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace_dev);
+    if (cudaMemsetAsync(ws + L.status, 0, 64, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return forward_multi_kernel(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
+}
+
+int moe_mxfp4_forward_host(moe_mxfp4_handle* h, const void* x_host, int32_t num_tokens, void* y_host,
+                           void* workspace_dev, size_t workspace_bytes, void* stream) {
+    if (!h || num_tokens < 0 || num_tokens > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (num_tokens == 0) return MOE_OK;
+    if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(h->cfg, num_tokens);
+    if (!workspace_dev || (reinterpret_cast<uintptr_t>(workspace_dev) % kAlign) || workspace_bytes < L.total)
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace_dev);
+    const size_t xb = (size_t)num_tokens * h->cfg.hidden * 2;
+    const size_t yb = (size_t)num_tokens * h->cfg.hidden * ((h->cfg.flags & MOE_FLAG_OUT_BF16) ? 2 : 4);
+    if (cudaMemcpyAsync(ws + L.xstage, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) return MOE_ERR_CUDA;
+    const int r = moe_mxfp4_forward(h, ws + L.xstage, num_tokens, ws + L.ystage, workspace_dev, workspace_bytes,
+                                    stream, nullptr);
+    if (r != MOE_OK) return r;
+    if (cudaMemcpyAsync(y_host, ws + L.ystage, yb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return moe_mxfp4_check(h, workspace_dev, stream);
+}
+
+int moe_mxfp4_check(moe_mxfp4_handle* h, const void* workspace_dev, void* stream) {
+    if (!h || !workspace_dev) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    int s[2] = {0, 0};
+    if (cudaMemcpy(s, workspace_dev, sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    return s[0];
+}
+
+void moe_mxfp4_destroy(moe_mxfp4_handle* h) { delete h; }
+
+}  // extern "C"

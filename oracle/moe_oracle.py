@@ -119,12 +119,12 @@ def quantize(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     rows, cols = w.shape
     assert cols % MX_BLOCK == 0
     blocks = w.reshape(rows, cols // MX_BLOCK, MX_BLOCK).astype(np.float64)
-    amax = np.abs(blocks).max(axis=2)
+    amax = np.fabs(blocks).max(axis=2)
     _, ex = np.frexp(amax)                       # amax = m * 2^ex, m in [0.5, 1)
     byte = np.clip(ex - 1 - 2 + 127, 0, 254)
     byte = np.where(amax == 0, 127, byte).astype(np.int64)
     v = blocks / np.ldexp(1.0, byte - 127)[..., None]
-    mag = _round_e2m1_magnitude(np.abs(v))
+    mag = _round_e2m1_magnitude(np.fabs(v))
     sign = np.signbit(blocks).astype(np.uint8)
     codes = (sign << 3 | mag).reshape(rows, cols)
     q = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)

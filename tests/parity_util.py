@@ -1,0 +1,81 @@
+"""Helpers shared by the parity tests: oracle inputs from the seeded generator,
+and the tolerance of the layer output.
+
+Tolerance (stated by the workload definition): per token row, relative L2
+error <= 5e-3 and max abs error <= 1e-2 * rms(reference row), against the fp64
+oracle.  Routing indices and the token-expert grouping are compared bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from mxfp4_moe_expert_gb300.synth import Inputs, Workload, expert_weight
+from oracle import moe_oracle as O
+
+REL_L2 = 5e-3
+MAX_ABS_RMS = 1e-2
+
+
+def bf16_np(t: torch.Tensor) -> np.ndarray:
+    return O.bf16_to_f64(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def assert_rows_close(got: np.ndarray, ref: np.ndarray, rows=None, what=""):
+    rows = range(ref.shape[0]) if rows is None else rows
+    worst = (0.0, 0.0)
+    for t in rows:
+        r = ref[t]
+        g = got[t]
+        nrm = np.linalg.norm(r)
+        rms = nrm / np.sqrt(r.size)
+        rel = np.linalg.norm(g - r) / nrm if nrm > 0 else np.linalg.norm(g)
+        mx = np.max(np.fabs(g - r)) / rms if rms > 0 else np.max(np.fabs(g))
+        worst = (max(worst[0], rel), max(worst[1], mx))
+        assert rel <= REL_L2, f"{what} row {t}: rel L2 {rel:.3e}"
+        assert mx <= MAX_ABS_RMS, f"{what} row {t}: max abs / rms {mx:.3e}"
+    return worst
+
+
+class OracleExperts:
+    """Oracle-side experts of one layer: each routed expert's fp32 master weights
+    are redrawn by the generator (on `weights_device`, the device the GPU side
+    drew them on) and MXFP4-encoded by the oracle's own quantizer."""
+
+    def __init__(self, wl: Workload, layer: int, weights_device="cpu", check_against=None):
+        self.wl, self.layer, self.dev = wl, layer, weights_device
+        self.check = check_against  # optional device layer dict: its bytes must equal the oracle's
+        self.cache = {}
+
+    def quantized(self, e: int):
+        if e not in self.cache:
+            out = {}
+            for m in ("gate", "up", "down"):
+                w = expert_weight(self.wl, self.layer, e, m, self.dev).cpu().numpy()
+                q, s = O.quantize(w)
+                if self.check is not None:
+                    assert np.array_equal(self.check[m + "_q"][e].cpu().numpy(), q), (m, e)
+                    assert np.array_equal(self.check[m + "_s"][e].cpu().numpy(), s), (m, e)
+                out[m] = (q, s)
+            self.cache[e] = out
+        return self.cache[e]
+
+    def __call__(self, e: int) -> O.ExpertMatrices:
+        d = self.quantized(e)
+        return O.ExpertMatrices(*d["gate"], *d["up"], *d["down"])
+
+
+def oracle_quantizer_to(device):
+    """Quantizer for device_layers that uses the oracle (CPU) and uploads the bytes."""
+    def qz(w):
+        q, s = O.quantize(w.cpu().numpy())
+        return torch.from_numpy(q).to(device), torch.from_numpy(s).to(device)
+    return qz
+
+
+def oracle_layer_args(inputs: Inputs, layer: int):
+    L = inputs.layers[layer]
+    wr = bf16_np(L.router_w)
+    b = L.router_b.double().numpy()
+    nw = bf16_np(L.norm_w) if L.norm_w is not None else None
+    return wr, b, nw

@@ -1,0 +1,57 @@
+"""The C-ABI library builds, loads, and exports every function include/*.h declares (CPU only)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import mxfp4_moe_expert_gb300 as pkg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(moe_mxfp4_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    if not os.path.exists(pkg.LIB_PATH):
+        from mxfp4_moe_expert_gb300 import build
+        build.build()
+    return pkg.LIB_PATH
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert {"moe_mxfp4_create", "moe_mxfp4_forward", "moe_mxfp4_destroy"} <= names
+    assert names == set(pkg.EXPORTED), names ^ set(pkg.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_host_side_validation(lib_path):
+    pkg.load_library(lib_path)
+    assert pkg.moe_mxfp4_status_string(pkg.MOE_OK) == "ok"
+    assert "workspace" in pkg.moe_mxfp4_status_string(pkg.MOE_ERR_WORKSPACE)
+    # argument checks that return before touching a device
+    st, h = pkg.moe_mxfp4_create(pkg.moe_mxfp4_config(0, 256, 128, 8, 2, 8, 1e-6, 0, 0, 0, 0, 0), [pkg.moe_mxfp4_layer()])
+    assert st == pkg.MOE_ERR_INVALID_ARG and not h
+    st, h = pkg.moe_mxfp4_create(pkg.moe_mxfp4_config(1, 200, 128, 8, 2, 8, 1e-6, 0, 0, 0, 0, 0), [pkg.moe_mxfp4_layer()])
+    assert st == pkg.MOE_ERR_INVALID_ARG
+    st, h = pkg.moe_mxfp4_create(pkg.moe_mxfp4_config(1, 256, 128, 8, 9, 8, 1e-6, 0, 0, 0, 0, 0), [pkg.moe_mxfp4_layer()])
+    assert st == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_quantize(None, 1, 32, None, None, None) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_forward(None, None, 8, None, None, 0, None) == pkg.MOE_ERR_INVALID_ARG
+    pkg.moe_mxfp4_destroy(None)

@@ -1,0 +1,259 @@
+"""GPU parity of the CUDA path against the fp64 oracle, through the C ABI.
+
+Routing indices and the token-expert grouping must be bit-exact; each output
+row must meet rel L2 <= 5e-3 and max abs <= 1e-2 * rms(ref row).  Inputs are
+the seeded workloads; the oracle always encodes weights with its own
+quantizer (the device copy may come from the library's quantizer only after
+its bytes are shown equal to the oracle's).
+"""
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_moe_expert_gb300 as pkg
+from mxfp4_moe_expert_gb300.synth import WORKLOADS, Workload, expert_weight, make_inputs
+from mxfp4_moe_expert_gb300.workload import device_layers
+from oracle import moe_oracle as O
+from parity_util import (OracleExperts, assert_rows_close, bf16_np, oracle_layer_args, oracle_quantizer_to)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import os
+    if not os.path.exists(pkg.LIB_PATH):
+        from mxfp4_moe_expert_gb300 import build
+        build.build()
+    pkg.load_library()
+
+
+def _moe(wl, layers, flags=0, **kw):
+    if wl.norm:
+        flags |= pkg.MOE_FLAG_NORM
+    return pkg.MoeLayers(hidden=wl.H, inter=wl.I, num_experts=wl.E, top_k=wl.k, max_tokens=wl.T,
+                         layers=layers, flags=flags, rms_eps=wl.rms_eps, **kw)
+
+
+def _run(moe, x, T=None):
+    T = x.shape[0] if T is None else T
+    bufs, dbg = moe.debug_buffers(T)
+    y = moe.forward(x, dbg=dbg, check=True)
+    torch.cuda.synchronize()
+    return y, {k: v.cpu().numpy() for k, v in bufs.items()}
+
+
+def _check_routing(dbgl, ref, what=""):
+    assert np.array_equal(dbgl["idx"], ref["idx"]), what
+    assert np.array_equal(dbgl["counts"], ref["counts"]), what
+    assert np.array_equal(dbgl["offsets"], ref["offsets"]), what
+    assert np.array_equal(dbgl["perm"], ref["perm"]), what
+    assert np.allclose(dbgl["gate"], ref["gate"], rtol=1e-5, atol=1e-6), what
+
+
+def _dbg_layer(bufs, l):
+    return dict(idx=bufs["topk_idx"][l], gate=bufs["topk_gate"][l], counts=bufs["expert_counts"][l],
+                offsets=bufs["expert_offsets"][l], perm=bufs["perm"][l])
+
+
+# ----------------------------------------------------------------------------- quantizer
+
+
+def test_quantize_kernel_bit_exact():
+    g = torch.Generator().manual_seed(11)
+    w = torch.randn((96, 1024), generator=g) * torch.exp2(torch.randint(-30, 30, (96, 1), generator=g).float())
+    w[0, :32] = 0.0
+    w[1, :32] = -0.0
+    w[2, :32] = torch.tensor([4.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0] * 4) * torch.tensor([1.0, -1.0] * 16)
+    w[3, :32] = 1e-42                         # subnormal block
+    w[4, :32] = 3.0e38                        # near the fp32 maximum
+    w[5, 0] = 7.99
+    q_ref, s_ref = O.quantize(w.numpy())
+    q, s = pkg.quantize(w.to(DEV))
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+def test_quantize_kernel_matches_oracle_on_expert_weights():
+    wl = WORKLOADS["mid"]
+    w = expert_weight(wl, 0, 5, "down", DEV)
+    q, s = pkg.quantize(w)
+    q_ref, s_ref = O.quantize(w.cpu().numpy())
+    assert np.array_equal(q.cpu().numpy(), q_ref) and np.array_equal(s.cpu().numpy(), s_ref)
+
+
+# ----------------------------------------------------------------------------- full oracle, small shapes
+
+
+SMALL = [
+    WORKLOADS["tiny"],
+    Workload("ragged", T=13, H=1024, I=384, E=16, k=4, seed=0x5EED0100),
+    Workload("top1", T=5, H=512, I=256, E=6, k=1, seed=0x5EED0101),
+    Workload("k_eq_E", T=3, H=256, I=128, E=4, k=4, seed=0x5EED0102),
+    Workload("one_token", T=1, H=768, I=512, E=32, k=8, seed=0x5EED0103),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_layer_parity_full_oracle(wl):
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    moe = _moe(wl, layers)
+    y, bufs = _run(moe, inputs.x.to(DEV))
+    wr, b, _ = oracle_layer_args(inputs, 0)
+    ref = O.moe_layer(bf16_np(inputs.x), wr, b, wl.k, OracleExperts(wl, 0, "cpu"))
+    _check_routing(_dbg_layer(bufs, 0), ref, wl.name)
+    assert_rows_close(y.double().cpu().numpy(), ref["y"], what=wl.name)
+    moe.close()
+
+
+def test_stack_parity_small():
+    wl = Workload("stack_small", T=6, H=512, I=256, E=12, k=3, layers=4, norm=True, seed=0x5EED0104)
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    moe = _moe(wl, layers)
+    y, bufs = _run(moe, inputs.x.to(DEV))
+    L = []
+    for l in range(wl.layers):
+        wr, b, nw = oracle_layer_args(inputs, l)
+        L.append(dict(wr=wr, b=b, norm_w=nw, expert_fn=OracleExperts(wl, l, "cpu")))
+    ref = O.moe_stack(bf16_np(inputs.x), L, wl.k, wl.rms_eps)
+    for l in range(wl.layers):
+        margins = [O.topk_margin(ref["layers"][l]["logits"][t], wl.k) for t in range(wl.T)]
+        assert min(margins) > 1e-5, (l, min(margins))
+        _check_routing(_dbg_layer(bufs, l), ref["layers"][l], f"layer {l}")
+    assert_rows_close(y.double().cpu().numpy(), ref["y"], what="stack")
+    moe.close()
+
+
+def test_bf16_output_and_host_entry_point():
+    wl = SMALL[1]
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    moe32 = _moe(wl, layers)
+    y32 = moe32.forward(inputs.x.to(DEV), check=True)
+    moe16 = _moe(wl, layers, flags=pkg.MOE_FLAG_OUT_BF16)
+    y16 = moe16.forward(inputs.x.to(DEV), check=True)
+    assert y16.dtype == torch.bfloat16
+    assert torch.equal(y16, y32.to(torch.bfloat16))
+    ws = moe32.new_workspace(wl.T)
+    xh = inputs.x.clone().pin_memory()
+    yh = torch.empty((wl.T, wl.H), dtype=torch.float32).pin_memory()
+    moe32.forward_host(xh, yh, ws)
+    assert torch.equal(yh, y32.cpu())
+    moe32.close()
+    moe16.close()
+
+
+def test_expert_shards_sum_to_full_layer():
+    wl = SMALL[1]
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    x = inputs.x.to(DEV)
+    full = _moe(wl, layers).forward(x, check=True)
+    parts = [_moe(wl, layers, expert_begin=b, expert_end=e).forward(x, check=True) for b, e in ((0, 5), (5, 11), (11, 16))]
+    total = parts[0].double() + parts[1].double() + parts[2].double()
+    assert_rows_close(total.cpu().numpy(), full.double().cpu().numpy(), what="shards")
+
+
+def test_down_scale_plus_one_doubles_output_exactly():
+    wl = SMALL[0]
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    x = inputs.x.to(DEV)
+    y1 = _moe(wl, layers).forward(x, check=True)
+    L2 = dict(layers[0])
+    L2["down_s"] = layers[0]["down_s"] + 1
+    y2 = _moe(wl, [L2]).forward(x, check=True)
+    assert torch.equal(y2, 2 * y1)
+
+
+def test_nan_scale_of_a_routed_expert_is_reported():
+    wl = SMALL[0]
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    moe = _moe(wl, layers)
+    bufs, dbg = moe.debug_buffers(wl.T)
+    moe.forward(inputs.x.to(DEV), dbg=dbg, check=True)
+    e = int(bufs["topk_idx"][0, 0, 0])
+    L2 = dict(layers[0])
+    L2["up_s"] = layers[0]["up_s"].clone()
+    L2["up_s"][e, 3, 1] = 0xFF
+    bad = _moe(wl, [L2])
+    with pytest.raises(pkg.MoeError) as ei:
+        bad.forward(inputs.x.to(DEV), check=True)
+    assert ei.value.status == pkg.MOE_ERR_BAD_SCALE
+
+
+def test_empty_and_invalid_calls():
+    wl = SMALL[0]
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    moe = _moe(wl, layers)
+    ws = moe.new_workspace(wl.T)
+    st = torch.cuda.current_stream().cuda_stream
+    x = inputs.x.to(DEV)
+    y = torch.zeros((wl.T, wl.H), device=DEV)
+    assert pkg.moe_mxfp4_forward(moe.handle, x.data_ptr(), 0, y.data_ptr(), ws.data_ptr(), ws.numel(), st) == 0
+    assert pkg.moe_mxfp4_forward(moe.handle, x.data_ptr(), wl.T + 1, y.data_ptr(), ws.data_ptr(), ws.numel(),
+                                 st) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_forward(moe.handle, x.data_ptr(), wl.T, y.data_ptr(), ws.data_ptr(), ws.numel() - 256,
+                                 st) == pkg.MOE_ERR_WORKSPACE
+    assert pkg.moe_mxfp4_forward(moe.handle, x.data_ptr(), wl.T, y.data_ptr(), ws.data_ptr() + 16, ws.numel() - 256,
+                                 st) == pkg.MOE_ERR_WORKSPACE
+    L2 = dict(layers[0])
+    L2["gate_q"] = torch.empty(wl.E * wl.I * wl.H // 2 + 16, dtype=torch.uint8, device=DEV)[8:]
+    with pytest.raises(pkg.MoeError):
+        _moe(wl, [L2])
+    moe.close()
+
+
+# ----------------------------------------------------------------------------- full sizes, sampled tokens
+
+
+def _full_size(name, sample_tokens):
+    wl = WORKLOADS[name]
+    inputs, layers = device_layers(wl, device=DEV)          # library quantizer, weights drawn on the GPU
+    moe = _moe(wl, layers)
+    y, bufs = _run(moe, inputs.x.to(DEV))
+    got = y.double().cpu().numpy()
+    xf = bf16_np(inputs.x)
+    if not wl.norm:
+        wr, b, _ = oracle_layer_args(inputs, 0)
+        logits = O.router_logits(xf, wr, b)
+        idx, gate = O.topk_gates(logits, wl.k)
+        counts, offsets, perm = O.assignment(idx, wl.E)
+        _check_routing(_dbg_layer(bufs, 0), dict(idx=idx, gate=gate, counts=counts, offsets=offsets, perm=perm),
+                       name)
+        experts = OracleExperts(wl, 0, DEV, check_against=layers[0])
+        for t in sample_tokens:
+            r = O.moe_token(xf[t], wr, b, wl.k, experts)
+            assert_rows_close(got[t:t + 1], r["y"][None], what=f"{name} token {t}")
+    else:
+        L = []
+        for l in range(wl.layers):
+            wr, b, nw = oracle_layer_args(inputs, l)
+            L.append(dict(wr=wr, b=b, norm_w=nw, expert_fn=OracleExperts(wl, l, DEV, check_against=layers[l])))
+        for t in sample_tokens:   # the stack is per token: one token's trajectory needs k experts per layer
+            ref = O.moe_stack(xf[t:t + 1], L, wl.k, wl.rms_eps)
+            for l in range(wl.layers):
+                lr = ref["layers"][l]
+                assert O.topk_margin(lr["logits"][0], wl.k) > 1e-5
+                assert np.array_equal(bufs["topk_idx"][l, t], lr["idx"][0]), (l, t)
+            assert_rows_close(got[t:t + 1], ref["y"], what=f"{name} token {t}")
+    moe.close()
+    del layers
+    torch.cuda.empty_cache()
+
+
+def test_mid_layer_sampled():
+    _full_size("mid", [0, 3, 7])
+
+
+def test_large_layer_sampled():
+    _full_size("large", [2, 6])
+
+
+def test_batched_layer_sampled():
+    _full_size("batched", [0, 131, 255])
+
+
+def test_stack_sampled():
+    _full_size("stack", [1, 6])
