@@ -244,16 +244,16 @@ def _full_size(name, sample_tokens):
 
 
 def test_mid_layer_sampled():
-    _full_size("mid", [0, 3, 7])
+    _full_size("mid", [0, 7])
 
 
 def test_large_layer_sampled():
-    _full_size("large", [2, 6])
+    _full_size("large", [2])
 
 
 def test_batched_layer_sampled():
-    _full_size("batched", [0, 131, 255])
+    _full_size("batched", [0, 255])
 
 
 def test_stack_sampled():
-    _full_size("stack", [1, 6])
+    _full_size("stack", [1])
