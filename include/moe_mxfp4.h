@@ -154,6 +154,29 @@ void moe_mxfp4_destroy(moe_mxfp4_handle* h);
 /* Static description of a status code. */
 const char* moe_mxfp4_status_string(int status);
 
+/* Allocation-free forward.  The pages have no counterpart to this call; it exists for
+ * callers that cannot allocate device memory at the point where they run the layer --
+ * for example a host program that reserved all of HBM up front for its own pool, a
+ * plugin inside a framework that owns every device allocation, or a latency-bound loop
+ * that cannot afford cudaMalloc's device-wide synchronisation.
+ * It runs exactly moe_mxfp4_forward, but its workspace is a fixed static array inside
+ * this library (MOE_MXFP4_STATIC_WORKSPACE_BYTES = 16 MiB per GPU, held from the moment
+ * the library's device code is loaded until the process exits) instead of caller memory.
+ * The caller still provides x_dev and y_dev (device memory, as for moe_mxfp4_forward).
+ *  - Returns MOE_ERR_WORKSPACE, and runs nothing, when num_tokens needs more workspace
+ *    than the static array holds (moe_mxfp4_workspace_bytes tells the need).
+ *  - The first call on a device, with that device current, looks up the array's device
+ *    address (once per device); make that first call before any stream capture.
+ *  - All calls on a device share the one array and leave their contents in it; the
+ *    forward re-initialises everything it needs.  Calls whose work overlaps on the GPU
+ *    (different streams, or different handles at the same time) race on the array.
+ *  - Never calls cudaMalloc, cudaFree or any other allocating routine.
+ *  - Synchronises the stream before it returns and returns the device status of the
+ *    call (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_BAD_SCALE), like moe_mxfp4_check. */
+#define MOE_MXFP4_STATIC_WORKSPACE_BYTES (16u << 20)
+int moe_mxfp4_forward_static(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens, void* y_dev,
+                             void* stream);
+
 /* MXFP4 conversion of an fp32 matrix w_dev [rows, cols] (cols a multiple of 32)
  * into nibbles q_dev [rows, cols/2] and E8M0 scales s_dev [rows, cols/32], by the
  * OCP MX v1.0 rule: per block of 32, X = 2^(floor(log2 amax) - 2) (byte clamped to

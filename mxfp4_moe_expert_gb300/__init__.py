@@ -36,7 +36,10 @@ EXPORTED = (
     "moe_mxfp4_destroy",
     "moe_mxfp4_status_string",
     "moe_mxfp4_quantize",
+    "moe_mxfp4_forward_static",
 )
+
+MOE_MXFP4_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
 class moe_mxfp4_config(ctypes.Structure):
@@ -111,6 +114,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_mxfp4_status_string.restype = ctypes.c_char_p
     lib.moe_mxfp4_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, P, P]
     lib.moe_mxfp4_quantize.restype = ctypes.c_int
+    lib.moe_mxfp4_forward_static.argtypes = [P, P, ctypes.c_int32, P, P]
+    lib.moe_mxfp4_forward_static.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -169,6 +174,12 @@ def moe_mxfp4_destroy(handle) -> None:
 
 def moe_mxfp4_quantize(w_ptr, rows, cols, q_ptr, s_ptr, stream_ptr) -> int:
     return load_library().moe_mxfp4_quantize(w_ptr, rows, cols, q_ptr, s_ptr, stream_ptr)
+
+
+def moe_mxfp4_forward_static(handle, x_ptr, num_tokens, y_ptr, stream_ptr) -> int:
+    """Forward with the library's own static workspace (no device allocation
+    anywhere); synchronises the stream and returns the device status."""
+    return load_library().moe_mxfp4_forward_static(handle, x_ptr, num_tokens, y_ptr, stream_ptr)
 
 
 # ----------------------------------------------------------------------------- torch convenience

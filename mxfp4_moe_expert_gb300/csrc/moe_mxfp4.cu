@@ -254,3 +254,42 @@ int moe_mxfp4_check(moe_mxfp4_handle* h, const void* workspace_dev, void* stream
 void moe_mxfp4_destroy(moe_mxfp4_handle* h) { delete h; }
 
 }  // extern "C"
+
+// ---- allocation-free forward ---------------------------------------------------
+// For callers that may not allocate device memory when they run the layer: the
+// workspace lives in this file-scope array, one per GPU that loads the library.
+// Host code must not use the array's name as a pointer (on the host it only
+// stands for the symbol); its device address is looked up once per device.
+#include <mutex>
+
+namespace {
+static __device__ __align__(256) unsigned char g_static_workspace[MOE_MXFP4_STATIC_WORKSPACE_BYTES];
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxStaticDevices] = {};
+}  // namespace
+
+extern "C" int moe_mxfp4_forward_static(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens, void* y_dev,
+                                        void* stream) {
+    if (!h || num_tokens < 0 || num_tokens > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (num_tokens == 0) return MOE_OK;
+    if (ws_layout(h->cfg, num_tokens).total > MOE_MXFP4_STATIC_WORKSPACE_BYTES) return MOE_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev != h->device) return MOE_ERR_INVALID_ARG;
+    if (dev < 0 || dev >= kMaxStaticDevices) return MOE_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (!g_static_ptr[dev]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return MOE_ERR_CUDA;
+            g_static_ptr[dev] = p;
+        }
+        ws = g_static_ptr[dev];
+    }
+    const int r = moe_mxfp4_forward(h, x_dev, num_tokens, y_dev, ws, MOE_MXFP4_STATIC_WORKSPACE_BYTES, stream,
+                                    nullptr);
+    if (r != MOE_OK) return r;
+    return moe_mxfp4_check(h, ws, stream);
+}
