@@ -111,13 +111,18 @@ typedef struct {
  * pointers are non-NULL (device memory, caller-owned):
  *   topk_idx int32 [L, T, k], topk_gate fp32 [L, T, k], expert_counts int32 [L, E],
  *   expert_offsets int32 [L, E+1], perm int32 [L, T*k] (pair ids t*k+j grouped by
- *   expert, ascending by (t, j) inside an expert). */
+ *   expert, ascending by (t, j) inside an expert).
+ * expert_events, when non-NULL, points to 2*L cudaEvent_t handles (host array,
+ * caller-created): the forward records events[2l] on the stream right before the
+ * expert kernel of layer l and events[2l+1] right after it, so a caller can time
+ * that kernel alone. */
 typedef struct {
     int32_t* topk_idx_dev;
     float* topk_gate_dev;
     int32_t* expert_counts_dev;
     int32_t* expert_offsets_dev;
     int32_t* perm_dev;
+    void* const* expert_events;
 } moe_mxfp4_debug;
 
 /* Validates the config and the layer pointers (alignment, device), and checks

@@ -80,6 +80,7 @@ class moe_mxfp4_debug(ctypes.Structure):
         ("expert_counts_dev", ctypes.c_void_p),
         ("expert_offsets_dev", ctypes.c_void_p),
         ("perm_dev", ctypes.c_void_p),
+        ("expert_events", ctypes.c_void_p),
     ]
 
 
@@ -242,8 +243,16 @@ class MoeLayers:
                     expert_counts=torch.zeros((L, E), **i32), expert_offsets=torch.zeros((L, E + 1), **i32),
                     perm=torch.full((L, T * k), -1, **i32))
         dbg = moe_mxfp4_debug(*(bufs[n].data_ptr() for n in
-                                ("topk_idx", "topk_gate", "expert_counts", "expert_offsets", "perm")))
+                                ("topk_idx", "topk_gate", "expert_counts", "expert_offsets", "perm")), None)
         return bufs, dbg
+
+    def expert_timing(self, events):
+        """A debug descriptor that only records `events` (2 per layer, torch.cuda.Event
+        created with enable_timing) around each layer's expert kernel."""
+        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        dbg = moe_mxfp4_debug(None, None, None, None, None, ctypes.cast(arr, ctypes.c_void_p))
+        dbg._events_keepalive = arr
+        return dbg
 
     def forward(self, x, y=None, workspace=None, stream=None, dbg=None, check=False):
         """x: bf16 CUDA [T, H].  Returns y (fp32, or bf16 with MOE_FLAG_OUT_BF16)."""

@@ -8,14 +8,19 @@
 #include <new>
 #include <vector>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "expert_simple.cuh"
+#include "expert_tma.cuh"
 #include "layer_ops.cuh"
 #include "route.cuh"
 
 struct moe_mxfp4_handle {
     moe_mxfp4_config cfg;
     std::vector<moe_mxfp4_layer> layers;
+    std::vector<moe::TmaMaps> maps;   // per layer, when the TMA expert path applies
+    bool tma = false;
     int device = 0;
     int sm_count = 0;
     int e_begin = 0, e_end = 0;
@@ -30,8 +35,17 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 // Byte offsets of the workspace sections for T tokens.
 struct WsLayout {
-    size_t status, xstage, ystage, act, resid, logits, idx, gate, counts, offsets, perm, active, hbuf, partial, total;
+    size_t status, xstage, ystage, act, resid, logits, idx, gate, counts, offsets, perm, active, hbuf, partial;
+    size_t act16, act_scale, h16, h_scale, items, sync, rpart, total;
 };
+
+// Upper bound of the work items of one layer: every routed expert contributes
+// ceil(n_e / 8) token chunks, i.e. at most T*k/8 + min(E, T*k) chunks.
+size_t max_items(const moe_mxfp4_config& c, int T) {
+    const size_t pairs = (size_t)T * c.top_k;
+    const size_t chunks = (pairs + moe::kTmaTok - 1) / moe::kTmaTok + std::min<size_t>(c.num_experts, pairs);
+    return chunks * (size_t)(c.inter / moe::kTmaRows + c.hidden / moe::kTmaRows);
+}
 
 WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     WsLayout L{};
@@ -52,6 +66,13 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     L.active = take((E + 1) * 4);
     L.hbuf = take((size_t)T * k * I * 4);
     L.partial = take((size_t)T * k * H * 4);
+    L.act16 = take((size_t)T * H * 2);
+    L.act_scale = take((size_t)T * 4);
+    L.h16 = take((size_t)T * k * I * 2);
+    L.h_scale = take((size_t)T * k * (I / 128) * 4);
+    L.items = take(max_items(c, T) * sizeof(moe::ItemRec));
+    L.sync = take((8 + 2 * E) * 4);   // n_items[2], queue, abort, ..., done[E], need[E]
+    L.rpart = take((size_t)(H / moe::kRouteSlice + 1) * T * E * 4);   // router partials per 512-column slice
     L.total = o;
     return L;
 }
@@ -77,6 +98,42 @@ int check_layer(const moe_mxfp4_config& c, const moe_mxfp4_layer& l) {
         if (!l.norm_w_dev || !aligned16(l.norm_w_dev) || !is_device_ptr(l.norm_w_dev)) return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2D uint8 tensor [rows, row_bytes] with boxes of box_x bytes x 128 rows.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_x, bool swizzle) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {row_bytes, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_x, (cuuint32_t)moe::kTmaRows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_maps(const moe_mxfp4_config& c, const moe_mxfp4_layer& l, moe::TmaMaps* m) {
+    const uint64_t H = c.hidden, I = c.inter, E = c.num_experts;
+    return encode_2d(&m->gate_q, l.gate_q_dev, H / 2, E * I, 128, true) &&
+           encode_2d(&m->up_q, l.up_q_dev, H / 2, E * I, 128, true) &&
+           encode_2d(&m->down_q, l.down_q_dev, I / 2, E * H, 128, true) &&
+           encode_2d(&m->gate_s, l.gate_s_dev, H / 32, E * I, 16, false) &&
+           encode_2d(&m->up_s, l.up_s_dev, H / 32, E * I, 16, false) &&
+           encode_2d(&m->down_s, l.down_s_dev, I / 32, E * H, 16, false);
 }
 
 moe::RouteBufs route_bufs(char* ws, const WsLayout& L) {
@@ -132,10 +189,72 @@ int forward_multi_kernel(moe_mxfp4_handle* h, const void* x, int T, void* y, cha
             act, T, H, reinterpret_cast<const __nv_bfloat16*>(ly.router_w_dev), ly.router_b_dev, E, rb.logits);
         moe::route_select_kernel<<<1, 1024, sel_smem, st>>>(rb.logits, T, E, k, h->e_begin, h->e_end, rb);
         const moe::ExpertWeights w{ly.gate_q_dev, ly.gate_s_dev, ly.up_q_dev, ly.up_s_dev, ly.down_q_dev, ly.down_s_dev};
+        if (dbg && dbg->expert_events) cudaEventRecord(static_cast<cudaEvent_t>(dbg->expert_events[2 * l]), st);
         moe::gateup_simple_kernel<<<dim3(I / 32, max_active), 256, 0, st>>>(act, H, I, k, w, rb, hbuf, status, l);
         moe::down_simple_kernel<<<dim3(H / 32, max_active), 256, 0, st>>>(hbuf, H, I, w, rb, partial, status, l);
+        if (dbg && dbg->expert_events) cudaEventRecord(static_cast<cudaEvent_t>(dbg->expert_events[2 * l + 1]), st);
         const bool last = l == c.num_layers - 1;
         moe::combine_kernel<<<dim3(T, (H + 1023) / 1024), 256, 0, st>>>(partial, rb, H, k, h->e_begin, h->e_end,
+                                                                        resid, last ? y : nullptr, y_bf16);
+        copy_debug(dbg, l, T, E, k, rb, st);
+    }
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Forward with the warp-specialised TMA expert kernel: per layer, routing and
+// grouping kernels, the work list, one persistent expert launch, the combine.
+int forward_tma(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, const WsLayout& L, cudaStream_t st,
+                const moe_mxfp4_debug* dbg) {
+    const moe_mxfp4_config& c = h->cfg;
+    const int H = c.hidden, I = c.inter, E = c.num_experts, k = c.top_k;
+    const bool norm = (c.flags & MOE_FLAG_NORM) != 0;
+    const int y_bf16 = (c.flags & MOE_FLAG_OUT_BF16) ? 1 : 0;
+    int* status = reinterpret_cast<int*>(ws + L.status);
+    float* act = reinterpret_cast<float*>(ws + L.act);
+    float* resid = norm ? reinterpret_cast<float*>(ws + L.resid) : nullptr;
+    const moe::RouteBufs rb = route_bufs(ws, L);
+    int* sync = reinterpret_cast<int*>(ws + L.sync);
+    moe::WorkList wl;
+    wl.items = reinterpret_cast<moe::ItemRec*>(ws + L.items);
+    wl.n_items = sync;
+    wl.queue = sync + 2;
+    wl.abort = sync + 3;
+    wl.done = sync + 8;
+    wl.need = sync + 8 + E;
+    moe::ExpertArgs ea;
+    ea.H = H; ea.I = I; ea.k = k;
+    ea.act16 = reinterpret_cast<const __half*>(ws + L.act16);
+    ea.act_scale = reinterpret_cast<const float*>(ws + L.act_scale);
+    ea.h16 = reinterpret_cast<__half*>(ws + L.h16);
+    ea.h_scale = reinterpret_cast<float*>(ws + L.h_scale);
+    ea.partial = reinterpret_cast<float*>(ws + L.partial);
+    ea.rb = rb;
+    ea.wl = wl;
+    ea.status = status;
+    ea.timeout_ns = (unsigned long long)c.timeout_us * 1000ull;
+    const size_t sel_smem = (size_t)(33 * E + 64) * sizeof(int);
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+    if (norm)   // r_0 = x
+        moe::prep_layer_kernel<<<T, moe::kPrepThreads, 0, st>>>(xb, H, resid, nullptr, 0.0f, act,
+                                                                const_cast<__half*>(ea.act16),
+                                                                const_cast<float*>(ea.act_scale));
+    for (int l = 0; l < c.num_layers; ++l) {
+        const moe_mxfp4_layer& ly = h->layers[l];
+        moe::prep_layer_kernel<<<T, moe::kPrepThreads, 0, st>>>(
+            xb, H, resid, norm ? reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev) : nullptr, c.rms_eps, act,
+            const_cast<__half*>(ea.act16), const_cast<float*>(ea.act_scale));
+        float* rpart = reinterpret_cast<float*>(ws + L.rpart);
+        moe::route_partial_kernel<<<dim3((E + 31) / 32, H / moe::kRouteSlice), 256, 0, st>>>(
+            act, T, H, reinterpret_cast<const __nv_bfloat16*>(ly.router_w_dev), E, rpart);
+        moe::route_select_kernel<<<1, 1024, sel_smem, st>>>(rb.logits, T, E, k, h->e_begin, h->e_end, rb, rpart,
+                                                             H / moe::kRouteSlice, ly.router_b_dev);
+        moe::build_items_kernel<<<1, 1024, 0, st>>>(rb, H, I, k, wl);
+        ea.layer = l;
+        if (dbg && dbg->expert_events) cudaEventRecord(static_cast<cudaEvent_t>(dbg->expert_events[2 * l]), st);
+        moe::expert_tma_kernel<<<h->sm_count, moe::kTmaThreads, moe::kTmaSmemBytes, st>>>(h->maps[l], ea);
+        if (dbg && dbg->expert_events) cudaEventRecord(static_cast<cudaEvent_t>(dbg->expert_events[2 * l + 1]), st);
+        const bool last = l == c.num_layers - 1;
+        moe::combine_kernel<<<dim3(T, (H + 1023) / 1024), 256, 0, st>>>(ea.partial, rb, H, k, h->e_begin, h->e_end,
                                                                         resid, last ? y : nullptr, y_bf16);
         copy_debug(dbg, l, T, E, k, rb, st);
     }
@@ -191,6 +310,18 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
 
     moe_mxfp4_handle* h = new (std::nothrow) moe_mxfp4_handle();
     if (!h) return MOE_ERR_INVALID_ARG;
+    // the TMA expert path takes K = H and K = I in whole 512-element stages
+    // (which also makes every scale row a multiple of 16 bytes)
+    h->tma = (c.hidden % moe::kTmaKC == 0) && (c.inter % moe::kTmaKC == 0) && !(c.flags & MOE_FLAG_MULTI_KERNEL);
+    if (h->tma) {
+        h->maps.resize(c.num_layers);
+        for (int l = 0; l < c.num_layers && h->tma; ++l) h->tma = make_maps(c, layers[l], &h->maps[l]);
+        if (h->tma && cudaFuncSetAttribute(moe::expert_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           moe::kTmaSmemBytes) != cudaSuccess) {
+            delete h;
+            return MOE_ERR_CUDA;
+        }
+    }
     h->cfg = c;
     if (h->cfg.timeout_us == 0) h->cfg.timeout_us = kDefaultTimeoutUs;
     h->layers.assign(layers, layers + c.num_layers);
@@ -219,6 +350,9 @@ int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace_dev);
     if (cudaMemsetAsync(ws + L.status, 0, 64, st) != cudaSuccess) return MOE_ERR_CUDA;
+    // the TMA work-item code holds up to 512 token chunks of 8 per expert
+    if (h->tma && num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok)
+        return forward_tma(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
     return forward_multi_kernel(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
 }
 

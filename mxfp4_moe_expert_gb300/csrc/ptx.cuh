@@ -110,4 +110,19 @@ __device__ __forceinline__ float fma_f16hi(uint32_t w2, uint32_t x2, float acc) 
     return r;
 }
 
+// D = A * B + C for one 16x8x16 tile: A f16 row-major 16x16 (4 regs), B f16
+// "col" 16x8 (2 regs), C/D fp32 (4 regs); products exact, fp32 accumulation.
+// Register layout (g = lane / 4, q = lane % 4): a0 (row g, k 2q..2q+1),
+// a1 (row g+8, k 2q..), a2 (row g, k 2q+8..), a3 (row g+8, k 2q+8..);
+// b0 (k 2q..2q+1, col g), b1 (k 2q+8..2q+9, col g); d0 (g, 2q), d1 (g, 2q+1),
+// d2 (g+8, 2q), d3 (g+8, 2q+1).
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                              const float (&c)[4]) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
 }  // namespace moe

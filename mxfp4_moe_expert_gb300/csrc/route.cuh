@@ -56,6 +56,70 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const float* __restri
     }
 }
 
+// Partial router logits over 512-column slices of H:
+//   partial[s, t, e] = sum_{h in slice s} act[t, h] * Wr[e, h].
+// Grid (ceil(E / 32), H / 512), 256 threads.  Each warp owns 4 expert rows and
+// keeps their 512-column slice in registers (lane l: columns 16l..16l+15); the
+// block stages the activations of 16 tokens at a time in shared memory, so each
+// weight byte and each activation byte is read once.  The slices are summed in
+// a fixed order by route_select_kernel (deterministic).
+constexpr int kRouteSlice = 512;
+constexpr int kRouteTokGroup = 16;
+__global__ void __launch_bounds__(256) route_partial_kernel(const float* __restrict__ act, int T, int H,
+                                                            const __nv_bfloat16* __restrict__ wr, int E,
+                                                            float* __restrict__ partial) {
+    __shared__ __align__(16) float xs[kRouteTokGroup][kRouteSlice];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slice = blockIdx.y;
+    const int c0 = slice * kRouteSlice + lane * 16;
+    const int e0 = blockIdx.x * 32 + warp * 4;
+    float w[4][16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int e = e0 + q;
+        if (e < E) {
+            const uint4* src = reinterpret_cast<const uint4*>(wr + (size_t)e * H + c0);
+            const uint4 a = __ldg(src), b = __ldg(src + 1);
+            const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                w[q][2 * i] = bf16_lo(v[i]);
+                w[q][2 * i + 1] = bf16_hi(v[i]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[q][i] = 0.0f;
+        }
+    }
+    for (int t0 = 0; t0 < T; t0 += kRouteTokGroup) {
+        const int nt = min(kRouteTokGroup, T - t0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < nt * (kRouteSlice / 4); i += blockDim.x) {
+            const int t = i / (kRouteSlice / 4), c = i % (kRouteSlice / 4);
+            reinterpret_cast<float4*>(xs[t])[c] =
+                __ldg(reinterpret_cast<const float4*>(act + (size_t)(t0 + t) * H + slice * kRouteSlice) + c);
+        }
+        __syncthreads();
+        for (int t = 0; t < nt; ++t) {
+            const float4* xp = reinterpret_cast<const float4*>(&xs[t][lane * 16]);
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 v = xp[i];
+                x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc = fmaf(x[i], w[q][i], acc);
+                acc = warp_sum(acc);
+                if (lane == q && e0 + q < E) partial[((size_t)slice * T + t0 + t) * E + e0 + q] = acc;
+            }
+        }
+    }
+}
+
 // (v1, e1) comes before (v2, e2) in routing order: larger logit first, then lower index.
 __device__ __forceinline__ bool route_before(float v1, int e1, float v2, int e2) {
     return v1 > v2 || (v1 == v2 && e1 < e2);
@@ -94,28 +158,50 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int* scratch) {
 // One block of 1024 threads.  Pairs routed outside [e_begin, e_end) are not
 // grouped (another shard computes them).  Dynamic shared memory:
 // (33 * E + 64) ints.
-__global__ void __launch_bounds__(1024) route_select_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                            int e_begin, int e_end, RouteBufs rb) {
+__global__ void __launch_bounds__(1024) route_select_kernel(const float* logits, int T, int E, int k,
+                                                            int e_begin, int e_end, RouteBufs rb,
+                                                            const float* __restrict__ partial = nullptr,
+                                                            int n_slices = 0, const float* __restrict__ bias = nullptr) {
     extern __shared__ int smem[];
+    if (partial) {
+        // logits = bias + sum of the slice partials, slices in ascending order
+        for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
+            float z = 0.0f;
+            for (int s = 0; s < n_slices; ++s) z += partial[(size_t)s * T * E + i];
+            rb.logits[i] = z + (bias ? bias[i % E] : 0.0f);
+        }
+        __syncthreads();
+        logits = rb.logits;
+    }
     int* cnt = smem;                 // [E]
     int* wcnt = smem + E;            // [32][E] per-warp counts, then their running prefix
     int* scratch = wcnt + 32 * E;    // [64]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     // ---- top-k + gates: one warp per token, k rounds of a warp arg-max that
-    // only admits candidates after the previous pick in routing order.
+    // only admits candidates after the previous pick in routing order.  Lane l
+    // keeps the logits of experts l, l+32, ... in registers (E <= 1024).
     for (int t = warp; t < T; t += 32) {
         const float* lrow = logits + (size_t)t * E;
+        float lv[kMaxExperts / 32];
+#pragma unroll
+        for (int i = 0; i < kMaxExperts / 32; ++i) {
+            const int e = lane + 32 * i;
+            float v = e < E ? lrow[e] : __int_as_float(0xFF800000);
+            if (v != v) v = __int_as_float(0xFF800000);  // NaN ranks last
+            lv[i] = v;
+        }
         float prev_v = __int_as_float(0x7F800000);  // +inf
         int prev_e = -1;
         float my_sel = 0.0f;
         for (int j = 0; j < k; ++j) {
             float bv = __int_as_float(0xFF800000);  // -inf
             int be = 0x7FFFFFFF;
-            for (int e = lane; e < E; e += 32) {
-                float v = lrow[e];
-                if (v != v) v = __int_as_float(0xFF800000);  // NaN ranks last
-                if (route_before(prev_v, prev_e, v, e) && route_before(v, e, bv, be)) { bv = v; be = e; }
+#pragma unroll
+            for (int i = 0; i < kMaxExperts / 32; ++i) {
+                const int e = lane + 32 * i;
+                const float v = lv[i];
+                if (e < E && route_before(prev_v, prev_e, v, e) && route_before(v, e, bv, be)) { bv = v; be = e; }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {

@@ -7,6 +7,9 @@ oracle.  Routing indices and the token-expert grouping are compared bit-exact.
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -34,6 +37,10 @@ def assert_rows_close(got: np.ndarray, ref: np.ndarray, rows=None, what=""):
         worst = (max(worst[0], rel), max(worst[1], mx))
         assert rel <= REL_L2, f"{what} row {t}: rel L2 {rel:.3e}"
         assert mx <= MAX_ABS_RMS, f"{what} row {t}: max abs / rms {mx:.3e}"
+    log = os.environ.get("MOE_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"what": what, "worst_rel_l2": worst[0], "worst_maxabs_over_rms": worst[1]}) + "\n")
     return worst
 
 

@@ -47,12 +47,20 @@ def _run(moe, x, T=None):
     return y, {k: v.cpu().numpy() for k, v in bufs.items()}
 
 
-def _check_routing(dbgl, ref, what=""):
+def _check_routing(dbgl, ref, what="", deep=False):
+    """Indices and grouping bit-exact.  Gates: a layer that sees the exact input
+    (the first) within fp32 rounding of the softmax; a deeper layer of a stack
+    sees a residual that already carries the earlier layers' output error (each
+    within the stated output tolerance), which moves its logits by ~1e-4 and its
+    gates by ~1e-5 .. 1e-4, so they are compared within 5e-4."""
     assert np.array_equal(dbgl["idx"], ref["idx"]), what
     assert np.array_equal(dbgl["counts"], ref["counts"]), what
     assert np.array_equal(dbgl["offsets"], ref["offsets"]), what
     assert np.array_equal(dbgl["perm"], ref["perm"]), what
-    assert np.allclose(dbgl["gate"], ref["gate"], rtol=1e-5, atol=1e-6), what
+    if deep:
+        assert np.allclose(dbgl["gate"], ref["gate"], rtol=0, atol=5e-4), what
+    else:
+        assert np.allclose(dbgl["gate"], ref["gate"], rtol=1e-5, atol=1e-6), what
 
 
 def _dbg_layer(bufs, l):
@@ -89,12 +97,19 @@ def test_quantize_kernel_matches_oracle_on_expert_weights():
 # ----------------------------------------------------------------------------- full oracle, small shapes
 
 
+# Shapes whose H and I are multiples of 512 run the TMA expert kernel; the others
+# run the multi-kernel path.
 SMALL = [
     WORKLOADS["tiny"],
     Workload("ragged", T=13, H=1024, I=384, E=16, k=4, seed=0x5EED0100),
     Workload("top1", T=5, H=512, I=256, E=6, k=1, seed=0x5EED0101),
     Workload("k_eq_E", T=3, H=256, I=128, E=4, k=4, seed=0x5EED0102),
     Workload("one_token", T=1, H=768, I=512, E=32, k=8, seed=0x5EED0103),
+    Workload("tma_ragged", T=13, H=1024, I=512, E=16, k=4, seed=0x5EED0110),
+    Workload("tma_top1", T=5, H=512, I=512, E=6, k=1, seed=0x5EED0111),
+    Workload("tma_k_eq_E", T=3, H=512, I=1024, E=4, k=4, seed=0x5EED0112),
+    Workload("tma_one_token", T=1, H=1536, I=512, E=32, k=8, seed=0x5EED0113),
+    Workload("tma_many_tokens", T=40, H=512, I=512, E=4, k=2, seed=0x5EED0114),
 ]
 
 
@@ -110,8 +125,11 @@ def test_layer_parity_full_oracle(wl):
     moe.close()
 
 
-def test_stack_parity_small():
-    wl = Workload("stack_small", T=6, H=512, I=256, E=12, k=3, layers=4, norm=True, seed=0x5EED0104)
+@pytest.mark.parametrize("wl", [
+    Workload("stack_small", T=6, H=512, I=256, E=12, k=3, layers=4, norm=True, seed=0x5EED0104),
+    Workload("stack_tma", T=7, H=1024, I=512, E=12, k=3, layers=3, norm=True, seed=0x5EED0115),
+], ids=lambda w: w.name)
+def test_stack_parity_small(wl):
     inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
     moe = _moe(wl, layers)
     y, bufs = _run(moe, inputs.x.to(DEV))
@@ -123,7 +141,7 @@ def test_stack_parity_small():
     for l in range(wl.layers):
         margins = [O.topk_margin(ref["layers"][l]["logits"][t], wl.k) for t in range(wl.T)]
         assert min(margins) > 1e-5, (l, min(margins))
-        _check_routing(_dbg_layer(bufs, l), ref["layers"][l], f"layer {l}")
+        _check_routing(_dbg_layer(bufs, l), ref["layers"][l], f"layer {l}", deep=l > 0)
     assert_rows_close(y.double().cpu().numpy(), ref["y"], what="stack")
     moe.close()
 
@@ -144,6 +162,15 @@ def test_bf16_output_and_host_entry_point():
     assert torch.equal(yh, y32.cpu())
     moe32.close()
     moe16.close()
+
+
+@pytest.mark.parametrize("wl", [SMALL[0], SMALL[5]], ids=lambda w: w.name)
+def test_tma_and_multi_kernel_paths_agree(wl):
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    x = inputs.x.to(DEV)
+    a = _moe(wl, layers).forward(x, check=True)
+    b = _moe(wl, layers, flags=pkg.MOE_FLAG_MULTI_KERNEL).forward(x, check=True)
+    assert_rows_close(a.double().cpu().numpy(), b.double().cpu().numpy(), what="paths")
 
 
 def test_expert_shards_sum_to_full_layer():
