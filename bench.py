@@ -176,6 +176,9 @@ def run_gpu(args):
     wl = WORKLOADS[args.workload]
     inputs, layers = device_layers(wl, device=dev)
     flags = pkg.MOE_FLAG_NORM if wl.norm else 0
+    persistent = args.path == "persistent" and moe_tma(wl)
+    if args.path == "multi":
+        flags |= pkg.MOE_FLAG_MULTI_KERNEL
     moe = pkg.MoeLayers(hidden=wl.H, inter=wl.I, num_experts=wl.E, top_k=wl.k, max_tokens=wl.T, layers=layers,
                         flags=flags, rms_eps=wl.rms_eps)
     x = inputs.x.to(dev)
@@ -201,7 +204,8 @@ def run_gpu(args):
     for evs in kev:            # torch creates CUDA events on first record
         for e in evs:
             e.record(stream)
-    kdbg = [moe.expert_timing(evs) for evs in kev]
+    # per-kernel events force the one-launch-per-phase path: only used there
+    kdbg = [None if persistent else moe.expert_timing(evs) for evs in kev]
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -223,12 +227,24 @@ def run_gpu(args):
     if sampler:
         sampler.__exit__()
     per = [a.elapsed_time(b) * 1e3 for a, b in ev]   # us per forward
-    kern = [sum(evs[2 * l].elapsed_time(evs[2 * l + 1]) for l in range(L)) * 1e3 / L for evs in kev]  # us per layer
+    if persistent:   # the whole forward is one kernel (plus two tiny memsets)
+        kern = [v / L for v in per]
+    else:
+        kern = [sum(evs[2 * l].elapsed_time(evs[2 * l + 1]) for l in range(L)) * 1e3 / L for evs in kev]
     us = statistics.mean(per)
     kern_us = statistics.mean(kern)
     st_code = pkg.moe_mxfp4_check(moe.handle, wsp.data_ptr(), st)
     if st_code != 0:
         raise pkg.MoeError(st_code, "forward")
+    phases = None
+    if persistent:   # CTA 0's phase-end timestamps of the last forward (workspace bytes 64..)
+        nst = 2 + 4 * min(L, 8)
+        ts = wsp[64:64 + 8 * nst].cpu().view(torch.int64).tolist()
+        names = ["staging"] + [f"l{l}_{n}" for l in range(min(L, 8)) for n in ("router", "route", "experts", "combine")]
+        phases = {n: round((ts[i + 1] - ts[i]) / 1e3, 2) for i, n in enumerate(names)}
+        sub = wsp[64 + 8 * 40:64 + 8 * 52].cpu().view(torch.int64).tolist()   # routing / router sub-steps, layer 0
+        phases["l0_route_steps"] = [round((sub[i + 1] - sub[i]) / 1e3, 2) for i in range(4)]
+        phases["l0_router_unit0"] = [round((sub[8 + i + 1] - sub[8 + i]) / 1e3, 2) for i in range(3)]
     if ws > 1:
         t = torch.tensor([us], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -252,10 +268,16 @@ def run_gpu(args):
         return
     peak, peak_kind = _peaks()
     gbs = alg_bytes / (us * 1e-6) / 1e9
-    # the expert kernel's algorithmic bytes: the routed experts' nibbles and scales, once per layer
-    kern_bytes = sum(n_active) * wl.expert_bytes / wl.layers
+    # algorithmic bytes of the timed kernel per layer: the persistent kernel moves all
+    # of the layer's bytes; the separate expert kernel the routed experts' nibbles and scales
+    kern_bytes = alg_bytes / wl.layers if persistent else sum(n_active) * wl.expert_bytes / wl.layers
     kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
-    launches_per_step = (1 + 7 * wl.layers) if moe_tma(wl) else (1 + 5 * wl.layers + (wl.layers if wl.norm else 0))
+    if persistent:
+        launches_per_step = -(-wl.layers // 8)
+    elif moe_tma(wl):
+        launches_per_step = (1 if wl.norm else 0) + 6 * wl.layers
+    else:
+        launches_per_step = 1 + 5 * wl.layers + (wl.layers if wl.norm else 0)
     clocks = sampler.summary() if sampler else None
     line = {
         "metric": "us_per_moe_layer_per_verify_block", "value": round(us / wl.layers, 2), "unit": "us",
@@ -263,16 +285,18 @@ def run_gpu(args):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (MXFP4 weights)",
         "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "layers": wl.layers, "routed_experts": n_active, "algorithmic_bytes": alg_bytes,
+                   "layers": wl.layers, "path": "persistent" if persistent else args.path, "routed_experts": n_active, "algorithmic_bytes": alg_bytes,
                    "l2": "flushed between steps (256 MiB write outside the per-step events)",
                    "parallelism": f"replicas{ws}"},
         "hbm_gbs": round(gbs, 1),
         "implied_tokens_per_s": round(ACCEPTANCE_LENGTH / (us * 1e-6), 1),
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(kern_gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "expert FFN kernel", "kernel_us_per_layer": round(kern_us, 2),
+                     "kernel": "persistent forward kernel" if persistent else "expert FFN kernel",
+                     "kernel_us_per_layer": round(kern_us, 2),
                      "kernel_bytes_per_layer": int(kern_bytes)},
         "forward_hbm_frac": round(gbs / peak, 4),
+        "phases_us": phases,
         "e2e": {"value": round(e2e_us / wl.layers, 2), "unit": "us", "h2d_bytes_per_step": wl.T * wl.H * 2,
                 "d2h_bytes_per_step": wl.T * wl.H * 4},
         "gpu_launches": launches_per_step * args.steps,
@@ -331,6 +355,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-experts", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="persistent", choices=["persistent", "multi"],
+                    help="one cooperative launch per forward, or one launch per phase")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -76,7 +76,12 @@ extern "C" {
 #define MOE_FLAG_NORM         (1u << 0) /* pre-norm residual stack (see above) */
 #define MOE_FLAG_OUT_BF16     (1u << 1) /* y is bf16 instead of fp32 */
 #define MOE_FLAG_MULTI_KERNEL (1u << 2) /* one launch per phase (comparison path) */
-#define MOE_FLAG_NO_DENSE     (1u << 3) /* never use the tensor-core expert path */
+#define MOE_FLAG_NO_DENSE     (1u << 3) /* reserved */
+#define MOE_FLAG_DEBUG_STALL  (1u << 4) /* testing aid: the forward withholds one device-side signal (one
+                                          * CTA's first grid-barrier arrival in the persistent forward; the
+                                          * gate/up completions of the first routed expert in the one-launch-
+                                          * per-phase forward), so its waits run out after timeout_us and the
+                                          * status becomes MOE_ERR_TIMEOUT; nothing hangs or faults */
 
 typedef struct moe_mxfp4_handle moe_mxfp4_handle; /* opaque, host-side */
 
@@ -131,7 +136,10 @@ typedef struct {
 int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
                      moe_mxfp4_handle** out);
 
-/* Bytes of device workspace a forward over num_tokens tokens needs. */
+/* Bytes of device workspace a forward over num_tokens tokens needs.  The first 512
+ * bytes hold the status words; in a persistent forward, bytes 64..335 receive CTA 0's
+ * %globaltimer (uint64 ns) at the end of each phase (start, input staging, and per
+ * layer l: router 2+4l, routing 3+4l, experts 4+4l, combine 5+4l), for profiling. */
 int moe_mxfp4_workspace_bytes(const moe_mxfp4_handle* h, int32_t num_tokens, size_t* bytes);
 
 /* Runs the layer (stack) on num_tokens rows of x_dev into y_dev.  workspace_dev

@@ -26,6 +26,7 @@ MOE_FLAG_NORM = 1 << 0
 MOE_FLAG_OUT_BF16 = 1 << 1
 MOE_FLAG_MULTI_KERNEL = 1 << 2
 MOE_FLAG_NO_DENSE = 1 << 3
+MOE_FLAG_DEBUG_STALL = 1 << 4
 
 EXPORTED = (
     "moe_mxfp4_create",

@@ -51,8 +51,11 @@ constexpr int kSlotAux = 512;                              // down items: h segm
 constexpr int kSlotBytes = kSlotNib + kSlotScale + kSlotAct + kSlotAux;  // 43 KB, multiple of 1024
 static_assert(kSlotBytes % 1024 == 0, "slots hold 1024-byte-aligned swizzled boxes");
 constexpr int kEpiBytes = kTmaRows * kTmaTok * 2 * 4;      // K-half exchange: 8 KB
-constexpr int kTmaSmemBytes = 1024 /*align slack*/ + kTmaStages * kSlotBytes + kEpiBytes + 1024 /*barriers, meta*/;
+constexpr int kTmaSmemBytes =
+    1024 /*align slack*/ + kTmaStages * kSlotBytes + kEpiBytes + 2048 /*barriers, slot meta, routing table*/;
 static_assert(kTmaSmemBytes <= 232448, "shared memory of the expert kernel");
+static_assert(8 * (2 * kTmaStages + 1) + sizeof(int) * 8 * kTmaStages + sizeof(int) * (4 + 6 * 64) <= 2048,
+              "barriers, slot metadata and routing table fit their region");
 
 enum : int { kItemGateUp = 0, kItemDown = 1 };
 
@@ -69,29 +72,42 @@ struct TmaMaps {
 
 // One work item, as the producer reads it (64 bytes): everything it needs to
 // issue the item's copies without further dependent loads.
-struct ItemRec {
+struct __align__(16) ItemRec {
     int code;          // item_code(kind, rb, tc, a)
     int e;             // expert id
     int beg;           // first position of the item's pairs in perm
     int ntok;          // pairs in the item (1..8)
-    int tok[kTmaTok];  // gate/up items: token index of each pair
+    int tok[kTmaTok];  // gate/up items: token of each pair; down items: pair id (t*k + j)
     int pad[4];
+};
+
+// Routing state of one layer kept in shared memory by every CTA when the verify
+// block is small (T*k <= 64 pairs): the work items are derived from it directly.
+constexpr int kRtMaxPairs = 64;
+struct RouteTable {
+    int n_active, n_chunks, pad0, pad1;
+    int e[kRtMaxPairs];        // per routed expert (ascending id): expert id
+    int beg[kRtMaxPairs];      // first position in perm
+    int cnt[kRtMaxPairs];      // pairs routed to it
+    int chunk0[kRtMaxPairs];   // index of its first chunk of <= 8 pairs
+    int tok[kRtMaxPairs];      // per perm position: token
+    int pair[kRtMaxPairs];     // per perm position: pair id t*k + j
 };
 
 // Per-forward work list and synchronisation words (workspace, zeroed per layer).
 struct WorkList {
-    ItemRec* items;    // all gate/up items, then all down items
+    ItemRec* items;    // all gate/up items, then all down items (unused with a routing table)
     int* n_items;      // [0] = total, [1] = number of gate/up items
-    int* queue;        // next item to claim
-    int* done;         // [E] gate/up items finished, per active-expert index
+    int* queue;        // next item to claim (zero at the start of the phase)
+    int* done;         // [E] gate/up items finished, per active-expert index (zero at the start)
     int* need;         // [E] gate/up items per active-expert index
     int* abort;        // set when any wait times out
 };
 
 struct ExpertArgs {
     int H, I, k, layer;
-    const __half* act16;     // [T, H] f16 activations, x * 2^-p_t
-    const float* act_scale;  // [T] 2^p_t
+    const __half* act16;     // [T, H] f16 activations, x * 2^-p (p per token and 128-wide segment)
+    const float* act_fac;    // [T, H / 128] 2^p of each segment
     __half* h16;             // [pairs, I] f16 SwiGLU output, h * 2^-q
     float* h_scale;          // [pairs, I / 128] 2^q per 128-row segment
     float* partial;          // [pairs (pair id t*k + j), H]
@@ -99,7 +115,51 @@ struct ExpertArgs {
     WorkList wl;
     int* status;
     unsigned long long timeout_ns;
+    int debug_stall;         // testing aid: the first routed expert never signals its gate/up items
+    const RouteTable* rt;    // shared-memory routing table, or NULL (items come from wl)
 };
+
+// What changes between the expert phases of one launch (layer, counters, table).
+struct ExpertLayer {
+    int layer;
+    int* queue;
+    int* done;
+    const RouteTable* rt;
+};
+
+// Item idx of the phase, from the routing table (rbu / rbd: row blocks of gate/up and down).
+__device__ __forceinline__ ItemRec table_item(const RouteTable* rt, int idx, int rbu, int rbd) {
+    const int n_gu = rt->n_chunks * rbu;
+    const bool down = idx >= n_gu;
+    const int j = down ? idx - n_gu : idx;
+    const int nrb = down ? rbd : rbu;
+    const int chunk = j / nrb, rbi = j % nrb;
+    int lo = 0, hi = rt->n_active - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (rt->chunk0[mid] <= chunk) lo = mid; else hi = mid - 1;
+    }
+    const int tc = chunk - rt->chunk0[lo];
+    ItemRec r;
+    r.code = item_code(down ? 1 : 0, rbi, tc, lo);
+    r.e = rt->e[lo];
+    r.beg = rt->beg[lo] + tc * kTmaTok;
+    r.ntok = min(kTmaTok, rt->cnt[lo] - tc * kTmaTok);
+#pragma unroll
+    for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? rt->pair[r.beg + q] : rt->tok[r.beg + q]) : 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) r.pad[q] = 0;
+    return r;
+}
+
+__device__ __forceinline__ ItemRec load_item(const ItemRec* src) {
+    ItemRec r;
+    const int4* s = reinterpret_cast<const int4*>(src);
+    int4* d = reinterpret_cast<int4*>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = __ldcg(s + i);
+    return r;
+}
 
 struct SlotMeta {
     int kind, a, e, beg, ntok, stage, nstages, rb;
@@ -210,15 +270,11 @@ __device__ __forceinline__ void mma_stage(const uint8_t* slot, int rbase, int kh
                 const int r0 = rbase + 16 * tt + g;   // r0 & 7 == (r0 + 8) & 7 == g
                 const uint32_t w0 = *reinterpret_cast<const uint32_t*>(box + r0 * 128 + ((j ^ g) << 4) + 4 * q);
                 const uint32_t w1 = *reinterpret_cast<const uint32_t*>(box + (r0 + 8) * 128 + ((j ^ g) << 4) + 4 * q);
-                uint32_t a0[4], a1[4];
-                a0[0] = e2m1x2_to_f16x2(w0);
-                a0[1] = e2m1x2_to_f16x2(w1);
-                a0[2] = e2m1x2_to_f16x2(w0 >> 8);
-                a0[3] = e2m1x2_to_f16x2(w1 >> 8);
-                a1[0] = e2m1x2_to_f16x2(w0 >> 16);
-                a1[1] = e2m1x2_to_f16x2(w1 >> 16);
-                a1[2] = e2m1x2_to_f16x2(w0 >> 24);
-                a1[3] = e2m1x2_to_f16x2(w1 >> 24);
+                uint32_t c0[4], c1[4];   // bytes 0..3 of rows g and g+8
+                e2m1x8_to_f16x2(w0, c0);
+                e2m1x8_to_f16x2(w1, c1);
+                const uint32_t a0[4] = {c0[0], c1[0], c0[1], c1[1]};
+                const uint32_t a1[4] = {c0[2], c1[2], c0[3], c1[3]};
                 const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 float d[4];
                 mma_16816_f16(d, a0, xv.x, xv.y, zero);
@@ -241,55 +297,71 @@ __device__ __forceinline__ void mma_stage(const uint8_t* slot, int rbase, int kh
     }
 }
 
-__global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid_constant__ TmaMaps maps,
-                                                                    const ExpertArgs args) {
-    extern __shared__ uint8_t smem_raw[];
+// Shared memory of the expert phase: the slot ring, the K-half exchange area,
+// the ring / epilogue mbarriers and the per-slot metadata.
+struct ExpertSmem {
+    uint8_t* slots;
+    float* epi;          // [2][128 rows][8 tokens]
+    uint64_t* full;      // [kTmaStages]
+    uint64_t* empty;     // [kTmaStages]
+    uint64_t* epi_bar;
+    SlotMeta* meta;      // [kTmaStages]
+    RouteTable* rt;      // small-block routing table (persistent forward)
+};
+
+__device__ __forceinline__ ExpertSmem expert_smem(uint8_t* smem_raw) {
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* slots = smem;
-    float* epi = reinterpret_cast<float*>(smem + kTmaStages * kSlotBytes);           // [2][128 rows][8 tok]
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaStages * kSlotBytes + kEpiBytes);
-    uint64_t* empty = full + kTmaStages;
-    uint64_t* epi_bar = empty + kTmaStages;
-    SlotMeta* meta = reinterpret_cast<SlotMeta*>(epi_bar + 1);
+    ExpertSmem sm;
+    sm.slots = smem;
+    sm.epi = reinterpret_cast<float*>(smem + kTmaStages * kSlotBytes);
+    sm.full = reinterpret_cast<uint64_t*>(smem + kTmaStages * kSlotBytes + kEpiBytes);
+    sm.empty = sm.full + kTmaStages;
+    sm.epi_bar = sm.empty + kTmaStages;
+    sm.meta = reinterpret_cast<SlotMeta*>(sm.epi_bar + 1);
+    sm.rt = reinterpret_cast<RouteTable*>(sm.meta + kTmaStages);
+    return sm;
+}
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const unsigned long long deadline = globaltimer_ns() + args.timeout_ns;
-    const int H = args.H, I = args.I;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kTmaStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kTmaConsumerWarps);
-        }
-        mbar_init(epi_bar, kTmaConsumerWarps);
-        fence_barrier_init();
+// One thread initialises the barriers (then the block synchronises).
+__device__ __forceinline__ void expert_smem_init(const ExpertSmem& sm) {
+    for (int s = 0; s < kTmaStages; ++s) {
+        mbar_init(&sm.full[s], 1);
+        mbar_init(&sm.empty[s], kTmaConsumerWarps);
     }
-    __syncthreads();
+    mbar_init(sm.epi_bar, kTmaConsumerWarps);
+    fence_barrier_init();
+}
 
-    if (warp == kTmaConsumerWarps) {
-        // ------------------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tensormap(&maps.gate_q);
-            prefetch_tensormap(&maps.up_q);
-            prefetch_tensormap(&maps.down_q);
-            prefetch_tensormap(&maps.gate_s);
-            prefetch_tensormap(&maps.up_s);
-            prefetch_tensormap(&maps.down_s);
-            const int n_items = args.wl.n_items[0];
-            uint32_t it = 0;
+// Producer of one expert phase (one thread): claims items until the queue is
+// empty, streams their stages into the ring and finally publishes an END slot.
+// `it` is the ring position, carried across phases.  Returns false on a timeout.
+__device__ bool expert_produce(const TmaMaps& maps, const ExpertArgs& args, const ExpertLayer lay, const ExpertSmem& sm,
+                               uint32_t& it, unsigned long long deadline) {
+    uint8_t* slots = sm.slots;
+    uint64_t* full = sm.full;
+    uint64_t* empty = sm.empty;
+    SlotMeta* meta = sm.meta;
+    const int H = args.H, I = args.I;
+    {
+        {
+            // work-list data is written by another CTA in the same launch: read it from L2
+            const int rbu = I / kTmaRows, rbd = H / kTmaRows;
+            const int n_items = lay.rt ? lay.rt->n_chunks * (rbu + rbd) : __ldcg(args.wl.n_items);
             bool finished = false, failed = false;
             // one item of lookahead: the next record is claimed and loaded while
             // the current item's stages are issued
-            int next_idx = atomicAdd(args.wl.queue, 1);
+            int next_idx = atomicAdd(lay.queue, 1);
             ItemRec next{};
-            if (next_idx < n_items) next = args.wl.items[next_idx];
+            if (next_idx < n_items)
+                next = lay.rt ? table_item(lay.rt, next_idx, rbu, rbd) : load_item(args.wl.items + next_idx);
             while (!finished && !failed) {
                 const int idx = next_idx;
                 const ItemRec cur = next;
                 const bool end = idx >= n_items;
                 if (!end) {
-                    next_idx = atomicAdd(args.wl.queue, 1);
-                    if (next_idx < n_items) next = args.wl.items[next_idx];
+                    next_idx = atomicAdd(lay.queue, 1);
+                    if (next_idx < n_items)
+                        next = lay.rt ? table_item(lay.rt, next_idx, rbu, rbd) : load_item(args.wl.items + next_idx);
                 }
                 int kind = 0, a = 0, e = 0, beg = 0, ntok = 0, nstages = 1, rb = 0;
                 if (!end) {
@@ -310,10 +382,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
                     m.kind = end ? -1 : kind; m.a = a; m.e = e; m.beg = beg; m.ntok = ntok;
                     m.stage = s; m.nstages = nstages; m.rb = rb;
                     meta[slot] = m;
-                    if (end) { mbar_arrive(&full[slot]); finished = true; break; }
+                    if (end) { mbar_arrive(&full[slot]); ++it; finished = true; break; }
                     uint8_t* dst = slots + slot * kSlotBytes;
-                    const uint32_t bytes = kSlotNib + kSlotScale + (uint32_t)ntok * (kTmaKC * 2) +
-                                           (kind == kItemDown ? (uint32_t)ntok * 16u : 0u);
+                    const uint32_t bytes = kSlotNib + kSlotScale + (uint32_t)ntok * (kTmaKC * 2 + 16u);
                     mbar_arrive_expect_tx(&full[slot], bytes);
                     ++it;   // this slot now has copies in flight
                     const CUtensorMap* mq;
@@ -343,15 +414,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
                     }
                     uint8_t* act_dst = dst + kSlotNib + kSlotScale;
                     if (kind == kItemGateUp) {
-                        for (int i = 0; i < ntok; ++i)
+                        uint8_t* aux = act_dst + kSlotAct;
+                        for (int i = 0; i < ntok; ++i) {
                             bulk_load(act_dst + i * kActStride, args.act16 + (size_t)cur.tok[i] * H + k0,
                                       kTmaKC * 2, &full[slot]);
+                            // the 4 segment factors (128 activations each) of this stage's K range
+                            bulk_load(aux + i * 16, args.act_fac + (size_t)cur.tok[i] * (H / 128) + k0 / 128, 16,
+                                      &full[slot]);
+                        }
                     } else {
                         if (!h_ready) {
                             // every gate/up item of this expert must have stored h
-                            const int need = args.wl.need[a];
+                            const int need = lay.rt ? (lay.rt->cnt[a] + kTmaTok - 1) / kTmaTok * rbu
+                                                     : __ldcg(args.wl.need + a);
                             uint32_t spins = 0;
-                            while (ld_acquire_gpu(args.wl.done + a) < need) {
+                            while (ld_acquire_gpu(lay.done + a) < need) {
                                 if ((++spins & 63u) == 0 &&
                                     (globaltimer_ns() > deadline ||
                                      *reinterpret_cast<const volatile int*>(args.wl.abort))) {
@@ -376,7 +453,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
                 }
             }
             if (failed) {
-                if (atomicExch(args.wl.abort, 1) == 0) raise_status(args.status, MOE_ERR_TIMEOUT, args.layer * 65536);
+                if (atomicExch(args.wl.abort, 1) == 0) raise_status(args.status, MOE_ERR_TIMEOUT, lay.layer * 65536);
                 // every copy this CTA issued must land before the CTA exits
                 const uint32_t issued = it < (uint32_t)kTmaStages ? it : (uint32_t)kTmaStages;
                 for (uint32_t q = 0; q < issued; ++q) {
@@ -385,11 +462,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
                                 globaltimer_ns() + args.timeout_ns);
                 }
             }
+            return !failed;
         }
-        return;
     }
+}
 
-    // ---------------------------------------------------------------------- consumers
+// Consumers of one expert phase (warps 0..kTmaConsumerWarps-1): consume slots until
+// the END slot (which they release too).  `it` and `epi_uses` are carried across
+// phases.  Returns false on a timeout / abort.
+__device__ bool expert_consume(const ExpertArgs& args, const ExpertLayer lay, const ExpertSmem& sm, uint32_t& it,
+                               uint32_t& epi_uses, int warp, int lane, unsigned long long deadline) {
+    const uint8_t* slots = sm.slots;
+    float* epi = sm.epi;
+    uint64_t* full = sm.full;
+    uint64_t* empty = sm.empty;
+    uint64_t* epi_bar = sm.epi_bar;
+    const SlotMeta* meta = sm.meta;
+    const int H = args.H, I = args.I;
     const int rp = warp % kTmaRowGroups, kh = warp / kTmaRowGroups;
     const int rbase = 16 * kTmaTiles * rp;
     const int g = lane >> 2, q = lane & 3;
@@ -398,7 +487,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
     for (int tt = 0; tt < kTmaTiles; ++tt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) accG[tt][i] = accU[tt][i] = 0.0f;
-    uint32_t epi_uses = 0;
     // consumer-wide barrier on an mbarrier (8 warp arrivals) with a bounded wait
     auto consumer_sync = [&]() -> bool {
         __syncwarp();
@@ -411,12 +499,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
     auto row_of = [&](int tt, int i) { return rbase + 16 * tt + g + 8 * (i >> 1); };
     auto tok_of = [&](int i) { return 2 * q + (i & 1); };
     bool failed = false;
-    for (uint32_t it = 0;; ++it) {
+    for (;; ++it) {
         const int slot = it % kTmaStages;
         const uint32_t n = it / kTmaStages;
         if (!warp_wait_phase(&full[slot], n & 1, deadline, args.wl.abort)) { failed = true; break; }
         const SlotMeta m = meta[slot];
-        if (m.kind < 0) break;
+        if (m.kind < 0) {   // END: release the slot so the ring stays in step for the next phase
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            ++it;
+            break;
+        }
         const uint8_t* sl = slots + slot * kSlotBytes;
         if (m.stage == 0) {
 #pragma unroll
@@ -435,11 +528,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
                                  (sc.x >> 6) & (sc.x >> 7) & 0x01010101u) |
                                 (sc.y & (sc.y >> 1) & (sc.y >> 2) & (sc.y >> 3) & (sc.y >> 4) & (sc.y >> 5) &
                                  (sc.y >> 6) & (sc.y >> 7) & 0x01010101u);
-            if (ff) raise_status(args.status, MOE_ERR_BAD_SCALE, args.layer * 65536 + m.e);
+            if (ff) raise_status(args.status, MOE_ERR_BAD_SCALE, lay.layer * 65536 + m.e);
         }
         if (m.kind == kItemGateUp) {
-            if (m.stage & 1) mma_stage<kTmaTiles>(sl, rbase, kh, lane, accU, false);
-            else mma_stage<kTmaTiles>(sl, rbase, kh, lane, accG, false);
+            if (m.stage & 1) mma_stage<kTmaTiles>(sl, rbase, kh, lane, accU, true);
+            else mma_stage<kTmaTiles>(sl, rbase, kh, lane, accG, true);
         } else {
             mma_stage<kTmaTiles>(sl, rbase, kh, lane, accG, true);
         }
@@ -465,17 +558,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
             float hv[kTmaTiles][4];
             float mx0 = 0.0f, mx1 = 0.0f;   // tokens 2q, 2q+1 over this thread's rows
             if (kh == 0) {
-                const int t0 = 2 * q < m.ntok ? args.rb.perm[m.beg + 2 * q] / args.k : 0;
-                const int t1 = 2 * q + 1 < m.ntok ? args.rb.perm[m.beg + 2 * q + 1] / args.k : 0;
-                const float xs0 = args.act_scale[t0], xs1 = args.act_scale[t1];
 #pragma unroll
                 for (int tt = 0; tt < kTmaTiles; ++tt)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int r = row_of(tt, i), c = tok_of(i);
-                        const float xs = (i & 1) ? xs1 : xs0;
-                        const float gg = (accG[tt][i] + exG[r * kTmaTok + c]) * xs;
-                        const float uu = (accU[tt][i] + exU[r * kTmaTok + c]) * xs;
+                        const float gg = accG[tt][i] + exG[r * kTmaTok + c];
+                        const float uu = accU[tt][i] + exU[r * kTmaTok + c];
                         const float h = silu(gg) * uu;
                         hv[tt][i] = h;
                         if (i & 1) mx1 = fmaxf(mx1, fabsf(h)); else mx0 = fmaxf(mx0, fabsf(h));
@@ -516,10 +605,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
                 }
             }
             if (!consumer_sync()) { failed = true; break; }
-            if (threadIdx.x == 0) {
+            if (threadIdx.x == 0 && !(args.debug_stall && m.a == 0)) {
                 __threadfence();
                 fence_proxy_async_global();
-                red_release_add_gpu(args.wl.done + m.a, 1);
+                red_release_add_gpu(lay.done + m.a, 1);
             }
         } else {
             if (kh == 0) {
@@ -527,7 +616,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
                 for (int c = 0; c < 2; ++c) {
                     const int tok = 2 * q + c;
                     if (tok < m.ntok) {
-                        const int pair = args.rb.perm[m.beg + tok];
+                        const int pair = lay.rt ? lay.rt->pair[m.beg + tok] : __ldcg(args.rb.perm + m.beg + tok);
 #pragma unroll
                         for (int tt = 0; tt < kTmaTiles; ++tt)
 #pragma unroll
@@ -543,21 +632,56 @@ __global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid
         }
     }
     if (failed && lane == 0) {
-        if (atomicExch(args.wl.abort, 1) == 0) raise_status(args.status, MOE_ERR_TIMEOUT, args.layer * 65536);
+        if (atomicExch(args.wl.abort, 1) == 0) raise_status(args.status, MOE_ERR_TIMEOUT, lay.layer * 65536);
     }
+    return !failed;
+}
+
+__global__ void __launch_bounds__(kTmaThreads, 1) expert_tma_kernel(const __grid_constant__ TmaMaps maps,
+                                                                    const ExpertArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const ExpertSmem sm = expert_smem(smem_raw);
+    if (threadIdx.x == 0) expert_smem_init(sm);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned long long deadline = globaltimer_ns() + args.timeout_ns;
+    uint32_t it = 0, epi_uses = 0;
+    const ExpertLayer lay{args.layer, args.wl.queue, args.wl.done, args.rt};
+    if (warp == kTmaConsumerWarps) {
+        if (lane == 0) {
+            prefetch_tensormap(&maps.gate_q);
+            prefetch_tensormap(&maps.up_q);
+            prefetch_tensormap(&maps.down_q);
+            prefetch_tensormap(&maps.gate_s);
+            prefetch_tensormap(&maps.up_s);
+            prefetch_tensormap(&maps.down_s);
+            expert_produce(maps, args, lay, sm, it, deadline);
+        }
+        return;
+    }
+    expert_consume(args, lay, sm, it, epi_uses, warp, lane, deadline);
 }
 
 // Builds the work list of one layer from the grouping: for every routed expert
 // (active index a) and every chunk of up to 8 of its tokens, I/128 gate/up
 // items, then H/128 down items, each with its full record.  One block of 1024 threads.
-__global__ void __launch_bounds__(1024) build_items_kernel(RouteBufs rb, int H, int I, int k, WorkList wl) {
+__global__ void __launch_bounds__(1024) build_items_kernel(RouteBufs rb, int H, int I, int k, WorkList wl, int T) {
     __shared__ int s_gu[kMaxExperts + 1];
+    __shared__ int s_act[kMaxExperts], s_beg[kMaxExperts], s_cnt[kMaxExperts];
     __shared__ int s_scan[64];
+    extern __shared__ int s_perm[];   // [T * k] pair id of each perm position
     const int n_active = rb.active[0];
     const int rbu = I / kTmaRows, rbd = H / kTmaRows;
     const int a = threadIdx.x;
     int chunks = 0;
-    if (a < n_active) chunks = (rb.counts[rb.active[1 + a]] + kTmaTok - 1) / kTmaTok;
+    if (a < n_active) {
+        const int e = rb.active[1 + a];
+        s_act[a] = e;
+        s_beg[a] = rb.offsets[e];
+        s_cnt[a] = rb.counts[e];
+        chunks = (s_cnt[a] + kTmaTok - 1) / kTmaTok;
+    }
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) s_perm[i] = rb.perm[i];
     const int off = block_excl_scan_1024(chunks, s_scan);
     const int total_chunks = s_scan[32];
     if (a < n_active) {
@@ -587,14 +711,13 @@ __global__ void __launch_bounds__(1024) build_items_kernel(RouteBufs rb, int H, 
             if (s_gu[mid] <= chunk) lo = mid; else hi = mid - 1;
         }
         const int aa = lo, tc = chunk - s_gu[aa];
-        const int e = rb.active[1 + aa];
         ItemRec r;
         r.code = item_code(down ? kItemDown : kItemGateUp, rbi, tc, aa);
-        r.e = e;
-        r.beg = rb.offsets[e] + tc * kTmaTok;
-        r.ntok = min(kTmaTok, rb.counts[e] - tc * kTmaTok);
+        r.e = s_act[aa];
+        r.beg = s_beg[aa] + tc * kTmaTok;
+        r.ntok = min(kTmaTok, s_cnt[aa] - tc * kTmaTok);
 #pragma unroll
-        for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? rb.perm[r.beg + q] / k : 0;
+        for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? s_perm[r.beg + q] : s_perm[r.beg + q] / k) : 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q) r.pad[q] = 0;
         wl.items[i] = r;
@@ -605,13 +728,13 @@ __global__ void __launch_bounds__(1024) build_items_kernel(RouteBufs rb, int H, 
 //   norm_w == NULL: act[t] = fp32(x[t]) (x bf16), and resid[t] = act[t] when resid != NULL;
 //   norm_w != NULL: act[t] = resid[t] * w / sqrt(mean(resid[t]^2) + eps)  (RMSNorm);
 // then act16[t] = f16(act[t] * 2^-p_t) with 2^p_t from the row maximum (exact for
-// bf16-valued rows), act_scale[t] = 2^p_t.  Fixed reduction order.
+// bf16-valued rows), and 2^p_t as the factor of every 128-wide segment of the row.
 constexpr int kPrepThreads = 1024;
 __global__ void __launch_bounds__(kPrepThreads) prep_layer_kernel(const __nv_bfloat16* __restrict__ x, int H,
                                                                   float* resid, const __nv_bfloat16* __restrict__ norm_w,
                                                                   float eps, float* __restrict__ act,
                                                                   __half* __restrict__ act16,
-                                                                  float* __restrict__ act_scale) {
+                                                                  float* __restrict__ act_fac) {
     __shared__ float red[2][32];
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -659,7 +782,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_layer_kernel(const __nv_bfl
             if (resid && !norm_w) resid[(size_t)t * H + h] = v[i];
         }
     }
-    if (threadIdx.x == 0) act_scale[t] = exp2i(p);
+    for (int i = threadIdx.x; i < H / 128; i += blockDim.x) act_fac[(size_t)t * (H / 128) + i] = exp2i(p);
 }
 
 }  // namespace moe

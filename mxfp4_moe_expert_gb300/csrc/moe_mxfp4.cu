@@ -14,6 +14,7 @@
 #include "expert_simple.cuh"
 #include "expert_tma.cuh"
 #include "layer_ops.cuh"
+#include "persist.cuh"
 #include "route.cuh"
 
 struct moe_mxfp4_handle {
@@ -21,6 +22,7 @@ struct moe_mxfp4_handle {
     std::vector<moe_mxfp4_layer> layers;
     std::vector<moe::TmaMaps> maps;   // per layer, when the TMA expert path applies
     bool tma = false;
+    int persist_grid = 0;              // CTAs of the persistent forward (one per SM), 0 = unavailable
     int device = 0;
     int sm_count = 0;
     int e_begin = 0, e_end = 0;
@@ -36,7 +38,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // Byte offsets of the workspace sections for T tokens.
 struct WsLayout {
     size_t status, xstage, ystage, act, resid, logits, idx, gate, counts, offsets, perm, active, hbuf, partial;
-    size_t act16, act_scale, h16, h_scale, items, sync, rpart, total;
+    size_t act16, act_fac, ss, tickets, h16, h_scale, items, sync, rpart, total;
 };
 
 // Upper bound of the work items of one layer: every routed expert contributes
@@ -52,7 +54,7 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     const size_t H = (size_t)c.hidden, I = (size_t)c.inter, E = (size_t)c.num_experts, k = (size_t)c.top_k;
-    L.status = take(64);
+    L.status = take(512);   // status words, grid-barrier counters, persistent-forward phase timestamps
     L.xstage = take((size_t)T * H * 2);
     L.ystage = take((size_t)T * H * 4);
     L.act = take((size_t)T * H * 4);
@@ -67,12 +69,14 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     L.hbuf = take((size_t)T * k * I * 4);
     L.partial = take((size_t)T * k * H * 4);
     L.act16 = take((size_t)T * H * 2);
-    L.act_scale = take((size_t)T * 4);
+    L.act_fac = take((size_t)T * (H / 128) * 4);
+    L.ss = take((size_t)T * (H / 1024 + 1) * 4);
+    L.tickets = take((size_t)moe::kMaxPersistLayers * (E + 1) * 4);   // per-layer queue + done counters
     L.h16 = take((size_t)T * k * I * 2);
     L.h_scale = take((size_t)T * k * (I / 128) * 4);
     L.items = take(max_items(c, T) * sizeof(moe::ItemRec));
     L.sync = take((8 + 2 * E) * 4);   // n_items[2], queue, abort, ..., done[E], need[E]
-    L.rpart = take((size_t)(H / moe::kRouteSlice + 1) * T * E * 4);   // router partials per 512-column slice
+    L.rpart = take((size_t)(H / 512 + 1) * T * E * 4);   // router partials per 512- or 1024-column slice
     L.total = o;
     return L;
 }
@@ -224,7 +228,7 @@ int forward_tma(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, co
     moe::ExpertArgs ea;
     ea.H = H; ea.I = I; ea.k = k;
     ea.act16 = reinterpret_cast<const __half*>(ws + L.act16);
-    ea.act_scale = reinterpret_cast<const float*>(ws + L.act_scale);
+    ea.act_fac = reinterpret_cast<const float*>(ws + L.act_fac);
     ea.h16 = reinterpret_cast<__half*>(ws + L.h16);
     ea.h_scale = reinterpret_cast<float*>(ws + L.h_scale);
     ea.partial = reinterpret_cast<float*>(ws + L.partial);
@@ -232,23 +236,25 @@ int forward_tma(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, co
     ea.wl = wl;
     ea.status = status;
     ea.timeout_ns = (unsigned long long)c.timeout_us * 1000ull;
+    ea.debug_stall = (c.flags & MOE_FLAG_DEBUG_STALL) ? 1 : 0;
+    ea.rt = nullptr;
     const size_t sel_smem = (size_t)(33 * E + 64) * sizeof(int);
     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
     if (norm)   // r_0 = x
         moe::prep_layer_kernel<<<T, moe::kPrepThreads, 0, st>>>(xb, H, resid, nullptr, 0.0f, act,
                                                                 const_cast<__half*>(ea.act16),
-                                                                const_cast<float*>(ea.act_scale));
+                                                                const_cast<float*>(ea.act_fac));
     for (int l = 0; l < c.num_layers; ++l) {
         const moe_mxfp4_layer& ly = h->layers[l];
         moe::prep_layer_kernel<<<T, moe::kPrepThreads, 0, st>>>(
             xb, H, resid, norm ? reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev) : nullptr, c.rms_eps, act,
-            const_cast<__half*>(ea.act16), const_cast<float*>(ea.act_scale));
+            const_cast<__half*>(ea.act16), const_cast<float*>(ea.act_fac));
         float* rpart = reinterpret_cast<float*>(ws + L.rpart);
         moe::route_partial_kernel<<<dim3((E + 31) / 32, H / moe::kRouteSlice), 256, 0, st>>>(
             act, T, H, reinterpret_cast<const __nv_bfloat16*>(ly.router_w_dev), E, rpart);
         moe::route_select_kernel<<<1, 1024, sel_smem, st>>>(rb.logits, T, E, k, h->e_begin, h->e_end, rb, rpart,
                                                              H / moe::kRouteSlice, ly.router_b_dev);
-        moe::build_items_kernel<<<1, 1024, 0, st>>>(rb, H, I, k, wl);
+        moe::build_items_kernel<<<1, 1024, (size_t)T * k * sizeof(int), st>>>(rb, H, I, k, wl, T);
         ea.layer = l;
         if (dbg && dbg->expert_events) cudaEventRecord(static_cast<cudaEvent_t>(dbg->expert_events[2 * l]), st);
         moe::expert_tma_kernel<<<h->sm_count, moe::kTmaThreads, moe::kTmaSmemBytes, st>>>(h->maps[l], ea);
@@ -257,6 +263,81 @@ int forward_tma(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, co
         moe::combine_kernel<<<dim3(T, (H + 1023) / 1024), 256, 0, st>>>(ea.partial, rb, H, k, h->e_begin, h->e_end,
                                                                         resid, last ? y : nullptr, y_bf16);
         copy_debug(dbg, l, T, E, k, rb, st);
+    }
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Persistent forward: one cooperative launch per (up to) 8 layers.
+int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, const WsLayout& L,
+                       cudaStream_t st, const moe_mxfp4_debug* dbg) {
+    const moe_mxfp4_config& c = h->cfg;
+    const int H = c.hidden, I = c.inter, E = c.num_experts, k = c.top_k;
+    int* sync = reinterpret_cast<int*>(ws + L.sync);
+    moe::PersistParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.T = T; p.H = H; p.I = I; p.E = E; p.k = k;
+    p.e_begin = h->e_begin; p.e_end = h->e_end;
+    p.y_bf16 = (c.flags & MOE_FLAG_OUT_BF16) ? 1 : 0;
+    p.norm = (c.flags & MOE_FLAG_NORM) ? 1 : 0;
+    p.eps = c.rms_eps;
+    p.x = reinterpret_cast<const __nv_bfloat16*>(x);
+    p.y = y;
+    p.resid = reinterpret_cast<float*>(ws + L.resid);
+    p.act16 = reinterpret_cast<__half*>(ws + L.act16);
+    p.act_fac = reinterpret_cast<float*>(ws + L.act_fac);
+    p.ss = reinterpret_cast<float*>(ws + L.ss);
+    p.rpart = reinterpret_cast<float*>(ws + L.rpart);
+    moe::ExpertArgs& ea = p.ea;
+    ea.H = H; ea.I = I; ea.k = k; ea.layer = 0;
+    ea.act16 = p.act16;
+    ea.act_fac = p.act_fac;
+    ea.h16 = reinterpret_cast<__half*>(ws + L.h16);
+    ea.h_scale = reinterpret_cast<float*>(ws + L.h_scale);
+    ea.partial = reinterpret_cast<float*>(ws + L.partial);
+    ea.rb = route_bufs(ws, L);
+    ea.wl.items = reinterpret_cast<moe::ItemRec*>(ws + L.items);
+    ea.wl.n_items = sync;
+    ea.wl.queue = sync + 2;
+    ea.wl.abort = sync + 3;
+    ea.wl.done = sync + 8;
+    ea.wl.need = sync + 8 + E;
+    ea.status = reinterpret_cast<int*>(ws + L.status);
+    ea.timeout_ns = (unsigned long long)c.timeout_us * 1000ull;
+    ea.debug_stall = (c.flags & MOE_FLAG_DEBUG_STALL) ? 1 : 0;
+    ea.rt = nullptr;
+    p.queues = reinterpret_cast<int*>(ws + L.tickets);
+    p.dones = p.queues + moe::kMaxPersistLayers;
+    p.bar = reinterpret_cast<unsigned*>(ws + L.status + 16);
+    p.route_flag = reinterpret_cast<int*>(ws + L.status + 20);
+    p.tstamp = reinterpret_cast<unsigned long long*>(ws + L.status + 64);
+    if (dbg) {
+        p.dbg.idx = dbg->topk_idx_dev;
+        p.dbg.gate = dbg->topk_gate_dev;
+        p.dbg.counts = dbg->expert_counts_dev;
+        p.dbg.offsets = dbg->expert_offsets_dev;
+        p.dbg.perm = dbg->perm_dev;
+    }
+    if (cudaMemsetAsync(sync + 3, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;   // abort flag
+    for (int l0 = 0; l0 < c.num_layers; l0 += moe::kMaxPersistLayers) {
+        const int nl = std::min(moe::kMaxPersistLayers, c.num_layers - l0);
+        p.L = nl;
+        p.layer_base = l0;
+        p.init_from_x = l0 == 0 ? 1 : 0;
+        p.write_y = (l0 + nl == c.num_layers) ? 1 : 0;
+        for (int l = 0; l < nl; ++l) {
+            const moe_mxfp4_layer& ly = h->layers[l0 + l];
+            p.layer[l].maps = h->maps[l0 + l];
+            p.layer[l].router_w = reinterpret_cast<const __nv_bfloat16*>(ly.router_w_dev);
+            p.layer[l].router_b = ly.router_b_dev;
+            p.layer[l].norm_w = reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev);
+        }
+        if (l0 > 0 && cudaMemsetAsync(ws + L.status + 16, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaMemsetAsync(ws + L.tickets, 0, (size_t)moe::kMaxPersistLayers * (E + 1) * 4, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        void* kargs[] = {&p};
+        if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(moe::persist_kernel), dim3(h->persist_grid),
+                                        dim3(moe::kTmaThreads), kargs, moe::kTmaSmemBytes, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -312,7 +393,7 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
     if (!h) return MOE_ERR_INVALID_ARG;
     // the TMA expert path takes K = H and K = I in whole 512-element stages
     // (which also makes every scale row a multiple of 16 bytes)
-    h->tma = (c.hidden % moe::kTmaKC == 0) && (c.inter % moe::kTmaKC == 0) && !(c.flags & MOE_FLAG_MULTI_KERNEL);
+    h->tma = (c.hidden % moe::kTmaKC == 0) && (c.inter % moe::kTmaKC == 0);
     if (h->tma) {
         h->maps.resize(c.num_layers);
         for (int l = 0; l < c.num_layers && h->tma; ++l) h->tma = make_maps(c, layers[l], &h->maps[l]);
@@ -321,6 +402,21 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
             delete h;
             return MOE_ERR_CUDA;
         }
+        if (h->tma && cudaFuncSetAttribute(moe::build_items_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)(std::min<size_t>((size_t)c.max_tokens * c.top_k, 512u * moe::kTmaTok) *
+                                                 sizeof(int))) != cudaSuccess)
+            h->tma = false;
+        if (h->tma && cudaFuncSetAttribute(moe::persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           moe::kTmaSmemBytes) == cudaSuccess) {
+            int per_sm = 0;
+            int coop = 0;
+            cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+            if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe::persist_kernel, moe::kTmaThreads,
+                                                                      moe::kTmaSmemBytes) == cudaSuccess &&
+                per_sm >= 1)
+                h->persist_grid = prop.multiProcessorCount;
+        }
+        cudaGetLastError();
     }
     h->cfg = c;
     if (h->cfg.timeout_us == 0) h->cfg.timeout_us = kDefaultTimeoutUs;
@@ -351,8 +447,12 @@ int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens
     char* ws = static_cast<char*>(workspace_dev);
     if (cudaMemsetAsync(ws + L.status, 0, 64, st) != cudaSuccess) return MOE_ERR_CUDA;
     // the TMA work-item code holds up to 512 token chunks of 8 per expert
-    if (h->tma && num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok)
+    if (h->tma && num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok) {
+        const bool events = dbg && dbg->expert_events;
+        if (h->persist_grid > 0 && !(h->cfg.flags & MOE_FLAG_MULTI_KERNEL) && !events)
+            return forward_persistent(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
         return forward_tma(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
+    }
     return forward_multi_kernel(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
 }
 

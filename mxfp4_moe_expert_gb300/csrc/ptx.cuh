@@ -91,6 +91,15 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
     asm("{\n .reg .b8 b;\n cvt.u8.u32 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}" : "=r"(r) : "r"(byte_in_low_bits));
     return r;
 }
+// The four code pairs (bytes 0..3) of a word -> four f16x2 values; the bytes are
+// unpacked as 8-bit registers, which the conversion reads directly.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(w));
+}
 // acc + w.lo * x.lo and acc + w.hi * x.hi with f16 operands, fp32 product and sum
 // (the product of two f16 values is exact in fp32; one rounding per step).
 __device__ __forceinline__ float fma_f16lo(uint32_t w2, uint32_t x2, float acc) {

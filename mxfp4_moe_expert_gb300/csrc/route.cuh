@@ -167,7 +167,14 @@ __global__ void __launch_bounds__(1024) route_select_kernel(const float* logits,
         // logits = bias + sum of the slice partials, slices in ascending order
         for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
             float z = 0.0f;
-            for (int s = 0; s < n_slices; ++s) z += partial[(size_t)s * T * E + i];
+            for (int s0 = 0; s0 < n_slices; s0 += 16) {   // up to 16 independent loads in flight
+                float a[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) a[u] = s0 + u < n_slices ? partial[(size_t)(s0 + u) * T * E + i] : 0.0f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (s0 + u < n_slices) z += a[u];
+            }
             rb.logits[i] = z + (bias ? bias[i % E] : 0.0f);
         }
         __syncthreads();

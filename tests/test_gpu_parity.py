@@ -284,3 +284,21 @@ def test_batched_layer_sampled():
 
 def test_stack_sampled():
     _full_size("stack", [1])
+
+
+@pytest.mark.parametrize("flags", [0, pkg.MOE_FLAG_MULTI_KERNEL], ids=["persistent", "multi_kernel"])
+def test_device_wait_timeout_is_reported_and_context_survives(flags):
+    """MOE_FLAG_DEBUG_STALL withholds one device-side signal (a grid-barrier arrival,
+    or the completion of one expert's gate/up items), so the waits that depend on it
+    run out after timeout_us (20 ms here): the kernel leaves and the status word says
+    MOE_ERR_TIMEOUT.  The next forward on the same device then runs normally."""
+    wl = SMALL[5]
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    x = inputs.x.to(DEV)
+    ref = _moe(wl, layers, flags=flags).forward(x, check=True)
+    stalled = _moe(wl, layers, flags=flags | pkg.MOE_FLAG_DEBUG_STALL, timeout_us=20000)
+    with pytest.raises(pkg.MoeError) as ei:
+        stalled.forward(x, check=True)
+    assert ei.value.status == pkg.MOE_ERR_TIMEOUT
+    again = _moe(wl, layers, flags=flags).forward(x, check=True)
+    assert torch.equal(again, ref)
