@@ -82,6 +82,8 @@ extern "C" {
                                           * gate/up completions of the first routed expert in the one-launch-
                                           * per-phase forward), so its waits run out after timeout_us and the
                                           * status becomes MOE_ERR_TIMEOUT; nothing hangs or faults */
+#define MOE_FLAG_TRACE        (1u << 5) /* profiling aid: the expert phase of the first layer records the
+                                          * first CTA's per-stage timestamps in the workspace (below) */
 
 typedef struct moe_mxfp4_handle moe_mxfp4_handle; /* opaque, host-side */
 
@@ -139,7 +141,11 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
 /* Bytes of device workspace a forward over num_tokens tokens needs.  The first 512
  * bytes hold the status words; in a persistent forward, bytes 64..335 receive CTA 0's
  * %globaltimer (uint64 ns) at the end of each phase (start, input staging, and per
- * layer l: router 2+4l, routing 3+4l, experts 4+4l, combine 5+4l), for profiling. */
+ * layer l: router 2+4l, routing 3+4l, experts 4+4l, combine 5+4l), for profiling.
+ * With MOE_FLAG_TRACE, bytes 4096..16383 receive the first layer's expert-phase
+ * timestamps of CTA 0 as 6 arrays of 256 uint64 (ns, ring stage or item i < 256):
+ * producer issues stage i, scale-factor warp sees it land, scale factors written,
+ * MMA thread starts it, MMAs issued, epilogue starts item i. */
 int moe_mxfp4_workspace_bytes(const moe_mxfp4_handle* h, int32_t num_tokens, size_t* bytes);
 
 /* Runs the layer (stack) on num_tokens rows of x_dev into y_dev.  workspace_dev

@@ -27,6 +27,7 @@ MOE_FLAG_OUT_BF16 = 1 << 1
 MOE_FLAG_MULTI_KERNEL = 1 << 2
 MOE_FLAG_NO_DENSE = 1 << 3
 MOE_FLAG_DEBUG_STALL = 1 << 4
+MOE_FLAG_TRACE = 1 << 5
 
 EXPORTED = (
     "moe_mxfp4_create",

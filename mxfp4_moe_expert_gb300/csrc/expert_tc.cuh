@@ -1,0 +1,813 @@
+// Expert FFN on the 5th-generation tensor cores, fed by TMA.
+//
+// Every routed expert's gate, up and down bytes are streamed from HBM once per
+// verify block: decode speed is bandwidth over bytes read ("MiMo x TileRT",
+// 万亿参数推理为什么特别难).  One CTA per SM pulls work items (worklist.cuh) from a
+// queue and runs them through a ring of shared-memory stages, with the roles of
+// the persistent engine's warp specialisation ("MiMo 把 1T 模型推到每秒千 token",
+// persistent engine kernel and warp specialization section):
+//   producer (one lane)   per stage (256 weight rows x 256 K): two TMA boxes of
+//                         packed E2M1 codes [128 rows x 128 B] (gate and up rows of a
+//                         gate/up item, or two 128-row blocks of a down item) in the
+//                         128-byte swizzled layout, and the activation operand (8
+//                         E2M1 terms per pair, below); the weights' E8M0 scales come
+//                         in pairs of wider boxes (several stages) through their own ring;
+//   MMA issuer (one lane) per stage 6 tcgen05.cp of the stage's scale rows and 4
+//                         block-scaled MMAs (kind::mxf4, K = 64 each): A = the
+//                         activation terms (M = 128 rows, rows 8p + j of pair slot p,
+//                         term j; rows 64.. unused), B = the weights (N = 256 rows),
+//                         one E8M0 scale per row and 32-element block, fp32
+//                         accumulator [128 x 256] in tensor memory;
+//   scale-factor warps    rearrange the stage's scales in shared memory into the
+//                         16-byte rows that tcgen05.cp puts into tensor memory;
+//   epilogue warps (8)    lanes 0..63 of the accumulator (two lane quarters x four
+//                         column chunks): sum each pair's 8 term rows (shuffle
+//                         reduce-scatter over groups of 8 lanes), then gate/up items
+//                         apply SwiGLU and store h split into 8 E2M1 terms in the
+//                         down projection's operand layout; down items store fp32
+//                         per-pair partial outputs.
+// One block-scaled MMA costs about the same for N = 64 as for N = 256, so the
+// weights take the wide operand: 8 KB of weights per MMA.  Every TMA request moves
+// whole 128-byte rows (narrower rows cost as much per request).
+// The weights are exact (E2M1 x E8M0 is what the format defines); each activation x
+// is replaced by the sum of 8 E2M1 terms with per-32 E8M0 scales, term j encoding
+// the residual of terms 0..j-1 (about 3.3 bits per term: the sum is within ~1e-7 of
+// max|x| of its block), and the tensor cores add exact products in fp32.
+#pragma once
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "route.cuh"
+#include "worklist.cuh"
+
+namespace moe {
+
+constexpr int kTcKS = 256;                 // K per stage
+constexpr int kTcStages = 4;               // ring slots
+constexpr int kTcTerms = 8;                // E2M1 terms per activation
+constexpr int kTcRowsA = kTmaTok * kTcTerms;   // activation rows used: pair slot p, term j -> row 8p + j
+constexpr int kTcN = kDownRows;            // weight rows per MMA (gate 128 | up 128, or 256 down rows)
+constexpr int kTcThreads = 512;            // 16 warps
+// warp roles: epilogue warps are those of lane quarters 0 and 1 (warp % 4 < 2)
+constexpr int kTcWarpProducer = 2, kTcWarpMma = 3;
+__device__ __forceinline__ bool tc_is_sf_warp(int w) { return w == 6 || w == 7 || w == 10 || w == 11; }
+__device__ __forceinline__ bool tc_is_epi_warp(int w) { return (w & 3) < 2; }
+constexpr int kTcEpiWarps = 8;
+constexpr int kTcSfWarps = 4;
+// slot layout (bytes)
+constexpr int kSlotB = 0;                  // weights [256 rows x 128 B] packed E2M1, 128-byte swizzle
+constexpr int kSlotA = 32768;              // activation terms [64 rows x 128 B]; the MMA's rows 64..127 read on (unused)
+constexpr int kSlotSfa = 40960;            // [64 rows x 8 blocks] E8M0 of the activation rows
+constexpr int kSlotAtoms = 41472;          // 6 x [32 rows x 16 B] scale rows for tcgen05.cp: SFA g0, g1, SFB (g, half) x 4
+constexpr int kTcSlotBytes = 45056;
+static_assert(kSlotA % 1024 == 0 && kTcSlotBytes % 1024 == 0, "swizzled operands are 1024-aligned");
+constexpr int kTcScaleEntry = 16384;       // a pair of weight-scale boxes [128 rows x up to 64 B]
+constexpr int kTcScaleRing = 2;
+constexpr int kTcAuxBytes = 3072;
+constexpr int kTcSmemBytes = 1024 /*align slack*/ + kTcStages * kTcSlotBytes + kTcScaleRing * kTcScaleEntry + kTcAuxBytes;
+static_assert(kTcSmemBytes <= 232448, "shared memory of the expert kernel");
+static_assert(kSlotA + 16384 <= kTcStages * kTcSlotBytes, "the MMA's unused activation rows stay inside shared memory");
+// tensor memory columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemAcc = 0;           // [128 lanes x 256 columns] (gate | up, or two down row blocks)
+constexpr uint32_t kTmemSf = 256;          // per slot 24: SFA groups at +0, +4; SFB groups at +8, +16 (8 columns each)
+constexpr uint32_t kTmemSfSlot = 24;
+static_assert(kTmemSf + kTmemSfSlot * kTcStages <= kTmemCols, "tensor memory");
+constexpr int kItemRing = 8;
+// global activation operand layouts (bytes); a "stage" is 256 consecutive K
+//   xb4: [T][H/256][8 term rows][128 B] packed E2M1, 128-byte swizzle (row phase = term)
+//   xsf: [T][H/256][8 term rows][8 blocks]
+//   hb4: [chunk][I/256][64 rows (8p + j)][128 B] swizzled; hsf: [chunk][I/256][64 rows][8 blocks]
+__host__ __device__ constexpr size_t xb4_bytes(int T, int H) { return (size_t)T * (H / 2) * kTcTerms; }
+__host__ __device__ constexpr size_t xsf_bytes(int T, int H) { return (size_t)T * (H / 32) * kTcTerms; }
+__host__ __device__ constexpr size_t hb4_chunk_bytes(int I) { return (size_t)(I / 2) * kTcRowsA; }
+__host__ __device__ constexpr size_t hsf_chunk_bytes(int I) { return (size_t)(I / 32) * kTcRowsA; }
+// Width (bytes = 32-element blocks) of a weight-scale box for K: the largest
+// multiple of 16 that divides K / 32 and is at most 64.
+__host__ __device__ constexpr int scale_box_width(int K) {
+    int w = 64;
+    while (w > 16 && (K / 32) % w) w -= 16;
+    return w;
+}
+
+struct TcMaps {
+    CUtensorMap gate_q, up_q, down_q;   // uint8 [rows, K/2], box {128 B, 128 rows}, 128-byte swizzle
+    CUtensorMap gate_s, up_s, down_s;   // uint8 [rows, K/32], box {scale_box_width(K) B, 128 rows}
+};
+
+struct TcArgs {
+    int H, I, T, layer;
+    const uint8_t* xb4;
+    const uint8_t* xsf;
+    uint8_t* hb4;
+    uint8_t* hsf;
+    float* partial;           // [pairs (t*k + j), H]
+    const ItemRec* items;     // work list (NULL with a routing table)
+    const int* n_items;
+    int* queue;               // zero at the start of the phase
+    int* done;                // [chunks] zero at the start of the phase
+    int* abort;
+    int* status;
+    unsigned long long timeout_ns;
+    int debug_stall;          // testing aid: chunk 0 never signals its gate/up items
+    const RouteTable* rt;     // shared-memory routing table, or NULL
+    unsigned long long* trace;   // [6][256] per-stage timestamps of CTA 0 (profiling), or NULL
+};
+
+// Profiling aid: event `ev` of ring stage / item i of CTA 0.
+__device__ __forceinline__ void tc_trace(const TcArgs& a, int ev, uint32_t i) {
+    if (a.trace && blockIdx.x == 0 && i < 256u) a.trace[ev * 256 + i] = globaltimer_ns();
+}
+
+struct TcSlotMeta {
+    int kind;       // kItemGateUp, kItemDown, or -1 (end of the phase)
+    int stage;      // stage within the item
+    int nstages;
+    int sc;         // scale-box pair counter value of this stage's pair
+    int sc_off;     // byte offset of the stage's 8 scale bytes within a box row
+    int sc_w;       // box row width (bytes)
+    int sc_last;    // last stage reading that pair
+    int pad;
+};
+
+struct TcItemInfo {
+    int kind, e, chunk, rb, ntok, pad0, pad1, pad2;
+    int ids[kTmaTok];   // gate/up: tokens; down: pair ids
+};
+
+struct TcSmem {
+    uint8_t* slots;
+    uint8_t* scales;    // [kTcScaleRing][2 boxes][kTcScaleEntry / 2]
+    uint64_t *full, *empty, *sfr, *accf, *acce, *ringf, *ringe, *sfull, *sempty, *epib, *drain;
+    uint32_t* tmem_slot;
+    TcSlotMeta* meta;
+    TcItemInfo* ring;
+    RouteTable* rt;
+    float* red;   // 64 floats of scratch for the persistent kernel's block reductions
+};
+
+__device__ __forceinline__ TcSmem tc_smem(uint8_t* smem_raw) {
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    TcSmem s;
+    s.slots = smem;
+    s.scales = smem + kTcStages * kTcSlotBytes;
+    uint8_t* aux = s.scales + kTcScaleRing * kTcScaleEntry;
+    uint64_t* b = reinterpret_cast<uint64_t*>(aux);
+    s.full = b; b += kTcStages;
+    s.empty = b; b += kTcStages;
+    s.sfr = b; b += kTcStages;
+    s.accf = b; b += 1;
+    s.acce = b; b += 1;
+    s.ringf = b; b += kItemRing;
+    s.ringe = b; b += kItemRing;
+    s.sfull = b; b += kTcScaleRing;
+    s.sempty = b; b += kTcScaleRing;
+    s.epib = b; b += 1;
+    s.drain = b; b += 1;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(aux + 384);
+    s.meta = reinterpret_cast<TcSlotMeta*>(aux + 400);
+    s.ring = reinterpret_cast<TcItemInfo*>(aux + 640);
+    s.rt = reinterpret_cast<RouteTable*>(aux + 640 + kItemRing * sizeof(TcItemInfo));
+    s.red = reinterpret_cast<float*>(aux + 640 + kItemRing * sizeof(TcItemInfo) + sizeof(RouteTable));
+    return s;
+}
+static_assert(8 * (3 * kTcStages + 2 + 2 * kItemRing + 2 * kTcScaleRing + 2) <= 384, "barriers");
+static_assert(400 + kTcStages * sizeof(TcSlotMeta) <= 640, "slot metadata");
+static_assert(640 + kItemRing * sizeof(TcItemInfo) + sizeof(RouteTable) + 64 * sizeof(float) <= kTcAuxBytes, "aux");
+
+// One thread initialises the barriers; then the block synchronises.
+__device__ __forceinline__ void tc_smem_init(const TcSmem& s) {
+    for (int i = 0; i < kTcStages; ++i) {
+        mbar_init(&s.full[i], 1);
+        mbar_init(&s.empty[i], 1);
+        mbar_init(&s.sfr[i], kTcSfWarps);
+    }
+    mbar_init(s.accf, 1);
+    mbar_init(s.acce, kTcEpiWarps);
+    for (int i = 0; i < kItemRing; ++i) {
+        mbar_init(&s.ringf[i], 1);
+        mbar_init(&s.ringe[i], kTcEpiWarps);
+    }
+    for (int i = 0; i < kTcScaleRing; ++i) {
+        mbar_init(&s.sfull[i], 1);
+        mbar_init(&s.sempty[i], kTcSfWarps);
+    }
+    mbar_init(s.epib, kTcEpiWarps);
+    mbar_init(s.drain, 1);
+    fence_barrier_init();
+}
+
+// Waits on an mbarrier phase until it completes or the deadline passes (drains;
+// ignores the abort flag).
+__device__ __forceinline__ bool drain_phase(uint64_t* bar, uint32_t parity, unsigned long long deadline) {
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() > deadline) return false;
+    return true;
+}
+
+// Waits on an mbarrier phase, bounded by a deadline; false on timeout or abort.
+// The thread sleeps in try_wait between checks (it wakes when the phase completes).
+constexpr uint32_t kSleepHintNs = 20000;
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, unsigned long long deadline,
+                                           const int* abort) {
+    while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
+        if (globaltimer_ns() > deadline) return false;
+        if (*reinterpret_cast<const volatile int*>(abort)) return false;
+    }
+    return true;
+}
+
+// The same wait for a whole warp: the warp leaves together (completion seen by all
+// lanes, or timeout / abort seen by any).
+__device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, unsigned long long deadline,
+                                                const int* abort) {
+    for (;;) {
+        const bool done = mbar_try_wait_sleep(bar, parity, kSleepHintNs);
+        if (__all_sync(0xFFFFFFFFu, done)) return true;
+        const bool stop = globaltimer_ns() > deadline || *reinterpret_cast<const volatile int*>(abort) != 0;
+        if (__any_sync(0xFFFFFFFFu, stop)) return false;
+    }
+}
+
+// Splits the 32 values of one MX block (one per lane) into kTcTerms E2M1 terms:
+// term j encodes the residual r left by terms 0..j-1 as codes c with r ~ c * X,
+// X the power of two with max|r| / X in (3, 6] (round to nearest even on the E2M1
+// grid; a value that rounds past 6 saturates and its excess stays in the residual
+// for the next term).  Its E8M0 scale byte is log2(X) + 127.  A residual that is
+// zero (or below 2^-120) gives zero codes and scale byte 0.  Returns the codes (term
+// j in bits 4j..4j+3) and, in sb0 / sb1, the scale bytes of terms 0-3 / 4-7 (term j
+// in byte j % 4, the same in every lane).
+__device__ __forceinline__ uint32_t split_e2m1_terms(float v, uint32_t& sb0, uint32_t& sb1) {
+    uint32_t codes = 0;
+    sb0 = sb1 = 0;
+    float r = v;
+#pragma unroll
+    for (int j = 0; j < kTcTerms; ++j) {
+        float m = fabsf(r);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const uint32_t eb = __float_as_uint(m) >> 23;   // biased exponent of max|r| (m >= 0)
+        if (eb >= 8u && eb < 255u) {
+            // X = 2^(e-2) with e = eb - 127 puts max|r| / X in [4, 8); halve the ratio when it exceeds 6
+            uint32_t xb = eb - 2u;
+            if (m > 6.0f * __uint_as_float(xb << 23)) ++xb;
+            const float X = __uint_as_float(xb << 23);
+            const float inv = __uint_as_float((254u - xb) << 23);   // 1 / X
+            const uint32_t c = f32_to_e2m1(r * inv);
+            r = fmaf(-e2m1_code_to_f32(c), X, r);   // exact: the code is r / X rounded to the E2M1 grid
+            codes |= c << (4 * j);
+            if (j < 4) sb0 |= xb << (8 * j); else sb1 |= xb << (8 * (j - 4));
+        }
+    }
+    return codes;
+}
+
+// 8x8 nibble transpose inside each group of 8 lanes: lane l returns, for term
+// j = l & 7, the codes of the 8 lanes (l & ~7) + 0..7 (lane i in bits 4i..4i+3).
+__device__ __forceinline__ uint32_t transpose_oct(uint32_t codes, int lane) {
+    const int base = lane & ~7, j = lane & 7;
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t v = __shfl_sync(0xFFFFFFFFu, codes, base + i);
+        w |= ((v >> (4 * j)) & 0xFu) << (4 * i);
+    }
+    return w;
+}
+
+// Stores the activation operand of token t, MX block kb (lane = element): codes into
+// xb4, scale bytes into xsf.  Whole warp.
+__device__ __forceinline__ void store_act_terms(uint8_t* xb4, uint8_t* xsf, int H, int t, int kb, int lane,
+                                                uint32_t codes, uint32_t sb0, uint32_t sb1) {
+    const uint32_t w = transpose_oct(codes, lane);   // term (lane & 7), elements (lane & ~7) .. +7
+    const int j = lane & 7;
+    const int st = kb >> 3;
+    const int byte = (kb & 7) * 16 + (lane >> 3) * 4;   // within the stage's 128-byte row
+    uint8_t* row = xb4 + (((size_t)t * (H / kTcKS) + st) * kTcTerms + j) * 128;
+    *reinterpret_cast<uint32_t*>(row + ((((byte >> 4) ^ j) << 4) | (byte & 15))) = w;
+    if (lane < kTcTerms)
+        xsf[(((size_t)t * (H / kTcKS) + st) * kTcTerms + lane) * 8 + (kb & 7)] =
+            (uint8_t)((lane < 4 ? sb0 : sb1) >> (8 * (lane & 3)));
+}
+
+// ---- producer (one thread) -----------------------------------------------------
+// Claims items until the queue is empty, streams their stages into the ring and
+// publishes an END slot.  The role state carries across phases.  Returns false on
+// a timeout / abort.
+struct TcRoleState {
+    uint32_t it;    // ring position (producer, MMA, scale-factor warps)
+    uint32_t n;     // item ring / accumulator position (producer, MMA, epilogue)
+    uint32_t sc;    // scale-box pairs (producer, scale-factor warps)
+    uint32_t eb;    // epilogue barrier uses
+};
+
+__device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, const TcSmem& s_in,
+                                        TcRoleState& rs_in, unsigned long long deadline) {
+    // arguments and counters in registers (the caller's copies live in local memory)
+    const TcArgs a = a_in;
+    const TcSmem s = s_in;
+    TcRoleState rs = rs_in;
+    const int H = a.H, I = a.I;
+    const int rbu = I / kTmaRows, rbd = H / kTcN;
+    const int n_items = a.rt ? a.rt->n_chunks * (rbu + rbd) : __ldcg(a.n_items);
+    const int wgu = scale_box_width(H), wd = scale_box_width(I);
+    bool failed = false;
+    int next_idx = atomicAdd(a.queue, 1);
+    ItemRec next{};
+    if (next_idx < n_items) next = a.rt ? table_item(a.rt, next_idx, rbu, rbd) : load_item(a.items + next_idx);
+    for (;;) {
+        const int idx = next_idx;
+        const ItemRec cur = next;
+        const bool end = idx >= n_items;
+        if (!end) {
+            next_idx = atomicAdd(a.queue, 1);
+            if (next_idx < n_items) next = a.rt ? table_item(a.rt, next_idx, rbu, rbd) : load_item(a.items + next_idx);
+        }
+        const int kind = end ? -1 : (cur.code >> 30) & 1;
+        const int rb = (cur.code >> 20) & 0x3FF;
+        {   // item record for the epilogue
+            const int re = rs.n % kItemRing;
+            if (!wait_phase(&s.ringe[re], ((rs.n / kItemRing) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
+            TcItemInfo inf;
+            inf.kind = kind;
+            inf.e = cur.e;
+            inf.chunk = cur.chunk;
+            inf.rb = rb;
+            inf.ntok = end ? 0 : cur.ntok;
+            inf.pad0 = inf.pad1 = inf.pad2 = 0;
+#pragma unroll
+            for (int q = 0; q < kTmaTok; ++q) inf.ids[q] = cur.tok[q];
+            s.ring[re] = inf;
+            mbar_arrive(&s.ringf[re]);
+            ++rs.n;
+        }
+        if (end) {
+            const int slot = rs.it % kTcStages;
+            if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
+            s.meta[slot] = TcSlotMeta{-1, 0, 1, 0, 0, 0, 0, 0};
+            mbar_arrive(&s.full[slot]);
+            ++rs.it;
+            break;
+        }
+        const int e = cur.e, ntok = cur.ntok;
+        const bool gu = kind == kItemGateUp;
+        const int nk = gu ? H / kTcKS : I / kTcKS;   // stages of the item
+        // the two 128-row weight boxes of a stage: (gate, up) rows rb*128.. or down rows rb*256.., +128
+        const CUtensorMap* mq0 = gu ? &maps.gate_q : &maps.down_q;
+        const CUtensorMap* mq1 = gu ? &maps.up_q : &maps.down_q;
+        const CUtensorMap* ms0 = gu ? &maps.gate_s : &maps.down_s;
+        const CUtensorMap* ms1 = gu ? &maps.up_s : &maps.down_s;
+        const int r0 = gu ? e * I + rb * kTmaRows : e * H + rb * kTcN;
+        const int r1 = gu ? r0 : r0 + kTmaRows;
+        const int sw = gu ? wgu : wd;                 // scale box width (bytes)
+        const int spb = sw / 8;                        // stages per scale-box pair
+        bool h_ready = gu;
+        for (int st = 0; st < nk; ++st) {
+            if (st % spb == 0) {   // the next pair of weight-scale boxes: blocks 8*st ..
+                const int se = rs.sc % kTcScaleRing;
+                if (!wait_phase(&s.sempty[se], ((rs.sc / kTcScaleRing) & 1) ^ 1, deadline, a.abort)) {
+                    failed = true;
+                    break;
+                }
+                uint8_t* sdst = s.scales + se * kTcScaleEntry;
+                mbar_arrive_expect_tx(&s.sfull[se], 2u * (uint32_t)sw * kTmaRows);
+                tma_load_2d(sdst, ms0, st * 8, r0, &s.sfull[se]);
+                tma_load_2d(sdst + kTcScaleEntry / 2, ms1, st * 8, r1, &s.sfull[se]);
+                ++rs.sc;
+            }
+            const int slot = rs.it % kTcStages;
+            if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
+            s.meta[slot] = TcSlotMeta{kind, st, nk, (int)rs.sc - 1, (st % spb) * 8, sw, st % spb == spb - 1 ? 1 : 0, 0};
+            if (!h_ready) {
+                // every gate/up item of this chunk must have stored its h block
+                uint32_t spins = 0;
+                while (ld_acquire_gpu(a.done + cur.chunk) < rbu) {
+                    if ((++spins & 63u) == 0 &&
+                        (globaltimer_ns() > deadline || *reinterpret_cast<const volatile int*>(a.abort))) {
+                        failed = true;
+                        break;
+                    }
+                }
+                if (failed) break;   // nothing issued on this slot yet
+                fence_proxy_async_global();
+                h_ready = true;
+            }
+            const uint32_t abytes = gu ? (uint32_t)ntok * (1024 + 64) : (uint32_t)(8192 + 512);
+            mbar_arrive_expect_tx(&s.full[slot], 2 * 16384 + abytes);
+            tc_trace(a, 0, rs.it);
+            ++rs.it;   // this slot now has copies in flight
+            uint8_t* dst = s.slots + (size_t)slot * kTcSlotBytes;
+            tma_load_2d(dst + kSlotB, mq0, st * 128, r0, &s.full[slot]);
+            tma_load_2d(dst + kSlotB + 16384, mq1, st * 128, r1, &s.full[slot]);
+            if (st + 3 < nk) {   // three stages ahead into L2
+                tma_prefetch_2d(mq0, (st + 3) * 128, r0);
+                tma_prefetch_2d(mq1, (st + 3) * 128, r1);
+            }
+            if (gu) {
+                for (int p = 0; p < ntok; ++p) {
+                    const size_t ts = (size_t)cur.tok[p] * (H / kTcKS) + st;
+                    bulk_load(dst + kSlotA + p * 1024, a.xb4 + ts * 1024, 1024, &s.full[slot]);
+                    bulk_load(dst + kSlotSfa + p * 64, a.xsf + ts * 64, 64, &s.full[slot]);
+                }
+            } else {
+                const size_t cs = (size_t)cur.chunk * (I / kTcKS) + st;
+                bulk_load(dst + kSlotA, a.hb4 + cs * 8192, 8192, &s.full[slot]);
+                bulk_load(dst + kSlotSfa, a.hsf + cs * 512, 512, &s.full[slot]);
+            }
+        }
+        if (failed) break;
+    }
+    if (failed) {
+        if (atomicExch(a.abort, 1) == 0) raise_status(a.status, MOE_ERR_TIMEOUT, a.layer * 65536);
+        // every copy this CTA issued must land before the CTA exits
+        const uint32_t issued = rs.it < (uint32_t)kTcStages ? rs.it : (uint32_t)kTcStages;
+        for (uint32_t q = 0; q < issued; ++q) {
+            const uint32_t last = rs.it - 1 - q;
+            drain_phase(&s.full[last % kTcStages], (last / kTcStages) & 1, globaltimer_ns() + a.timeout_ns);
+        }
+        const uint32_t sissued = rs.sc < (uint32_t)kTcScaleRing ? rs.sc : (uint32_t)kTcScaleRing;
+        for (uint32_t q = 0; q < sissued; ++q) {
+            const uint32_t last = rs.sc - 1 - q;
+            drain_phase(&s.sfull[last % kTcScaleRing], (last / kTcScaleRing) & 1, globaltimer_ns() + a.timeout_ns);
+        }
+    }
+    rs_in = rs;
+    return !failed;
+}
+
+// ---- MMA issuer (one thread) -----------------------------------------------------
+__device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint32_t tmem, TcRoleState& rs_in,
+                                    unsigned long long deadline) {
+    const TcArgs a = a_in;
+    const TcSmem s = s_in;
+    TcRoleState rs = rs_in;
+    constexpr uint32_t kIdesc = idesc_mxf4(128, kTcN);
+    const uint32_t slots = smem_u32(s.slots);
+    bool failed = false;
+    for (;;) {
+        const int slot = rs.it % kTcStages;
+        if (!wait_phase(&s.sfr[slot], (rs.it / kTcStages) & 1, deadline, a.abort)) { failed = true; break; }
+        tc_trace(a, 3, rs.it);
+        const TcSlotMeta m = s.meta[slot];
+        if (m.kind < 0) {   // END: release the slot and wake the epilogue
+            mbar_arrive(&s.empty[slot]);
+            ++rs.it;
+            if (!wait_phase(s.acce, (rs.n & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
+            mbar_arrive(s.accf);
+            ++rs.n;
+            break;
+        }
+        if (m.stage == 0) {   // the accumulator must have been read out
+            if (!wait_phase(s.acce, (rs.n & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
+            tc_fence_after();
+        }
+        const uint32_t sl = slots + (uint32_t)slot * kTcSlotBytes;
+        const uint32_t sf = tmem + kTmemSf + kTmemSfSlot * slot;
+#pragma unroll
+        for (int g = 0; g < 6; ++g)   // SFA g0, g1 -> +0, +4; SFB (g, half) -> +8 + 8g + 4 half
+            tc_cp_32x128_x4(sf + 4 * g, smem_desc_rows16(sl + kSlotAtoms + 512 * g));
+        const uint64_t ad = smem_desc_sw128(sl + kSlotA), bd = smem_desc_sw128(sl + kSlotB);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {   // K = 64 each: blocks 2kk, 2kk+1
+            const uint32_t id = 2 * (kk & 1);
+            tc_mma_mxf4(tmem + kTmemAcc, ad + 2 * kk, bd + 2 * kk, kIdesc | idesc_sf_ids(id, id), sf + 4 * (kk >> 1),
+                        sf + 8 + 8 * (kk >> 1), (m.stage == 0 && kk == 0) ? 0u : 1u);
+        }
+        tc_commit(&s.empty[slot]);
+        if (m.stage == m.nstages - 1) {
+            tc_commit(s.accf);
+            ++rs.n;
+        }
+        tc_trace(a, 4, rs.it);
+        ++rs.it;
+    }
+    if (failed && atomicExch(a.abort, 1) == 0) raise_status(a.status, MOE_ERR_TIMEOUT, a.layer * 65536);
+    rs_in = rs;
+    return !failed;
+}
+
+// ---- scale-factor warps ------------------------------------------------------------
+// The MMA reads activation row m's scales from lane m, column base + m / 32, and
+// weight row n's scales from lane n % 32 of the reading row's quarter, column
+// base + n / 32 (one 32-bit cell = 4 blocks; group g = blocks 4g..4g+3 of the
+// stage).  tcgen05.cp 32x128b.warpx4 puts 16-byte row r of a 512-byte block into
+// columns +0..3 of lane r of every quarter, so the blocks are: SFA group g, row r =
+// cells of activation rows r, 32 + r (rows 64.. unused); SFB group g, half h, row
+// r = cells of weight rows 128h + r, 128h + 32 + r, 128h + 64 + r, 128h + 96 + r.
+// Scale-factor warp w (0..3) handles rows 32w + lane of both weight boxes and, for
+// w < 2, activation row 32w + lane.
+__device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, TcRoleState& rs_in, int w, int lane,
+                                   unsigned long long deadline) {
+    const TcArgs a = a_in;
+    const TcSmem s = s_in;
+    TcRoleState rs = rs_in;
+    bool failed = false;
+    for (;;) {
+        const int slot = rs.it % kTcStages;
+        if (!warp_wait_phase(&s.full[slot], (rs.it / kTcStages) & 1, deadline, a.abort)) { failed = true; break; }
+        const TcSlotMeta m = s.meta[slot];
+        if (w == 0 && lane == 0) tc_trace(a, 1, rs.it);
+        if (m.kind >= 0) {
+            const int se = m.sc % kTcScaleRing;
+            if (!warp_wait_phase(&s.sfull[se], (m.sc / kTcScaleRing) & 1, deadline, a.abort)) { failed = true; break; }
+            uint8_t* sl = s.slots + (size_t)slot * kTcSlotBytes;
+            uint32_t* at = reinterpret_cast<uint32_t*>(sl + kSlotAtoms);
+            uint32_t ff = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint2 v = *reinterpret_cast<const uint2*>(s.scales + se * kTcScaleEntry + h * (kTcScaleEntry / 2) +
+                                                                (32 * w + lane) * m.sc_w + m.sc_off);
+                at[(2 + 0 * 2 + h) * 128 + lane * 4 + w] = v.x;   // SFB group 0, half h
+                at[(2 + 1 * 2 + h) * 128 + lane * 4 + w] = v.y;   // SFB group 1, half h
+                ff |= (v.x & (v.x >> 1) & (v.x >> 2) & (v.x >> 3) & (v.x >> 4) & (v.x >> 5) & (v.x >> 6) & (v.x >> 7) &
+                       0x01010101u) |
+                      (v.y & (v.y >> 1) & (v.y >> 2) & (v.y >> 3) & (v.y >> 4) & (v.y >> 5) & (v.y >> 6) & (v.y >> 7) &
+                       0x01010101u);
+            }
+            if (ff) raise_status(a.status, MOE_ERR_BAD_SCALE, a.layer * 65536);   // scale byte 0xFF (NaN)
+            if (w < 2) {
+                const uint2 v = *reinterpret_cast<const uint2*>(sl + kSlotSfa + (32 * w + lane) * 8);
+                at[0 * 128 + lane * 4 + w] = v.x;
+                at[1 * 128 + lane * 4 + w] = v.y;
+            }
+            fence_proxy_async_shared();   // read next by tcgen05.cp
+            __syncwarp();
+            if (m.sc_last && lane == 0) mbar_arrive(&s.sempty[se]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.sfr[slot]);
+        if (w == 0 && lane == 0) tc_trace(a, 2, rs.it);
+        ++rs.it;
+        if (m.kind < 0) break;
+    }
+    if (failed && lane == 0 && atomicExch(a.abort, 1) == 0) raise_status(a.status, MOE_ERR_TIMEOUT, a.layer * 65536);
+    rs_in = rs;
+    return !failed;
+}
+
+// Reduce-scatter of 32 values over the 8 lanes of each lane group (lane & 7): lane
+// j returns the group sums of values j, j + 8, j + 16, j + 24 (halving butterfly,
+// partner offsets 4, 2, 1; a fixed order, the same on every run).
+__device__ __forceinline__ void group8_reduce_scatter(const float (&v)[32], float (&out)[4], int lane) {
+    float a16[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {   // keep values with bit 2 of the index == bit 2 of the lane
+        const int k0 = (i & 3) | ((i >> 2) << 3), k1 = k0 | 4;   // pairs differing in bit 2
+        const bool hi = (lane & 4) != 0;
+        const float send = hi ? v[k0] : v[k1], keep = hi ? v[k1] : v[k0];
+        a16[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+    }
+    // a16[i] now stands for index k = (i & 3) | (bit2 of lane) << 2 | (i >> 2) << 3
+    float a8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {   // pairs differing in bit 1 of k: a16 indices (i&1) | ((i>>1)<<2) and +2
+        const int i0 = (i & 1) | ((i >> 1) << 2), i1 = i0 | 2;
+        const bool hi = (lane & 2) != 0;
+        const float send = hi ? a16[i0] : a16[i1], keep = hi ? a16[i1] : a16[i0];
+        a8[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+    }
+    // a8[i]: k = (i & 1) | (bit1 of lane) << 1 | (bit2 of lane) << 2 | (i >> 1) << 3
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {   // pairs differing in bit 0 of k: a8 indices 2i and 2i+1
+        const bool hi = (lane & 1) != 0;
+        const float send = hi ? a8[2 * i] : a8[2 * i + 1], keep = hi ? a8[2 * i + 1] : a8[2 * i];
+        out[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+    }
+    // out[i]: k = (lane & 7) | i << 3
+}
+
+// ---- epilogue warps (lane quarter q = warp % 4 < 2, column chunk c = warp / 4) -----
+// Accumulator lane 32q + l is activation row 32q + l: pair slot 4q + l / 8, term l % 8.
+// The warp reads columns 32c.. (gate rows / first down block) and 128 + 32c.. (up
+// rows / second down block): after the reduce-scatter lane l holds, for its pair,
+// the sums of columns 32c + 8s + (l % 8) and 128 + 32c + 8s + (l % 8), s = 0..3.
+__device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in, uint32_t tmem, TcRoleState& rs_in,
+                                         int warp, int lane, unsigned long long deadline) {
+    const TcArgs a = a_in;
+    const TcSmem s = s_in;
+    TcRoleState rs = rs_in;
+    const int q = warp & 3, c = warp >> 2;
+    const int H = a.H, I = a.I;
+    const int p = 4 * q + (lane >> 3), j = lane & 7;   // pair slot and term of this lane's row
+    bool failed = false;
+    // barrier of the epilogue warps (bounded)
+    auto epi_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s.epib);
+        const bool ok = warp_wait_phase(s.epib, rs.eb & 1, deadline, a.abort);
+        ++rs.eb;
+        return ok;
+    };
+    for (;;) {
+        const int re = rs.n % kItemRing;
+        if (!warp_wait_phase(s.accf, rs.n & 1, deadline, a.abort) ||
+            !warp_wait_phase(&s.ringf[re], (rs.n / kItemRing) & 1, deadline, a.abort)) {
+            failed = true;
+            break;
+        }
+        const TcItemInfo inf = s.ring[re];
+        tc_fence_after();
+        if (warp == 0 && lane == 0) tc_trace(a, 5, rs.n);
+        float G[4], U[4];
+        if (inf.kind >= 0) {
+            uint32_t r0[32], r1[32];
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemAcc + 32 * c;
+            tc_ld_x32(ta, r0);
+            tc_ld_x32(ta + 128, r1);
+            tc_wait_ld();
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
+            group8_reduce_scatter(v, G, lane);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r1[i]);
+            group8_reduce_scatter(v, U, lane);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(s.acce);
+            mbar_arrive(&s.ringe[re]);
+        }
+        ++rs.n;
+        if (inf.kind < 0) break;
+        const bool mine = p < inf.ntok;
+        if (inf.kind == kItemGateUp) {
+            // h = silu(g) * u for rows 32c + 8s + j of the item's 128 (s = 0..3); the 32
+            // rows 32c.. are one MX block of the down projection's K.  Split into 8 E2M1
+            // terms with block scales over the pair's 8 lanes, stored as rows 8p + t of
+            // the chunk's down operand at K = rb * 128 + 32c + 8s + j.
+            float hv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hv[i] = silu(G[i]) * U[i];
+            uint32_t codes[4] = {0u, 0u, 0u, 0u};   // per s: term t in bits 4t..4t+3
+            uint32_t sbt = 0;                        // this lane's scale byte: term j
+#pragma unroll
+            for (int t = 0; t < kTcTerms; ++t) {
+                float mx = fmaxf(fmaxf(fabsf(hv[0]), fabsf(hv[1])), fmaxf(fabsf(hv[2]), fabsf(hv[3])));
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+                const uint32_t eb = __float_as_uint(mx) >> 23;
+                if (eb >= 8u && eb < 255u) {
+                    uint32_t xb = eb - 2u;
+                    if (mx > 6.0f * __uint_as_float(xb << 23)) ++xb;
+                    const float X = __uint_as_float(xb << 23);
+                    const float inv = __uint_as_float((254u - xb) << 23);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t cd = f32_to_e2m1(hv[i] * inv);
+                        hv[i] = fmaf(-e2m1_code_to_f32(cd), X, hv[i]);
+                        codes[i] |= cd << (4 * t);
+                    }
+                    if (t == j) sbt = xb;
+                }
+            }
+            // lane j of the pair gets term j's codes of the pair's 8 lanes, for each s
+            uint32_t wd[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wd[i] = transpose_oct(codes[i], lane);
+            if (mine) {
+                uint8_t* hb = a.hb4 + (size_t)inf.chunk * hb4_chunk_bytes(I) + (size_t)(inf.rb >> 1) * 8192;
+                const int n = 8 * p + j;                        // operand row: pair slot p, term j
+                const int chunk16 = (inf.rb & 1) * 4 + c;       // 16-byte chunk of K (rb&1)*128 + 32c .. +31
+                *reinterpret_cast<uint4*>(hb + n * 128 + ((chunk16 ^ (n & 7)) << 4)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                a.hsf[(size_t)inf.chunk * hsf_chunk_bytes(I) + (size_t)(inf.rb >> 1) * 512 + n * 8 + 4 * (inf.rb & 1) + c] =
+                    (uint8_t)sbt;
+            }
+            fence_proxy_async_global();   // read next by bulk copies
+            if (!epi_sync()) { failed = true; break; }
+            if (warp == 0 && lane == 0 && !(a.debug_stall && inf.chunk == 0)) {
+                __threadfence();
+                fence_proxy_async_global();
+                red_release_add_gpu(a.done + inf.chunk, 1);
+            }
+        } else if (mine) {   // down: rows rb * 256 + 32c + 8s + j and + 128
+            float* dst = a.partial + (size_t)inf.ids[p] * H + (size_t)inf.rb * kTcN + 32 * c + j;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dst[8 * i] = G[i];
+                dst[128 + 8 * i] = U[i];
+            }
+        }
+    }
+    if (failed && lane == 0 && atomicExch(a.abort, 1) == 0) raise_status(a.status, MOE_ERR_TIMEOUT, a.layer * 65536);
+    rs_in = rs;
+    return !failed;
+}
+
+// One expert phase, dispatched by warp role; every thread of the block calls it.
+__device__ __forceinline__ void tc_phase(const TcMaps& maps, const TcArgs& a, const TcSmem& s, uint32_t tmem,
+                                         TcRoleState& rs, unsigned long long deadline) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == kTcWarpProducer) {
+        if (lane == 0) tc_produce(maps, a, s, rs, deadline);
+    } else if (warp == kTcWarpMma) {
+        if (lane == 0) tc_mma(a, s, tmem, rs, deadline);
+    } else if (tc_is_sf_warp(warp)) {
+        tc_sf(a, s, rs, (warp == 6) ? 0 : (warp == 7) ? 1 : (warp == 10) ? 2 : 3, lane, deadline);
+    } else if (tc_is_epi_warp(warp)) {
+        tc_epilogue(a, s, tmem, rs, warp, lane, deadline);
+    }
+}
+
+// Setup shared by the standalone and persistent kernels: barriers (thread 0) and
+// the tensor-memory allocation (the MMA warp).  Ends with a block-wide barrier.
+__device__ __forceinline__ uint32_t tc_setup(const TcSmem& s) {
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) tc_smem_init(s);
+    if (warp == kTcWarpMma) {
+        tmem_alloc(s.tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    return *s.tmem_slot;
+}
+
+// Teardown: every tcgen05 operation of the MMA thread has completed (bounded
+// wait), then the MMA warp frees the tensor memory.  All threads call it.
+__device__ __forceinline__ void tc_teardown(const TcSmem& s, uint32_t tmem, unsigned long long timeout_ns) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == kTcWarpMma && lane == 0) {
+        tc_commit(s.drain);
+        drain_phase(s.drain, 0, globaltimer_ns() + timeout_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kTcWarpMma) tmem_dealloc(tmem, kTmemCols);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) expert_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const TcSmem s = tc_smem(smem_raw);
+    const uint32_t tmem = tc_setup(s);
+    const unsigned long long deadline = globaltimer_ns() + args.timeout_ns;
+    if (threadIdx.x == kTcWarpProducer * 32) {
+        prefetch_tensormap(&maps.gate_q);
+        prefetch_tensormap(&maps.up_q);
+        prefetch_tensormap(&maps.down_q);
+        prefetch_tensormap(&maps.gate_s);
+        prefetch_tensormap(&maps.up_s);
+        prefetch_tensormap(&maps.down_s);
+    }
+    TcRoleState rs{0u, 0u, 0u, 0u};
+    tc_phase(maps, args, s, tmem, rs, deadline);
+    tc_teardown(s, tmem, args.timeout_ns);
+}
+
+// Input staging of one layer, one block of 1024 threads per token:
+//   norm_w == NULL: act[t] = fp32(x[t]) (x bf16), and resid[t] = act[t] when resid != NULL;
+//   norm_w != NULL: act[t] = resid[t] * w / sqrt(mean(resid[t]^2) + eps)  (RMSNorm);
+// then the expert operand of act[t]: 8 E2M1 terms per MX block (xb4, xsf).
+constexpr int kPrepThreads = 1024;
+__global__ void __launch_bounds__(kPrepThreads) prep_layer_kernel(const __nv_bfloat16* __restrict__ x, int T, int H,
+                                                                  float* resid, const __nv_bfloat16* __restrict__ norm_w,
+                                                                  float eps, float* __restrict__ act,
+                                                                  uint8_t* __restrict__ xb4, uint8_t* __restrict__ xsf) {
+    __shared__ float red[32];
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kPer = 16;   // H <= 16384: at most 16 values per thread
+    float v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int h = threadIdx.x + i * kPrepThreads;
+        v[i] = 0.0f;
+        if (h < H) v[i] = norm_w ? resid[(size_t)t * H + h] : __bfloat162float(x[(size_t)t * H + h]);
+    }
+    if (norm_w) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) ss = fmaf(v[i], v[i], ss);
+        ss = warp_sum(ss);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float tot = 0.0f;
+        for (int i = 0; i < 32; ++i) tot += red[i];
+        const float inv = 1.0f / sqrtf(tot / (float)H + eps);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int h = threadIdx.x + i * kPrepThreads;
+            if (h < H) v[i] = v[i] * inv * __bfloat162float(norm_w[h]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int h = threadIdx.x + i * kPrepThreads;   // block (h / 32) = 32 i + warp, element lane
+        if (i * kPrepThreads < H) {                      // warp-uniform (H is a multiple of 1024 or the tail is whole blocks)
+            if (h < H) {
+                act[(size_t)t * H + h] = v[i];
+                if (resid && !norm_w) resid[(size_t)t * H + h] = v[i];
+            }
+            if (h - lane < H) {
+                uint32_t sb0, sb1;
+                const uint32_t codes = split_e2m1_terms(v[i], sb0, sb1);
+                store_act_terms(xb4, xsf, H, t, h / 32, lane, codes, sb0, sb1);
+            }
+        }
+    }
+}
+
+}  // namespace moe

@@ -12,7 +12,7 @@
 
 #include "common.cuh"
 #include "expert_simple.cuh"
-#include "expert_tma.cuh"
+#include "expert_tc.cuh"
 #include "layer_ops.cuh"
 #include "persist.cuh"
 #include "route.cuh"
@@ -20,7 +20,7 @@
 struct moe_mxfp4_handle {
     moe_mxfp4_config cfg;
     std::vector<moe_mxfp4_layer> layers;
-    std::vector<moe::TmaMaps> maps;   // per layer, when the TMA expert path applies
+    std::vector<moe::TcMaps> maps;    // per layer, when the tensor-core expert path applies
     bool tma = false;
     int persist_grid = 0;              // CTAs of the persistent forward (one per SM), 0 = unavailable
     int device = 0;
@@ -38,15 +38,17 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // Byte offsets of the workspace sections for T tokens.
 struct WsLayout {
     size_t status, xstage, ystage, act, resid, logits, idx, gate, counts, offsets, perm, active, hbuf, partial;
-    size_t act16, act_fac, ss, tickets, h16, h_scale, items, sync, rpart, total;
+    size_t xb4, xsf, ss, tickets, hb4, hsf, items, sync, rpart, total;
 };
 
-// Upper bound of the work items of one layer: every routed expert contributes
-// ceil(n_e / 8) token chunks, i.e. at most T*k/8 + min(E, T*k) chunks.
-size_t max_items(const moe_mxfp4_config& c, int T) {
+// Upper bound of the chunks of one layer: every routed expert contributes
+// ceil(n_e / 8) chunks of its pairs, i.e. at most T*k/8 + min(E, T*k).
+size_t max_chunks(const moe_mxfp4_config& c, int T) {
     const size_t pairs = (size_t)T * c.top_k;
-    const size_t chunks = (pairs + moe::kTmaTok - 1) / moe::kTmaTok + std::min<size_t>(c.num_experts, pairs);
-    return chunks * (size_t)(c.inter / moe::kTmaRows + c.hidden / moe::kTmaRows);
+    return (pairs + moe::kTmaTok - 1) / moe::kTmaTok + std::min<size_t>(c.num_experts, pairs);
+}
+size_t max_items(const moe_mxfp4_config& c, int T) {
+    return max_chunks(c, T) * (size_t)(c.inter / moe::kTmaRows + c.hidden / moe::kTmaRows);
 }
 
 WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
@@ -54,7 +56,7 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     const size_t H = (size_t)c.hidden, I = (size_t)c.inter, E = (size_t)c.num_experts, k = (size_t)c.top_k;
-    L.status = take(512);   // status words, grid-barrier counters, persistent-forward phase timestamps
+    L.status = take(16384);   // status words, grid-barrier counters, phase timestamps, expert-phase trace
     L.xstage = take((size_t)T * H * 2);
     L.ystage = take((size_t)T * H * 4);
     L.act = take((size_t)T * H * 4);
@@ -68,14 +70,15 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     L.active = take((E + 1) * 4);
     L.hbuf = take((size_t)T * k * I * 4);
     L.partial = take((size_t)T * k * H * 4);
-    L.act16 = take((size_t)T * H * 2);
-    L.act_fac = take((size_t)T * (H / 128) * 4);
+    const size_t chunks = max_chunks(c, T);
+    L.xb4 = take(moe::xb4_bytes(T, (int)H));
+    L.xsf = take(moe::xsf_bytes(T, (int)H));
     L.ss = take((size_t)T * (H / 1024 + 1) * 4);
-    L.tickets = take((size_t)moe::kMaxPersistLayers * (E + 1) * 4);   // per-layer queue + done counters
-    L.h16 = take((size_t)T * k * I * 2);
-    L.h_scale = take((size_t)T * k * (I / 128) * 4);
+    L.tickets = take((size_t)moe::kMaxPersistLayers * (1 + chunks) * 4);   // per-layer queue + per-chunk done counters
+    L.hb4 = take(chunks * moe::hb4_chunk_bytes((int)I));
+    L.hsf = take(chunks * moe::hsf_chunk_bytes((int)I));
     L.items = take(max_items(c, T) * sizeof(moe::ItemRec));
-    L.sync = take((8 + 2 * E) * 4);   // n_items[2], queue, abort, ..., done[E], need[E]
+    L.sync = take((8 + chunks) * 4);   // n_items[2], queue, abort, ..., done[chunks]
     L.rpart = take((size_t)(H / 512 + 1) * T * E * 4);   // router partials per 512- or 1024-column slice
     L.total = o;
     return L;
@@ -130,14 +133,17 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t ro
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_maps(const moe_mxfp4_config& c, const moe_mxfp4_layer& l, moe::TmaMaps* m) {
+bool make_maps(const moe_mxfp4_config& c, const moe_mxfp4_layer& l, moe::TcMaps* m) {
     const uint64_t H = c.hidden, I = c.inter, E = c.num_experts;
+    // codes: [128 B x 128 rows] boxes (one 256-element stage), 128-byte swizzle;
+    // scales: boxes of scale_box_width(K) bytes (several stages) x 128 rows
+    const uint32_t wh = moe::scale_box_width((int)H), wi = moe::scale_box_width((int)I);
     return encode_2d(&m->gate_q, l.gate_q_dev, H / 2, E * I, 128, true) &&
            encode_2d(&m->up_q, l.up_q_dev, H / 2, E * I, 128, true) &&
            encode_2d(&m->down_q, l.down_q_dev, I / 2, E * H, 128, true) &&
-           encode_2d(&m->gate_s, l.gate_s_dev, H / 32, E * I, 16, false) &&
-           encode_2d(&m->up_s, l.up_s_dev, H / 32, E * I, 16, false) &&
-           encode_2d(&m->down_s, l.down_s_dev, I / 32, E * H, 16, false);
+           encode_2d(&m->gate_s, l.gate_s_dev, H / 32, E * I, wh, false) &&
+           encode_2d(&m->up_s, l.up_s_dev, H / 32, E * I, wh, false) &&
+           encode_2d(&m->down_s, l.down_s_dev, I / 32, E * H, wi, false);
 }
 
 moe::RouteBufs route_bufs(char* ws, const WsLayout& L) {
@@ -205,18 +211,8 @@ int forward_multi_kernel(moe_mxfp4_handle* h, const void* x, int T, void* y, cha
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// Forward with the warp-specialised TMA expert kernel: per layer, routing and
-// grouping kernels, the work list, one persistent expert launch, the combine.
-int forward_tma(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, const WsLayout& L, cudaStream_t st,
-                const moe_mxfp4_debug* dbg) {
-    const moe_mxfp4_config& c = h->cfg;
-    const int H = c.hidden, I = c.inter, E = c.num_experts, k = c.top_k;
-    const bool norm = (c.flags & MOE_FLAG_NORM) != 0;
-    const int y_bf16 = (c.flags & MOE_FLAG_OUT_BF16) ? 1 : 0;
-    int* status = reinterpret_cast<int*>(ws + L.status);
-    float* act = reinterpret_cast<float*>(ws + L.act);
-    float* resid = norm ? reinterpret_cast<float*>(ws + L.resid) : nullptr;
-    const moe::RouteBufs rb = route_bufs(ws, L);
+// Work list / counters of a forward in the workspace.
+moe::WorkList work_list(char* ws, const WsLayout& L) {
     int* sync = reinterpret_cast<int*>(ws + L.sync);
     moe::WorkList wl;
     wl.items = reinterpret_cast<moe::ItemRec*>(ws + L.items);
@@ -224,43 +220,73 @@ int forward_tma(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, co
     wl.queue = sync + 2;
     wl.abort = sync + 3;
     wl.done = sync + 8;
-    wl.need = sync + 8 + E;
-    moe::ExpertArgs ea;
-    ea.H = H; ea.I = I; ea.k = k;
-    ea.act16 = reinterpret_cast<const __half*>(ws + L.act16);
-    ea.act_fac = reinterpret_cast<const float*>(ws + L.act_fac);
-    ea.h16 = reinterpret_cast<__half*>(ws + L.h16);
-    ea.h_scale = reinterpret_cast<float*>(ws + L.h_scale);
-    ea.partial = reinterpret_cast<float*>(ws + L.partial);
-    ea.rb = rb;
-    ea.wl = wl;
-    ea.status = status;
-    ea.timeout_ns = (unsigned long long)c.timeout_us * 1000ull;
-    ea.debug_stall = (c.flags & MOE_FLAG_DEBUG_STALL) ? 1 : 0;
-    ea.rt = nullptr;
+    return wl;
+}
+
+// Expert-phase arguments shared by both tensor-core paths (per-layer fields set by the caller).
+moe::TcArgs tc_args(const moe_mxfp4_handle* h, int T, char* ws, const WsLayout& L) {
+    const moe_mxfp4_config& c = h->cfg;
+    moe::TcArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.H = c.hidden;
+    a.I = c.inter;
+    a.T = T;
+    a.xb4 = reinterpret_cast<const uint8_t*>(ws + L.xb4);
+    a.xsf = reinterpret_cast<const uint8_t*>(ws + L.xsf);
+    a.hb4 = reinterpret_cast<uint8_t*>(ws + L.hb4);
+    a.hsf = reinterpret_cast<uint8_t*>(ws + L.hsf);
+    a.partial = reinterpret_cast<float*>(ws + L.partial);
+    a.status = reinterpret_cast<int*>(ws + L.status);
+    a.timeout_ns = (unsigned long long)c.timeout_us * 1000ull;
+    a.debug_stall = (c.flags & MOE_FLAG_DEBUG_STALL) ? 1 : 0;
+    a.trace = nullptr;
+    return a;
+}
+
+// Forward with the tensor-core expert kernel, one launch per phase: per layer the
+// input staging (+ operand), router slices, top-k and grouping, the work list, one
+// persistent expert launch, the combine.
+int forward_tma(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, const WsLayout& L, cudaStream_t st,
+                const moe_mxfp4_debug* dbg) {
+    const moe_mxfp4_config& c = h->cfg;
+    const int H = c.hidden, I = c.inter, E = c.num_experts, k = c.top_k;
+    const bool norm = (c.flags & MOE_FLAG_NORM) != 0;
+    const int y_bf16 = (c.flags & MOE_FLAG_OUT_BF16) ? 1 : 0;
+    float* act = reinterpret_cast<float*>(ws + L.act);
+    float* resid = norm ? reinterpret_cast<float*>(ws + L.resid) : nullptr;
+    const moe::RouteBufs rb = route_bufs(ws, L);
+    const moe::WorkList wl = work_list(ws, L);
+    moe::TcArgs ta = tc_args(h, T, ws, L);
+    ta.items = wl.items;
+    ta.n_items = wl.n_items;
+    ta.queue = wl.queue;
+    ta.done = wl.done;
+    ta.abort = wl.abort;
+    uint8_t* xb4 = reinterpret_cast<uint8_t*>(ws + L.xb4);
+    uint8_t* xsf = reinterpret_cast<uint8_t*>(ws + L.xsf);
     const size_t sel_smem = (size_t)(33 * E + 64) * sizeof(int);
     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
     if (norm)   // r_0 = x
-        moe::prep_layer_kernel<<<T, moe::kPrepThreads, 0, st>>>(xb, H, resid, nullptr, 0.0f, act,
-                                                                const_cast<__half*>(ea.act16),
-                                                                const_cast<float*>(ea.act_fac));
+        moe::prep_layer_kernel<<<T, moe::kPrepThreads, 0, st>>>(xb, T, H, resid, nullptr, 0.0f, act, xb4, xsf);
     for (int l = 0; l < c.num_layers; ++l) {
         const moe_mxfp4_layer& ly = h->layers[l];
         moe::prep_layer_kernel<<<T, moe::kPrepThreads, 0, st>>>(
-            xb, H, resid, norm ? reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev) : nullptr, c.rms_eps, act,
-            const_cast<__half*>(ea.act16), const_cast<float*>(ea.act_fac));
+            xb, T, H, resid, norm ? reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev) : nullptr, c.rms_eps, act,
+            xb4, xsf);
         float* rpart = reinterpret_cast<float*>(ws + L.rpart);
         moe::route_partial_kernel<<<dim3((E + 31) / 32, H / moe::kRouteSlice), 256, 0, st>>>(
             act, T, H, reinterpret_cast<const __nv_bfloat16*>(ly.router_w_dev), E, rpart);
         moe::route_select_kernel<<<1, 1024, sel_smem, st>>>(rb.logits, T, E, k, h->e_begin, h->e_end, rb, rpart,
                                                              H / moe::kRouteSlice, ly.router_b_dev);
         moe::build_items_kernel<<<1, 1024, (size_t)T * k * sizeof(int), st>>>(rb, H, I, k, wl, T);
-        ea.layer = l;
+        ta.layer = l;
+        ta.trace = (l == 0 && (c.flags & MOE_FLAG_TRACE)) ? reinterpret_cast<unsigned long long*>(ws + L.status + 4096)
+                                                         : nullptr;
         if (dbg && dbg->expert_events) cudaEventRecord(static_cast<cudaEvent_t>(dbg->expert_events[2 * l]), st);
-        moe::expert_tma_kernel<<<h->sm_count, moe::kTmaThreads, moe::kTmaSmemBytes, st>>>(h->maps[l], ea);
+        moe::expert_tc_kernel<<<h->sm_count, moe::kTcThreads, moe::kTcSmemBytes, st>>>(h->maps[l], ta);
         if (dbg && dbg->expert_events) cudaEventRecord(static_cast<cudaEvent_t>(dbg->expert_events[2 * l + 1]), st);
         const bool last = l == c.num_layers - 1;
-        moe::combine_kernel<<<dim3(T, (H + 1023) / 1024), 256, 0, st>>>(ea.partial, rb, H, k, h->e_begin, h->e_end,
+        moe::combine_kernel<<<dim3(T, (H + 1023) / 1024), 256, 0, st>>>(ta.partial, rb, H, k, h->e_begin, h->e_end,
                                                                         resid, last ? y : nullptr, y_bf16);
         copy_debug(dbg, l, T, E, k, rb, st);
     }
@@ -271,11 +297,10 @@ int forward_tma(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, co
 int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char* ws, const WsLayout& L,
                        cudaStream_t st, const moe_mxfp4_debug* dbg) {
     const moe_mxfp4_config& c = h->cfg;
-    const int H = c.hidden, I = c.inter, E = c.num_experts, k = c.top_k;
-    int* sync = reinterpret_cast<int*>(ws + L.sync);
+    const int H = c.hidden, E = c.num_experts, k = c.top_k;
     moe::PersistParams p;
     std::memset(&p, 0, sizeof(p));
-    p.T = T; p.H = H; p.I = I; p.E = E; p.k = k;
+    p.T = T; p.H = H; p.I = c.inter; p.E = E; p.k = k;
     p.e_begin = h->e_begin; p.e_end = h->e_end;
     p.y_bf16 = (c.flags & MOE_FLAG_OUT_BF16) ? 1 : 0;
     p.norm = (c.flags & MOE_FLAG_NORM) ? 1 : 0;
@@ -283,28 +308,19 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     p.x = reinterpret_cast<const __nv_bfloat16*>(x);
     p.y = y;
     p.resid = reinterpret_cast<float*>(ws + L.resid);
-    p.act16 = reinterpret_cast<__half*>(ws + L.act16);
-    p.act_fac = reinterpret_cast<float*>(ws + L.act_fac);
+    p.xb4 = reinterpret_cast<uint8_t*>(ws + L.xb4);
+    p.xsf = reinterpret_cast<uint8_t*>(ws + L.xsf);
     p.ss = reinterpret_cast<float*>(ws + L.ss);
     p.rpart = reinterpret_cast<float*>(ws + L.rpart);
-    moe::ExpertArgs& ea = p.ea;
-    ea.H = H; ea.I = I; ea.k = k; ea.layer = 0;
-    ea.act16 = p.act16;
-    ea.act_fac = p.act_fac;
-    ea.h16 = reinterpret_cast<__half*>(ws + L.h16);
-    ea.h_scale = reinterpret_cast<float*>(ws + L.h_scale);
-    ea.partial = reinterpret_cast<float*>(ws + L.partial);
-    ea.rb = route_bufs(ws, L);
-    ea.wl.items = reinterpret_cast<moe::ItemRec*>(ws + L.items);
-    ea.wl.n_items = sync;
-    ea.wl.queue = sync + 2;
-    ea.wl.abort = sync + 3;
-    ea.wl.done = sync + 8;
-    ea.wl.need = sync + 8 + E;
-    ea.status = reinterpret_cast<int*>(ws + L.status);
-    ea.timeout_ns = (unsigned long long)c.timeout_us * 1000ull;
-    ea.debug_stall = (c.flags & MOE_FLAG_DEBUG_STALL) ? 1 : 0;
-    ea.rt = nullptr;
+    p.rb = route_bufs(ws, L);
+    p.wl = work_list(ws, L);
+    p.ta = tc_args(h, T, ws, L);
+    p.ta.items = p.wl.items;
+    p.ta.n_items = p.wl.n_items;
+    p.ta.abort = p.wl.abort;
+    if (c.flags & MOE_FLAG_TRACE) p.ta.trace = reinterpret_cast<unsigned long long*>(ws + L.status + 4096);
+    const int chunks = (int)max_chunks(c, T);
+    p.chunk_stride = chunks;
     p.queues = reinterpret_cast<int*>(ws + L.tickets);
     p.dones = p.queues + moe::kMaxPersistLayers;
     p.bar = reinterpret_cast<unsigned*>(ws + L.status + 16);
@@ -317,7 +333,7 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
         p.dbg.offsets = dbg->expert_offsets_dev;
         p.dbg.perm = dbg->perm_dev;
     }
-    if (cudaMemsetAsync(sync + 3, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;   // abort flag
+    if (cudaMemsetAsync(p.wl.abort, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
     for (int l0 = 0; l0 < c.num_layers; l0 += moe::kMaxPersistLayers) {
         const int nl = std::min(moe::kMaxPersistLayers, c.num_layers - l0);
         p.L = nl;
@@ -332,11 +348,11 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
             p.layer[l].norm_w = reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev);
         }
         if (l0 > 0 && cudaMemsetAsync(ws + L.status + 16, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
-        if (cudaMemsetAsync(ws + L.tickets, 0, (size_t)moe::kMaxPersistLayers * (E + 1) * 4, st) != cudaSuccess)
+        if (cudaMemsetAsync(ws + L.tickets, 0, (size_t)moe::kMaxPersistLayers * (1 + chunks) * 4, st) != cudaSuccess)
             return MOE_ERR_CUDA;
         void* kargs[] = {&p};
         if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(moe::persist_kernel), dim3(h->persist_grid),
-                                        dim3(moe::kTmaThreads), kargs, moe::kTmaSmemBytes, st) != cudaSuccess)
+                                        dim3(moe::kTcThreads), kargs, moe::kTcSmemBytes, st) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -391,14 +407,14 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
 
     moe_mxfp4_handle* h = new (std::nothrow) moe_mxfp4_handle();
     if (!h) return MOE_ERR_INVALID_ARG;
-    // the TMA expert path takes K = H and K = I in whole 512-element stages
-    // (which also makes every scale row a multiple of 16 bytes)
-    h->tma = (c.hidden % moe::kTmaKC == 0) && (c.inter % moe::kTmaKC == 0);
+    // the tensor-core expert path takes K = H and K = I in 256-element stages whose
+    // scale boxes are multiples of 16 bytes (K a multiple of 512)
+    h->tma = (c.hidden % 512 == 0) && (c.inter % 512 == 0);
     if (h->tma) {
         h->maps.resize(c.num_layers);
         for (int l = 0; l < c.num_layers && h->tma; ++l) h->tma = make_maps(c, layers[l], &h->maps[l]);
-        if (h->tma && cudaFuncSetAttribute(moe::expert_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           moe::kTmaSmemBytes) != cudaSuccess) {
+        if (h->tma && cudaFuncSetAttribute(moe::expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           moe::kTcSmemBytes) != cudaSuccess) {
             delete h;
             return MOE_ERR_CUDA;
         }
@@ -407,12 +423,12 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
                                                  sizeof(int))) != cudaSuccess)
             h->tma = false;
         if (h->tma && cudaFuncSetAttribute(moe::persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           moe::kTmaSmemBytes) == cudaSuccess) {
+                                           moe::kTcSmemBytes) == cudaSuccess) {
             int per_sm = 0;
             int coop = 0;
             cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-            if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe::persist_kernel, moe::kTmaThreads,
-                                                                      moe::kTmaSmemBytes) == cudaSuccess &&
+            if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe::persist_kernel, moe::kTcThreads,
+                                                                      moe::kTcSmemBytes) == cudaSuccess &&
                 per_sm >= 1)
                 h->persist_grid = prop.multiProcessorCount;
         }

@@ -3,16 +3,16 @@
 // pipeline stays resident instead of one launch per operator; implementation
 // guide "关键实现细节" item 3: per-launch gaps of 5-10 us and 10-30% operator-boundary
 // overhead at high token rates).  One CTA per SM, the expert kernel's block
-// shape (16 consumer warps + 1 producer warp).  Per layer:
+// shape (16 warps) and tensor-memory allocation.  Per layer:
 //   [router]           all CTAs, (32 experts x 1024 columns) units: partial logits
-//                      and the layer input in f16 (+ factors)
+//                      and the layer input as the experts' E4M3-term operand
 //   -- grid barrier --
 //   [route]            small blocks (T*k <= 64): every CTA sums the slice partials
 //                      (in order), takes the top-k and groups the pairs in its own
 //                      shared memory (identical results everywhere; CTA 0 also
 //                      publishes them); larger blocks: CTA 0 builds a global work
 //                      list while the other CTAs wait on a release flag
-//   [experts]          the work-queue expert phase of expert_tma.cuh
+//   [experts]          the work-queue expert phase of expert_tc.cuh
 //   -- grid barrier --
 //   [combine]          all CTAs, (token, 1024 columns) units: gate-weighted sum of
 //                      the pair outputs, residual add, sums of squares for the next
@@ -22,7 +22,7 @@
 // word and the abort flag, and every CTA leaves at its next wait.
 #pragma once
 
-#include "expert_tma.cuh"
+#include "expert_tc.cuh"
 #include "route.cuh"
 
 namespace moe {
@@ -35,7 +35,7 @@ constexpr int kPRouteTok = 8;        // tokens per round
 constexpr int kCombineChunk = 1024;  // columns per combine unit
 
 struct PersistLayer {
-    TmaMaps maps;
+    TcMaps maps;
     const __nv_bfloat16* router_w;
     const float* router_b;
     const __nv_bfloat16* norm_w;
@@ -62,14 +62,17 @@ struct PersistParams {
     const __nv_bfloat16* x;
     void* y;
     float* resid;      // [T, H] (stack)
-    __half* act16;     // [T, H]
-    float* act_fac;    // [T, H / 128]
+    uint8_t* xb4;      // expert operand of the layer input (expert_tc.cuh layouts)
+    uint8_t* xsf;
     float* ss;         // [T, ceil(H / 1024)] sums of squares of the residual per column chunk
     float* rpart;      // [H / 512, T, E]
     unsigned long long* tstamp;   // CTA 0's %globaltimer at phase ends (or NULL)
-    ExpertArgs ea;     // h16, h_scale, partial, rb, wl, status, timeout_ns (layer set per layer)
+    TcArgs ta;         // expert phase: operands, partial, status, timeout (per-layer fields set per layer)
+    RouteBufs rb;
+    WorkList wl;       // items / n_items / abort for larger blocks
     int* queues;       // [kMaxPersistLayers] expert-phase queue per layer (zeroed per launch)
-    int* dones;        // [kMaxPersistLayers, E] finished gate/up items per routed expert (zeroed per launch)
+    int* dones;        // [kMaxPersistLayers, chunk_stride] finished gate/up items per chunk (zeroed per launch)
+    int chunk_stride;
     unsigned* bar;     // grid barrier counter (zeroed per forward)
     int* route_flag;   // layers routed so far (zeroed per forward)
     PersistDebug dbg;
@@ -168,8 +171,7 @@ __device__ __forceinline__ float inv_rms(const PersistParams& p, int t) {
 // the group over the slice for every token, 8 tokens at a time.  Each warp loads its
 // 2 expert rows over the slice once; the slice of the layer input (x, or RMSNorm of
 // the residual for a stack) is staged in shared memory once per token group; units
-// of group 0 also write it in f16 with one power-of-two factor per (token, slice)
-// for the expert phase.
+// of group 0 also write it as the expert phase's operand (8 E2M1 terms per block).
 __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLayer& ly, int u, float* xs /*[8][512]*/,
                                          float* sinv /*[8]*/) {
     const int H = p.H, E = p.E, T = p.T;
@@ -224,21 +226,15 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
         }
         __syncthreads();
         if (t0 == 0) rs(2);
-        if (eg == 0 && warp < nt) {
-            // f16 activations of this slice for token t0 + warp, one power-of-two factor
-            const float* row = xs + warp * kPRouteSlice;
-            const int per = ncols / 32;
-            float m = 0.0f;
-            for (int i = 0; i < per; ++i) m = fmaxf(m, fabsf(row[lane * per + i]));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-            const int q = f16_exponent_for(m);
-            const float inv = exp2i(-q);
-            __half* dst = p.act16 + (size_t)(t0 + warp) * H + c0 + lane * per;
-            for (int i = 0; i < per; i += 2)
-                *reinterpret_cast<__half2*>(dst + i) =
-                    __floats2half2_rn(row[lane * per + i] * inv, row[lane * per + i + 1] * inv);
-            if (lane < ncols / 128) p.act_fac[(size_t)(t0 + warp) * (H / 128) + c0 / 128 + lane] = exp2i(q);
+        if (eg == 0) {
+            // expert operand of this slice: 8 E2M1 terms per MX block (token, 32 columns)
+            const int nb = ncols / 32;
+            for (int i = warp; i < nt * nb; i += blockDim.x >> 5) {
+                const int t = i / nb, kbl = i % nb;
+                uint32_t sb0, sb1;
+                const uint32_t codes = split_e2m1_terms(xs[t * kPRouteSlice + kbl * 32 + lane], sb0, sb1);
+                store_act_terms(p.xb4, p.xsf, H, t0 + t, c0 / 32 + kbl, lane, codes, sb0, sb1);
+            }
         }
         float accp[kPRouteTok][2];
 #pragma unroll
@@ -294,7 +290,7 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
 __device__ __noinline__ void route_local(const PersistParams& p, const PersistLayer& ly, int l, int* scratch,
                                          RouteTable* rt) {
     const int T = p.T, E = p.E, k = p.k, H = p.H;
-    const RouteBufs& rb = p.ea.rb;
+    const RouteBufs& rb = p.rb;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     auto sub = [&](int i) {   // sub-step timestamps of the first layer, CTA 0 (profiling)
         if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[40 + i] = globaltimer_ns();
@@ -455,7 +451,7 @@ __device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, 
     const int nc = (H + kCombineChunk - 1) / kCombineChunk;
     const int t = u / nc, c = u % nc;
     const int c0 = c * kCombineChunk, ncols = min(kCombineChunk, H - c0);
-    const RouteBufs& rb = p.ea.rb;
+    const RouteBufs& rb = p.rb;
     const bool last = l == p.L - 1;
     const size_t o = (size_t)t * H + c0;
     float gj[kMaxTopK];
@@ -474,7 +470,7 @@ __device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, 
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j) {
             if (j >= k || gj[j] == 0.0f) continue;
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ea.partial + (size_t)(t * k + j) * H + c0 + h));
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ta.partial + (size_t)(t * k + j) * H + c0 + h));
             acc.x = fmaf(gj[j], v.x, acc.x);
             acc.y = fmaf(gj[j], v.y, acc.y);
             acc.z = fmaf(gj[j], v.z, acc.z);
@@ -529,8 +525,8 @@ __device__ __noinline__ void stack_init_unit(const PersistParams& p, int u, floa
 // scratch: shared memory of at least (2 * E + 1 + 32 * E + 64) ints.
 __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLayer& ly, int l, int* scratch) {
     const int T = p.T, E = p.E, k = p.k, H = p.H;
-    const RouteBufs& rb = p.ea.rb;
-    const WorkList& wl = p.ea.wl;
+    const RouteBufs& rb = p.rb;
+    const WorkList& wl = p.wl;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     auto sub = [&](int i) {   // sub-step timestamps of the first layer (profiling)
         if (l == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[40 + i] = globaltimer_ns();
@@ -658,7 +654,7 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
     // ---- work list: chunks of <= 8 pairs per routed expert.  The grouping is
     // staged in shared memory first (the item records read it many times).
     const int n_active = misc[0];
-    const int rbu = p.I / kTmaRows, rbd = H / kTmaRows;
+    const int rbu = p.I / kTmaRows, rbd = H / kDownRows;
     int* chunk0 = flag;                 // [n_active]: first chunk index of each routed expert
     int* s_act = wcnt;                  // [n_active] expert ids
     int* s_beg = wcnt + E;              // [n_active] first perm position
@@ -674,9 +670,7 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
     __syncthreads();
     if (warp == 0) {
         for (int a = lane; a < n_active; a += 32) {
-            const int c = (s_cnt[a] + kTmaTok - 1) / kTmaTok;
-            chunk0[a] = c;
-            wl.need[a] = c * rbu;
+            chunk0[a] = (s_cnt[a] + kTmaTok - 1) / kTmaTok;
         }
         __syncwarp();
         const int total_chunks = warp_excl_scan(chunk0, n_active);
@@ -707,8 +701,9 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
         r.ntok = min(kTmaTok, s_cnt[lo] - tc * kTmaTok);
 #pragma unroll
         for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? s_perm[r.beg + q] : s_perm[r.beg + q] / k) : 0;
+        r.chunk = chunk;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) r.pad[q] = 0;
+        for (int q = 0; q < 3; ++q) r.pad[q] = 0;
         wl.items[i] = r;
     }
     sub(4);
@@ -724,40 +719,34 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
 
 // The expert phase of one layer, compiled as its own function (its register
 // allocation does not carry the rest of the persistent kernel's live state).
-__device__ __noinline__ void persist_expert_phase(const ExpertArgs args, const ExpertLayer lay, const TmaMaps* maps,
-                                                  uint8_t* smem_raw, uint32_t* it_p, uint32_t* it_c,
-                                                  uint32_t* epi_uses, unsigned long long deadline) {
-    const ExpertSmem sm = expert_smem(smem_raw);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == kTmaConsumerWarps) {
-        if (lane == 0) {
-            fence_proxy_async_global();   // inputs written by other CTAs before the last barrier / flag
-            uint32_t it = *it_p;
-            expert_produce(*maps, args, lay, sm, it, deadline);
-            *it_p = it;
-        }
-    } else {
-        uint32_t it = *it_c, eu = *epi_uses;
-        expert_consume(args, lay, sm, it, eu, warp, lane, deadline);
-        *it_c = it;
-        *epi_uses = eu;
+__device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMaps* maps, uint8_t* smem_raw,
+                                                  uint32_t tmem, TcRoleState* rs, unsigned long long deadline) {
+    const TcSmem s = tc_smem(smem_raw);
+    if (threadIdx.x == kTcWarpProducer * 32) {
+        fence_proxy_async_global();   // inputs written by other CTAs before the last barrier / flag
+        prefetch_tensormap(&maps->gate_q);
+        prefetch_tensormap(&maps->up_q);
+        prefetch_tensormap(&maps->down_q);
+        prefetch_tensormap(&maps->gate_s);
+        prefetch_tensormap(&maps->up_s);
+        prefetch_tensormap(&maps->down_s);
     }
+    TcRoleState r = *rs;
+    tc_phase(*maps, args, s, tmem, r, deadline);
+    *rs = r;
 }
 
-__global__ void __launch_bounds__(kTmaThreads, 1) persist_kernel(const __grid_constant__ PersistParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const ExpertSmem sm = expert_smem(smem_raw);
-    if (threadIdx.x == 0) expert_smem_init(sm);
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const unsigned long long deadline = globaltimer_ns() + p.ea.timeout_ns;
-    int* abort = p.ea.wl.abort;
-    int* status = p.ea.status;
-    float* red = sm.epi;                                   // block reductions (<= 32 floats)
+// All layers of one launch; returns early (in every thread of the block) on a timeout / abort.
+__device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* smem_raw, uint32_t tmem,
+                                            unsigned long long deadline) {
+    const TcSmem sm = tc_smem(smem_raw);
+    int* abort = p.wl.abort;
+    int* status = p.ta.status;
+    float* red = sm.red;                                   // block reductions (<= 32 floats)
     float* xs = reinterpret_cast<float*>(sm.slots);        // router staging / routing scratch
-    float* sinv = sm.epi + 64;                             // [8]
+    float* sinv = sm.red + 32;                             // [8]
     unsigned epoch = 0;
-    uint32_t it_p = 0, it_c = 0, epi_uses = 0;
+    TcRoleState rs{0u, 0u, 0u, 0u};
     const int n_sl = (p.H + kPRouteSlice - 1) / kPRouteSlice;
     const int units = ((p.E + kPRouteExperts - 1) / kPRouteExperts) * n_sl;
     const int cunits = p.T * ((p.H + kCombineChunk - 1) / kCombineChunk);
@@ -775,7 +764,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) persist_kernel(const __grid_co
     for (int l = 0; l < p.L; ++l) {
         const PersistLayer& ly = p.layer[l];
         for (int u = blockIdx.x; u < units; u += gridDim.x) router_unit(p, ly, u, xs, sinv);
-        const bool withhold = p.ea.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
+        const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
         if (!grid_sync(p.bar, epoch, deadline, abort, status, withhold)) return;
         stamp(2 + 4 * l);
         if (small) {
@@ -807,14 +796,28 @@ __global__ void __launch_bounds__(kTmaThreads, 1) persist_kernel(const __grid_co
         // the slots were written through the generic proxy; TMA writes them next
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
-        const ExpertLayer lay{p.layer_base + l, p.queues + l, p.dones + (size_t)l * p.E, small ? sm.rt : nullptr};
-        persist_expert_phase(p.ea, lay, &ly.maps, smem_raw, &it_p, &it_c, &epi_uses, deadline);
+        TcArgs ta = p.ta;
+        ta.layer = p.layer_base + l;
+        ta.queue = p.queues + l;
+        ta.done = p.dones + (size_t)l * p.chunk_stride;
+        ta.rt = small ? sm.rt : nullptr;
+        if (l != 0 || p.layer_base != 0) ta.trace = nullptr;
+        persist_expert_phase(ta, &ly.maps, smem_raw, tmem, &rs, deadline);
         if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
         stamp(4 + 4 * l);
         for (int u = blockIdx.x; u < cunits; u += gridDim.x) combine_unit(p, u, l, red);
         stamp(5 + 4 * l);
         if (l + 1 < p.L && !grid_sync(p.bar, epoch, deadline, abort, status)) return;
     }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_constant__ PersistParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const TcSmem sm = tc_smem(smem_raw);
+    const uint32_t tmem = tc_setup(sm);
+    const unsigned long long deadline = globaltimer_ns() + p.ta.timeout_ns;
+    persist_layers(p, smem_raw, tmem, deadline);
+    tc_teardown(sm, tmem, p.ta.timeout_ns);
 }
 
 }  // namespace moe

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace moe {
@@ -31,6 +32,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// The same test, suspending the thread in hardware until the phase completes or
+// about `hint_ns` pass (a waiting warp then takes no issue slots).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// Non-blocking test of a phase (try_wait may suspend the thread for a while).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -69,6 +94,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy writes of shared memory with later
+// async-proxy reads (TMA, tcgen05.cp / mma operands).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- named barriers (id 0 is __syncthreads) ----------------------------------
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -100,38 +131,99 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
         : "r"(w));
 }
-// acc + w.lo * x.lo and acc + w.hi * x.hi with f16 operands, fp32 product and sum
-// (the product of two f16 values is exact in fp32; one rounding per step).
-__device__ __forceinline__ float fma_f16lo(uint32_t w2, uint32_t x2, float acc) {
-    float r;
-    asm("{\n .reg .f16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
-        " fma.rn.f32.f16 %0, a0, b0, %3;\n}"
-        : "=f"(r)
-        : "r"(w2), "r"(x2), "f"(acc));
-    return r;
+}  // namespace moe
+
+namespace moe {
+
+// ---- tcgen05: tensor memory, block-scaled MMA, commits ----------------------------
+// Tensor-memory addresses are (lane << 16) | column.  A warp may only touch the 32
+// lanes of its quarter (warp % 4).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {   // whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
 }
-__device__ __forceinline__ float fma_f16hi(uint32_t w2, uint32_t x2, float acc) {
-    float r;
-    asm("{\n .reg .f16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
-        " fma.rn.f32.f16 %0, a1, b1, %3;\n}"
-        : "=f"(r)
-        : "r"(w2), "r"(x2), "f"(acc));
-    return r;
+__device__ __forceinline__ void tmem_relinquish() {   // whole warp
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {   // whole warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 4 consecutive 32-bit columns of this thread's lane (whole warp).
+__device__ __forceinline__ void tc_st_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 32 consecutive 32-bit columns of this thread's lane (whole warp); complete after tc_wait_ld.
+__device__ __forceinline__ void tc_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzled
+// layout: rows of 128 bytes, 8-row groups 1024 bytes apart, base 1024-aligned.  The
+// K offset inside the 128-byte row is added to the start address (16-byte units).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor of kind::mxf4 (dense, K-major packed E2M1 A and B = format
+// 1, E8M0 scales, K = 64): N >> 3, M >> 4; the scale-factor selectors (bits 4-5 for
+// B, 29-30 for A) are OR-ed in per MMA.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) { return (b_id << 4) | (a_id << 29); }
+// D[tmem] (+)= (A * SFA) x (B * SFB)^T over K = 64 (two 32-element blocks, scale
+// vector 2X: scale id 0 takes bytes 0-1 of each 32-bit scale cell, id 2 bytes 2-3).
+// The scale-factor addresses must be 4-column aligned.
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+// Shared-memory descriptor of a plain (unswizzled) block of 16-byte rows: row r at
+// start + 16 r (8-row groups 128 bytes apart).
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+// Copies 32 rows of 16 bytes (shared memory, smem_desc_rows16) into tensor memory:
+// row r -> columns taddr .. taddr+3 of lane r in every lane quarter.  Ordered with
+// the issuing thread's later tcgen05.mma.
+__device__ __forceinline__ void tc_cp_32x128_x4(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+// The mbarrier gets one arrival once every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
 }
 
-// D = A * B + C for one 16x8x16 tile: A f16 row-major 16x16 (4 regs), B f16
-// "col" 16x8 (2 regs), C/D fp32 (4 regs); products exact, fp32 accumulation.
-// Register layout (g = lane / 4, q = lane % 4): a0 (row g, k 2q..2q+1),
-// a1 (row g+8, k 2q..), a2 (row g, k 2q+8..), a3 (row g+8, k 2q+8..);
-// b0 (k 2q..2q+1, col g), b1 (k 2q+8..2q+9, col g); d0 (g, 2q), d1 (g, 2q+1),
-// d2 (g+8, 2q), d3 (g+8, 2q+1).
-__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
-                                              const float (&c)[4]) {
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+// ---- E2M1 encode ------------------------------------------------------------------
+// Round to nearest even on the E2M1 grid, saturating at +-6; returns the 4-bit code.
+__device__ __forceinline__ uint32_t f32_to_e2m1(float v) {
+    uint32_t r;
+    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %1;\n cvt.u32.u8 %0, t;\n}" : "=r"(r) : "f"(v));
+    return r & 0xFu;
+}
+// Exact value of a 4-bit E2M1 code.
+__device__ __forceinline__ float e2m1_code_to_f32(uint32_t code) {
+    return __half2float(__ushort_as_half((unsigned short)(e2m1x2_to_f16x2(code) & 0xFFFFu)));
 }
 
 }  // namespace moe

@@ -1,0 +1,152 @@
+// Work items of the expert phase.  The routed pairs of a layer are grouped per
+// expert (perm order: each expert's pairs in (token, slot) order) and cut into
+// chunks of at most 8 pairs.  For every chunk there are I/128 gate/up items (a
+// 128-row block of the gate and of the up matrix over all of K = H) and H/256 down
+// items (a 256-row block of the down matrix over all of K = I).
+#pragma once
+
+#include "common.cuh"
+#include "route.cuh"
+
+namespace moe {
+
+constexpr int kTmaRows = 128;   // rows per gate/up item (of each of the two matrices)
+constexpr int kDownRows = 256;  // rows per down item
+constexpr int kTmaTok = 8;      // pairs per chunk
+
+enum : int { kItemGateUp = 0, kItemDown = 1 };
+
+// Work item code: bit 30 = kind, bits 20..29 = row block, bits 11..19 = chunk of the
+// expert, bits 0..10 = index into the routed-expert list.
+__host__ __device__ __forceinline__ int item_code(int kind, int rb, int tc, int a) {
+    return (kind << 30) | (rb << 20) | (tc << 11) | a;
+}
+
+// One work item as the producer reads it (64 bytes).
+struct __align__(16) ItemRec {
+    int code;          // item_code(kind, rb, tc, a)
+    int e;             // expert id
+    int beg;           // first position of the chunk's pairs in perm
+    int ntok;          // pairs in the chunk (1..8)
+    int tok[kTmaTok];  // gate/up items: token of each pair; down items: pair id (t*k + j)
+    int chunk;         // chunk index within the layer
+    int pad[3];
+};
+
+// Routing state of one layer kept in shared memory by every CTA when the verify
+// block is small (T*k <= 64 pairs): the work items are derived from it directly.
+constexpr int kRtMaxPairs = 64;
+struct RouteTable {
+    int n_active, n_chunks, pad0, pad1;
+    int e[kRtMaxPairs];        // per routed expert (ascending id): expert id
+    int beg[kRtMaxPairs];      // first position in perm
+    int cnt[kRtMaxPairs];      // pairs routed to it
+    int chunk0[kRtMaxPairs];   // index of its first chunk
+    int tok[kRtMaxPairs];      // per perm position: token
+    int pair[kRtMaxPairs];     // per perm position: pair id t*k + j
+};
+
+// Per-forward work list (workspace).
+struct WorkList {
+    ItemRec* items;    // all gate/up items, then all down items
+    int* n_items;      // [0] = total, [1] = number of gate/up items
+    int* queue;        // next item to claim (zero at the start of the phase)
+    int* done;         // [chunks] gate/up items finished per chunk (zero at the start)
+    int* abort;        // set when any wait times out
+};
+
+// Item idx of the phase, from the routing table (rbu / rbd: row blocks of gate/up and down).
+__device__ __forceinline__ ItemRec table_item(const RouteTable* rt, int idx, int rbu, int rbd) {
+    const int n_gu = rt->n_chunks * rbu;
+    const bool down = idx >= n_gu;
+    const int j = down ? idx - n_gu : idx;
+    const int nrb = down ? rbd : rbu;
+    const int chunk = j / nrb, rbi = j % nrb;
+    int lo = 0, hi = rt->n_active - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (rt->chunk0[mid] <= chunk) lo = mid; else hi = mid - 1;
+    }
+    const int tc = chunk - rt->chunk0[lo];
+    ItemRec r;
+    r.code = item_code(down ? kItemDown : kItemGateUp, rbi, tc, lo);
+    r.e = rt->e[lo];
+    r.beg = rt->beg[lo] + tc * kTmaTok;
+    r.ntok = min(kTmaTok, rt->cnt[lo] - tc * kTmaTok);
+#pragma unroll
+    for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? rt->pair[r.beg + q] : rt->tok[r.beg + q]) : 0;
+    r.chunk = chunk;
+#pragma unroll
+    for (int q = 0; q < 3; ++q) r.pad[q] = 0;
+    return r;
+}
+
+// A record written by another CTA of the same launch: read from L2.
+__device__ __forceinline__ ItemRec load_item(const ItemRec* src) {
+    ItemRec r;
+    const int4* s = reinterpret_cast<const int4*>(src);
+    int4* d = reinterpret_cast<int4*>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = __ldcg(s + i);
+    return r;
+}
+
+// Builds the work list of one layer from the grouping (one block of 1024 threads):
+// chunk offsets by a scan over the routed experts, then every item's full record
+// (gate/up items first).  Dynamic shared memory: T*k ints (the perm).
+__global__ void __launch_bounds__(1024) build_items_kernel(RouteBufs rb, int H, int I, int k, WorkList wl, int T) {
+    __shared__ int s_gu[kMaxExperts + 1];
+    __shared__ int s_act[kMaxExperts], s_beg[kMaxExperts], s_cnt[kMaxExperts];
+    __shared__ int s_scan[64];
+    extern __shared__ int s_perm[];   // [T * k] pair id of each perm position
+    const int n_active = rb.active[0];
+    const int rbu = I / kTmaRows, rbd = H / kDownRows;
+    const int a = threadIdx.x;
+    int chunks = 0;
+    if (a < n_active) {
+        const int e = rb.active[1 + a];
+        s_act[a] = e;
+        s_beg[a] = rb.offsets[e];
+        s_cnt[a] = rb.counts[e];
+        chunks = (s_cnt[a] + kTmaTok - 1) / kTmaTok;
+    }
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) s_perm[i] = rb.perm[i];
+    const int off = block_excl_scan_1024(chunks, s_scan);
+    const int total_chunks = s_scan[32];
+    if (a < n_active) s_gu[a] = off;
+    for (int c = threadIdx.x; c < total_chunks; c += blockDim.x) wl.done[c] = 0;
+    __syncthreads();
+    const int n_gu = total_chunks * rbu;
+    if (threadIdx.x == 0) {
+        wl.n_items[0] = n_gu + total_chunks * rbd;
+        wl.n_items[1] = n_gu;
+        *wl.queue = 0;
+        *wl.abort = 0;
+    }
+    const int total = total_chunks * (rbu + rbd);
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const bool down = i >= n_gu;
+        const int j = down ? i - n_gu : i;
+        const int nrb = down ? rbd : rbu;
+        const int chunk = j / nrb, rbi = j % nrb;
+        int lo = 0, hi = n_active - 1;          // last aa with s_gu[aa] <= chunk
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_gu[mid] <= chunk) lo = mid; else hi = mid - 1;
+        }
+        const int aa = lo, tc = chunk - s_gu[aa];
+        ItemRec r;
+        r.code = item_code(down ? kItemDown : kItemGateUp, rbi, tc, aa);
+        r.e = s_act[aa];
+        r.beg = s_beg[aa] + tc * kTmaTok;
+        r.ntok = min(kTmaTok, s_cnt[aa] - tc * kTmaTok);
+#pragma unroll
+        for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? s_perm[r.beg + q] : s_perm[r.beg + q] / k) : 0;
+        r.chunk = chunk;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) r.pad[q] = 0;
+        wl.items[i] = r;
+    }
+}
+
+}  // namespace moe

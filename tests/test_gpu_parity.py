@@ -183,8 +183,8 @@ def test_expert_shards_sum_to_full_layer():
     assert_rows_close(total.cpu().numpy(), full.double().cpu().numpy(), what="shards")
 
 
-def test_down_scale_plus_one_doubles_output_exactly():
-    wl = SMALL[0]
+@pytest.mark.parametrize("wl", [SMALL[0], SMALL[5]], ids=lambda w: w.name)
+def test_down_scale_plus_one_doubles_output_exactly(wl):
     inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
     x = inputs.x.to(DEV)
     y1 = _moe(wl, layers).forward(x, check=True)
@@ -194,8 +194,8 @@ def test_down_scale_plus_one_doubles_output_exactly():
     assert torch.equal(y2, 2 * y1)
 
 
-def test_nan_scale_of_a_routed_expert_is_reported():
-    wl = SMALL[0]
+@pytest.mark.parametrize("wl", [SMALL[0], SMALL[5]], ids=lambda w: w.name)
+def test_nan_scale_of_a_routed_expert_is_reported(wl):
     inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
     moe = _moe(wl, layers)
     bufs, dbg = moe.debug_buffers(wl.T)
