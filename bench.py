@@ -7,8 +7,9 @@ combine) on seeded synthetic inputs resident in HBM.  The metric is
 microseconds per MoE layer per verify block (lower is better), reported with
 the achieved HBM bandwidth over the layer's algorithmic bytes (the routed
 experts' nibbles and scales, router weights, x read, y written) and its
-fraction of the measured copy bandwidth.  L2 is flushed (a 256 MiB write)
-between timed steps, outside the per-step events.  Prints one JSON line.
+fraction of the measured copy bandwidth.  L2 is flushed between timed steps,
+outside the per-step events (by default a 256 MiB write followed by a 256 MiB
+read, so each step starts from a cold and clean L2).  Prints one JSON line.
 
 `--impl reference` times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload and prints the same kind of line.
@@ -195,6 +196,17 @@ def run_gpu(args):
     n_active = [int((counts[l] > 0).sum()) for l in range(wl.layers)]
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.ones(64 << 20, dtype=torch.float32, device=dev) if args.flush == "clean" else None
+
+    def flush_l2(i):
+        # "write": a 256 MiB write (L2 is 129 MB) leaves L2 full of dirty lines of the
+        # flush buffer; "clean" then reads another 256 MiB buffer, so the write-back of
+        # those lines happens here and the timed forward starts from a clean, cold L2
+        if args.flush == "none":
+            return
+        flush.fill_(i & 0xFF)
+        if clean is not None:
+            clean.sum()
     for _ in range(max(args.warmup, 3)):
         moe.forward(x, y, wsp, st)
     torch.cuda.synchronize()
@@ -216,7 +228,7 @@ def run_gpu(args):
         time.sleep(0.1)
     t_wall = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(i)
         ev[i][0].record(stream)
         moe.forward(x, y, wsp, st, kdbg[i])
         ev[i][1].record(stream)
@@ -257,7 +269,7 @@ def run_gpu(args):
         moe.forward_host(xh, yh, wsp)
     e2e = []
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         moe.forward_host(xh, yh, wsp)
@@ -286,7 +298,7 @@ def run_gpu(args):
         "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "layers": wl.layers, "path": "persistent" if persistent else args.path, "routed_experts": n_active, "algorithmic_bytes": alg_bytes,
-                   "l2": "flushed between steps (256 MiB write outside the per-step events)",
+                   "l2": FLUSH_DESC[args.flush],
                    "parallelism": f"replicas{ws}"},
         "hbm_gbs": round(gbs, 1),
         "implied_tokens_per_s": round(ACCEPTANCE_LENGTH / (us * 1e-6), 1),
@@ -306,6 +318,14 @@ def run_gpu(args):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line))
+
+
+FLUSH_DESC = {
+    "write": "flushed between steps: 256 MiB write outside the per-step events (leaves dirty lines)",
+    "clean": "flushed between steps: 256 MiB write, then a 256 MiB read, outside the per-step events "
+             "(cold, clean L2); inputs also larger than L2",
+    "none": "not flushed; inputs larger than L2",
+}
 
 
 def moe_tma(wl):
@@ -355,6 +375,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-experts", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flush", default="clean", choices=["write", "clean", "none"],
+                    help="L2 state before each timed step (see FLUSH_DESC)")
     ap.add_argument("--path", default="persistent", choices=["persistent", "multi"],
                     help="one cooperative launch per forward, or one launch per phase")
     args = ap.parse_args()

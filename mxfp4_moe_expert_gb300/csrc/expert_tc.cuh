@@ -50,20 +50,24 @@ constexpr int kTcN = kDownRows;            // weight rows per MMA (gate 128 | up
 constexpr int kTcThreads = 512;            // 16 warps
 // warp roles: epilogue warps are those of lane quarters 0 and 1 (warp % 4 < 2)
 constexpr int kTcWarpProducer = 2, kTcWarpMma = 3;
-__device__ __forceinline__ bool tc_is_sf_warp(int w) { return w == 6 || w == 7 || w == 10 || w == 11; }
+__device__ __forceinline__ bool tc_is_sf_warp(int w) { return w == 6 || w == 7 || w == 10; }
 __device__ __forceinline__ bool tc_is_epi_warp(int w) { return (w & 3) < 2; }
 constexpr int kTcEpiWarps = 8;
-constexpr int kTcSfWarps = 4;
+constexpr int kTcSfWarps = 3;
 // slot layout (bytes)
 constexpr int kSlotB = 0;                  // weights [256 rows x 128 B] packed E2M1, 128-byte swizzle
 constexpr int kSlotA = 32768;              // activation terms [64 rows x 128 B]; the MMA's rows 64..127 read on (unused)
-constexpr int kSlotSfa = 40960;            // [64 rows x 8 blocks] E8M0 of the activation rows
-constexpr int kSlotAtoms = 41472;          // 6 x [32 rows x 16 B] scale rows for tcgen05.cp: SFA g0, g1, SFB (g, half) x 4
+constexpr int kSlotAtoms = 40960;          // 6 x [32 rows x 16 B] scale rows for tcgen05.cp: SFA g0, g1, SFB (g, half) x 4
 constexpr int kTcSlotBytes = 45056;
 static_assert(kSlotA % 1024 == 0 && kTcSlotBytes % 1024 == 0, "swizzled operands are 1024-aligned");
-constexpr int kTcScaleEntry = 16384;       // a pair of weight-scale boxes [128 rows x up to 64 B]
+// scale ring entry: a pair of weight-scale boxes [128 rows x up to 64 B] (at +0 and
+// +kScaleBox1), then the activation rows' E8M0 scales of the same stages (at +kScaleSfa):
+//   gate/up items: [pair p][stage in group][8 term rows][8 blocks]; down items: [stage][64 rows][8 blocks]
+constexpr int kScaleBox1 = 8192;
+constexpr int kScaleSfa = 16384;
+constexpr int kTcScaleEntry = 20480;
 constexpr int kTcScaleRing = 2;
-constexpr int kTcAuxBytes = 3072;
+constexpr int kTcAuxBytes = 4096;
 constexpr int kTcSmemBytes = 1024 /*align slack*/ + kTcStages * kTcSlotBytes + kTcScaleRing * kTcScaleEntry + kTcAuxBytes;
 static_assert(kTcSmemBytes <= 232448, "shared memory of the expert kernel");
 static_assert(kSlotA + 16384 <= kTcStages * kTcSlotBytes, "the MMA's unused activation rows stay inside shared memory");
@@ -138,7 +142,9 @@ struct TcItemInfo {
 struct TcSmem {
     uint8_t* slots;
     uint8_t* scales;    // [kTcScaleRing][2 boxes][kTcScaleEntry / 2]
-    uint64_t *full, *empty, *sfr, *accf, *acce, *ringf, *ringe, *sfull, *sempty, *epib, *drain;
+    uint64_t *full, *empty, *accf, *acce, *ringf, *ringe, *sfull, *sempty, *epib, *drain;
+    uint64_t *claim, *sfc, *drain2;   // slot claimed by the producer; scale factors in tensor memory; SF drain
+    uint64_t* rw;       // router-weight copies of the persistent kernel
     uint32_t* tmem_slot;
     TcSlotMeta* meta;
     TcItemInfo* ring;
@@ -155,7 +161,6 @@ __device__ __forceinline__ TcSmem tc_smem(uint8_t* smem_raw) {
     uint64_t* b = reinterpret_cast<uint64_t*>(aux);
     s.full = b; b += kTcStages;
     s.empty = b; b += kTcStages;
-    s.sfr = b; b += kTcStages;
     s.accf = b; b += 1;
     s.acce = b; b += 1;
     s.ringf = b; b += kItemRing;
@@ -164,6 +169,10 @@ __device__ __forceinline__ TcSmem tc_smem(uint8_t* smem_raw) {
     s.sempty = b; b += kTcScaleRing;
     s.epib = b; b += 1;
     s.drain = b; b += 1;
+    s.rw = b; b += 1;
+    s.claim = b; b += kTcStages;
+    s.sfc = b; b += kTcStages;
+    s.drain2 = b; b += 1;
     s.tmem_slot = reinterpret_cast<uint32_t*>(aux + 384);
     s.meta = reinterpret_cast<TcSlotMeta*>(aux + 400);
     s.ring = reinterpret_cast<TcItemInfo*>(aux + 640);
@@ -171,7 +180,7 @@ __device__ __forceinline__ TcSmem tc_smem(uint8_t* smem_raw) {
     s.red = reinterpret_cast<float*>(aux + 640 + kItemRing * sizeof(TcItemInfo) + sizeof(RouteTable));
     return s;
 }
-static_assert(8 * (3 * kTcStages + 2 + 2 * kItemRing + 2 * kTcScaleRing + 2) <= 384, "barriers");
+static_assert(8 * (4 * kTcStages + 2 + 2 * kItemRing + 2 * kTcScaleRing + 4) <= 384, "barriers");
 static_assert(400 + kTcStages * sizeof(TcSlotMeta) <= 640, "slot metadata");
 static_assert(640 + kItemRing * sizeof(TcItemInfo) + sizeof(RouteTable) + 64 * sizeof(float) <= kTcAuxBytes, "aux");
 
@@ -180,7 +189,6 @@ __device__ __forceinline__ void tc_smem_init(const TcSmem& s) {
     for (int i = 0; i < kTcStages; ++i) {
         mbar_init(&s.full[i], 1);
         mbar_init(&s.empty[i], 1);
-        mbar_init(&s.sfr[i], kTcSfWarps);
     }
     mbar_init(s.accf, 1);
     mbar_init(s.acce, kTcEpiWarps);
@@ -194,6 +202,12 @@ __device__ __forceinline__ void tc_smem_init(const TcSmem& s) {
     }
     mbar_init(s.epib, kTcEpiWarps);
     mbar_init(s.drain, 1);
+    mbar_init(s.rw, 1);
+    for (int i = 0; i < kTcStages; ++i) {
+        mbar_init(&s.claim[i], 1);
+        mbar_init(&s.sfc[i], kTcSfWarps);
+    }
+    mbar_init(s.drain2, kTcSfWarps);
     fence_barrier_init();
 }
 
@@ -207,7 +221,10 @@ __device__ __forceinline__ bool drain_phase(uint64_t* bar, uint32_t parity, unsi
 
 // Waits on an mbarrier phase, bounded by a deadline; false on timeout or abort.
 // The thread sleeps in try_wait between checks (it wakes when the phase completes).
-constexpr uint32_t kSleepHintNs = 20000;
+#ifndef MOE_SLEEP_HINT_NS
+#define MOE_SLEEP_HINT_NS 20000
+#endif
+constexpr uint32_t kSleepHintNs = MOE_SLEEP_HINT_NS;
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, unsigned long long deadline,
                                            const int* abort) {
     while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
@@ -301,6 +318,51 @@ struct TcRoleState {
     uint32_t eb;    // epilogue barrier uses
 };
 
+// L2 prefetch distance of the producer, in stages (32 KB of weights each), along the
+// sequence of the items it claims.  Off by default: measured on GB300 with the large
+// layer, every distance from 3 to 16 stages made the expert phase slower (the
+// producer thread spends its time issuing prefetches instead of loads).
+#ifndef MOE_PF_STAGES
+#define MOE_PF_STAGES 0
+#endif
+constexpr int kPfStages = MOE_PF_STAGES;
+
+// Where an item's weights live: the two 128-row code boxes of a stage, their scale
+// boxes, and the number of stages per scale-box pair.
+struct TcItemGeom {
+    const CUtensorMap *q0, *q1, *s0, *s1;
+    int r0, r1, nk, spb, sw;
+};
+__device__ __forceinline__ TcItemGeom tc_item_geom(const TcMaps& maps, const ItemRec& it, int H, int I, int wgu,
+                                                   int wd) {
+    const bool gu = ((it.code >> 30) & 1) == kItemGateUp;
+    const int rb = (it.code >> 20) & 0x3FF;
+    TcItemGeom g;
+    g.q0 = gu ? &maps.gate_q : &maps.down_q;
+    g.q1 = gu ? &maps.up_q : &maps.down_q;
+    g.s0 = gu ? &maps.gate_s : &maps.down_s;
+    g.s1 = gu ? &maps.up_s : &maps.down_s;
+    g.r0 = gu ? it.e * I + rb * kTmaRows : it.e * H + rb * kTcN;
+    g.r1 = gu ? g.r0 : g.r0 + kTmaRows;
+    g.nk = gu ? H / kTcKS : I / kTcKS;
+    g.sw = gu ? wgu : wd;
+    g.spb = g.sw / 8;
+    return g;
+}
+// Prefetches stage st of an item into L2 (its code boxes, and its scale boxes when a
+// new scale-box pair starts there).
+__device__ __forceinline__ void tc_prefetch_stage(const TcItemGeom& g, int st) {
+    tma_prefetch_2d(g.q0, st * 128, g.r0);
+    tma_prefetch_2d(g.q1, st * 128, g.r1);
+#ifndef MOE_PF_SCALES
+#define MOE_PF_SCALES 1
+#endif
+    if (MOE_PF_SCALES && st % g.spb == 0) {
+        tma_prefetch_2d(g.s0, st * 8, g.r0);
+        tma_prefetch_2d(g.s1, st * 8, g.r1);
+    }
+}
+
 __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, const TcSmem& s_in,
                                         TcRoleState& rs_in, unsigned long long deadline) {
     // arguments and counters in registers (the caller's copies live in local memory)
@@ -315,6 +377,7 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
     int next_idx = atomicAdd(a.queue, 1);
     ItemRec next{};
     if (next_idx < n_items) next = a.rt ? table_item(a.rt, next_idx, rbu, rbd) : load_item(a.items + next_idx);
+    int pf_next = 0;   // leading stages of the next item already prefetched
     for (;;) {
         const int idx = next_idx;
         const ItemRec cur = next;
@@ -345,41 +408,32 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
             const int slot = rs.it % kTcStages;
             if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
             s.meta[slot] = TcSlotMeta{-1, 0, 1, 0, 0, 0, 0, 0};
+            mbar_arrive(&s.claim[slot]);
             mbar_arrive(&s.full[slot]);
             ++rs.it;
             break;
         }
-        const int e = cur.e, ntok = cur.ntok;
+        const int ntok = cur.ntok;
         const bool gu = kind == kItemGateUp;
-        const int nk = gu ? H / kTcKS : I / kTcKS;   // stages of the item
         // the two 128-row weight boxes of a stage: (gate, up) rows rb*128.. or down rows rb*256.., +128
-        const CUtensorMap* mq0 = gu ? &maps.gate_q : &maps.down_q;
-        const CUtensorMap* mq1 = gu ? &maps.up_q : &maps.down_q;
-        const CUtensorMap* ms0 = gu ? &maps.gate_s : &maps.down_s;
-        const CUtensorMap* ms1 = gu ? &maps.up_s : &maps.down_s;
-        const int r0 = gu ? e * I + rb * kTmaRows : e * H + rb * kTcN;
-        const int r1 = gu ? r0 : r0 + kTmaRows;
-        const int sw = gu ? wgu : wd;                 // scale box width (bytes)
-        const int spb = sw / 8;                        // stages per scale-box pair
+        const TcItemGeom g = tc_item_geom(maps, cur, H, I, wgu, wd);
+        const int nk = g.nk;                           // stages of the item
+        const CUtensorMap* mq0 = g.q0;
+        const CUtensorMap* mq1 = g.q1;
+        const CUtensorMap* ms0 = g.s0;
+        const CUtensorMap* ms1 = g.s1;
+        const int r0 = g.r0, r1 = g.r1;
+        const int sw = g.sw;                           // scale box width (bytes)
+        const int spb = g.spb;                         // stages per scale-box pair
+        const bool has_next = next_idx < n_items;
+        const TcItemGeom gn = tc_item_geom(maps, next, H, I, wgu, wd);
+        for (int q = pf_next; q < min(kPfStages, nk); ++q) tc_prefetch_stage(g, q);   // not yet prefetched
+        pf_next = 0;
         bool h_ready = gu;
         for (int st = 0; st < nk; ++st) {
-            if (st % spb == 0) {   // the next pair of weight-scale boxes: blocks 8*st ..
-                const int se = rs.sc % kTcScaleRing;
-                if (!wait_phase(&s.sempty[se], ((rs.sc / kTcScaleRing) & 1) ^ 1, deadline, a.abort)) {
-                    failed = true;
-                    break;
-                }
-                uint8_t* sdst = s.scales + se * kTcScaleEntry;
-                mbar_arrive_expect_tx(&s.sfull[se], 2u * (uint32_t)sw * kTmaRows);
-                tma_load_2d(sdst, ms0, st * 8, r0, &s.sfull[se]);
-                tma_load_2d(sdst + kTcScaleEntry / 2, ms1, st * 8, r1, &s.sfull[se]);
-                ++rs.sc;
-            }
-            const int slot = rs.it % kTcStages;
-            if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
-            s.meta[slot] = TcSlotMeta{kind, st, nk, (int)rs.sc - 1, (st % spb) * 8, sw, st % spb == spb - 1 ? 1 : 0, 0};
             if (!h_ready) {
-                // every gate/up item of this chunk must have stored its h block
+                // every gate/up item of this chunk must have stored its h block (operand and
+                // scales, both read by copies below)
                 uint32_t spins = 0;
                 while (ld_acquire_gpu(a.done + cur.chunk) < rbu) {
                     if ((++spins & 63u) == 0 &&
@@ -388,31 +442,59 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                         break;
                     }
                 }
-                if (failed) break;   // nothing issued on this slot yet
+                if (failed) break;   // nothing issued for this item yet
                 fence_proxy_async_global();
                 h_ready = true;
             }
-            const uint32_t abytes = gu ? (uint32_t)ntok * (1024 + 64) : (uint32_t)(8192 + 512);
+            if (st % spb == 0) {   // the next pair of weight-scale boxes: blocks 8*st ..
+                const int se = rs.sc % kTcScaleRing;
+                if (!wait_phase(&s.sempty[se], ((rs.sc / kTcScaleRing) & 1) ^ 1, deadline, a.abort)) {
+                    failed = true;
+                    break;
+                }
+                uint8_t* sdst = s.scales + se * kTcScaleEntry;
+                const uint32_t sfa_bytes = gu ? (uint32_t)ntok * spb * 64 : (uint32_t)spb * 512;
+                mbar_arrive_expect_tx(&s.sfull[se], 2u * (uint32_t)sw * kTmaRows + sfa_bytes);
+                tma_load_2d(sdst, ms0, st * 8, r0, &s.sfull[se]);
+                tma_load_2d(sdst + kScaleBox1, ms1, st * 8, r1, &s.sfull[se]);
+                if (gu) {   // per pair: the group's stages of its token (contiguous in xsf)
+                    for (int p = 0; p < ntok; ++p)
+                        bulk_load(sdst + kScaleSfa + p * spb * 64,
+                                  a.xsf + ((size_t)cur.tok[p] * (H / kTcKS) + st) * 64, (uint32_t)spb * 64,
+                                  &s.sfull[se]);
+                } else {
+                    bulk_load(sdst + kScaleSfa, a.hsf + ((size_t)cur.chunk * (I / kTcKS) + st) * 512,
+                              (uint32_t)spb * 512, &s.sfull[se]);
+                }
+                ++rs.sc;
+            }
+            const int slot = rs.it % kTcStages;
+            if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
+            s.meta[slot] = TcSlotMeta{kind, st, nk, (int)rs.sc - 1, (st % spb) * 8, sw, st % spb == spb - 1 ? 1 : 0, spb};
+            mbar_arrive(&s.claim[slot]);   // the scale-factor warps may prepare this slot now
+            const uint32_t abytes = gu ? (uint32_t)ntok * 1024 : 8192u;
             mbar_arrive_expect_tx(&s.full[slot], 2 * 16384 + abytes);
             tc_trace(a, 0, rs.it);
             ++rs.it;   // this slot now has copies in flight
             uint8_t* dst = s.slots + (size_t)slot * kTcSlotBytes;
             tma_load_2d(dst + kSlotB, mq0, st * 128, r0, &s.full[slot]);
             tma_load_2d(dst + kSlotB + 16384, mq1, st * 128, r1, &s.full[slot]);
-            if (st + 3 < nk) {   // three stages ahead into L2
-                tma_prefetch_2d(mq0, (st + 3) * 128, r0);
-                tma_prefetch_2d(mq1, (st + 3) * 128, r1);
+            if (kPfStages > 0) {   // kPfStages ahead into L2: later in this item, else the start of the next one
+                const int ps = st + kPfStages;
+                if (ps < nk) {
+                    tc_prefetch_stage(g, ps);
+                } else if (has_next) {
+                    for (; pf_next <= ps - nk && pf_next < gn.nk; ++pf_next) tc_prefetch_stage(gn, pf_next);
+                }
             }
             if (gu) {
                 for (int p = 0; p < ntok; ++p) {
                     const size_t ts = (size_t)cur.tok[p] * (H / kTcKS) + st;
                     bulk_load(dst + kSlotA + p * 1024, a.xb4 + ts * 1024, 1024, &s.full[slot]);
-                    bulk_load(dst + kSlotSfa + p * 64, a.xsf + ts * 64, 64, &s.full[slot]);
                 }
             } else {
                 const size_t cs = (size_t)cur.chunk * (I / kTcKS) + st;
                 bulk_load(dst + kSlotA, a.hb4 + cs * 8192, 8192, &s.full[slot]);
-                bulk_load(dst + kSlotSfa, a.hsf + cs * 512, 512, &s.full[slot]);
             }
         }
         if (failed) break;
@@ -446,7 +528,13 @@ __device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint
     bool failed = false;
     for (;;) {
         const int slot = rs.it % kTcStages;
-        if (!wait_phase(&s.sfr[slot], (rs.it / kTcStages) & 1, deadline, a.abort)) { failed = true; break; }
+        // the stage's operands have landed and its scale factors are in tensor memory
+        if (!wait_phase(&s.full[slot], (rs.it / kTcStages) & 1, deadline, a.abort) ||
+            !wait_phase(&s.sfc[slot], (rs.it / kTcStages) & 1, deadline, a.abort)) {
+            failed = true;
+            break;
+        }
+        tc_fence_after();
         tc_trace(a, 3, rs.it);
         const TcSlotMeta m = s.meta[slot];
         if (m.kind < 0) {   // END: release the slot and wake the epilogue
@@ -463,9 +551,6 @@ __device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint
         }
         const uint32_t sl = slots + (uint32_t)slot * kTcSlotBytes;
         const uint32_t sf = tmem + kTmemSf + kTmemSfSlot * slot;
-#pragma unroll
-        for (int g = 0; g < 6; ++g)   // SFA g0, g1 -> +0, +4; SFB (g, half) -> +8 + 8g + 4 half
-            tc_cp_32x128_x4(sf + 4 * g, smem_desc_rows16(sl + kSlotAtoms + 512 * g));
         const uint64_t ad = smem_desc_sw128(sl + kSlotA), bd = smem_desc_sw128(sl + kSlotB);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {   // K = 64 each: blocks 2kk, 2kk+1
@@ -491,51 +576,80 @@ __device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint
 // weight row n's scales from lane n % 32 of the reading row's quarter, column
 // base + n / 32 (one 32-bit cell = 4 blocks; group g = blocks 4g..4g+3 of the
 // stage).  tcgen05.cp 32x128b.warpx4 puts 16-byte row r of a 512-byte block into
-// columns +0..3 of lane r of every quarter, so the blocks are: SFA group g, row r =
-// cells of activation rows r, 32 + r (rows 64.. unused); SFB group g, half h, row
-// r = cells of weight rows 128h + r, 128h + 32 + r, 128h + 64 + r, 128h + 96 + r.
-// Scale-factor warp w (0..3) handles rows 32w + lane of both weight boxes and, for
-// w < 2, activation row 32w + lane.
-__device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, TcRoleState& rs_in, int w, int lane,
-                                   unsigned long long deadline) {
+// columns +0..3 of lane r of every quarter, so the six blocks of a stage are:
+// SFA group g (block g), row r = cells of activation rows r, 32 + r (rows 64..
+// unused, zero); SFB group g, half h (block 2 + 2g + h), row r = cells of weight
+// rows 128h + r, 128h + 32 + r, 128h + 64 + r, 128h + 96 + r.  Warp w = 0, 1 builds
+// the SFB blocks of half h = w (both groups), warp 2 the SFA blocks; lane r builds
+// row r, and lane 0 copies the warp's two blocks into the slot's tensor-memory
+// columns and commits to sfc[slot] (three arrivals), which the MMA thread waits on.
+// A slot is prepared as soon as the producer has claimed it (its previous MMAs are
+// done): the scales come from the scale ring, not from the slot's own copies, so
+// the work overlaps the stage's weight copies.
+__device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, uint32_t tmem, TcRoleState& rs_in, int w,
+                                   int lane, unsigned long long deadline) {
     const TcArgs a = a_in;
     const TcSmem s = s_in;
     TcRoleState rs = rs_in;
     bool failed = false;
     for (;;) {
         const int slot = rs.it % kTcStages;
-        if (!warp_wait_phase(&s.full[slot], (rs.it / kTcStages) & 1, deadline, a.abort)) { failed = true; break; }
+        const uint32_t ph = (rs.it / kTcStages) & 1;
+        if (!warp_wait_phase(&s.claim[slot], ph, deadline, a.abort)) { failed = true; break; }
         const TcSlotMeta m = s.meta[slot];
         if (w == 0 && lane == 0) tc_trace(a, 1, rs.it);
         if (m.kind >= 0) {
             const int se = m.sc % kTcScaleRing;
             if (!warp_wait_phase(&s.sfull[se], (m.sc / kTcScaleRing) & 1, deadline, a.abort)) { failed = true; break; }
-            uint8_t* sl = s.slots + (size_t)slot * kTcSlotBytes;
-            uint32_t* at = reinterpret_cast<uint32_t*>(sl + kSlotAtoms);
-            uint32_t ff = 0;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint2 v = *reinterpret_cast<const uint2*>(s.scales + se * kTcScaleEntry + h * (kTcScaleEntry / 2) +
-                                                                (32 * w + lane) * m.sc_w + m.sc_off);
-                at[(2 + 0 * 2 + h) * 128 + lane * 4 + w] = v.x;   // SFB group 0, half h
-                at[(2 + 1 * 2 + h) * 128 + lane * 4 + w] = v.y;   // SFB group 1, half h
-                ff |= (v.x & (v.x >> 1) & (v.x >> 2) & (v.x >> 3) & (v.x >> 4) & (v.x >> 5) & (v.x >> 6) & (v.x >> 7) &
-                       0x01010101u) |
-                      (v.y & (v.y >> 1) & (v.y >> 2) & (v.y >> 3) & (v.y >> 4) & (v.y >> 5) & (v.y >> 6) & (v.y >> 7) &
-                       0x01010101u);
-            }
-            if (ff) raise_status(a.status, MOE_ERR_BAD_SCALE, a.layer * 65536);   // scale byte 0xFF (NaN)
+            const uint8_t* ent = s.scales + se * kTcScaleEntry;
+            uint8_t* at = s.slots + (size_t)slot * kTcSlotBytes + kSlotAtoms;
+            int b0, b1;   // the warp's two blocks
             if (w < 2) {
-                const uint2 v = *reinterpret_cast<const uint2*>(sl + kSlotSfa + (32 * w + lane) * 8);
-                at[0 * 128 + lane * 4 + w] = v.x;
-                at[1 * 128 + lane * 4 + w] = v.y;
+                uint2 v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    v[c] = *reinterpret_cast<const uint2*>(ent + w * kScaleBox1 + (32 * c + lane) * m.sc_w + m.sc_off);
+                uint32_t ff = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    ff |= (v[c].x & (v[c].x >> 1) & (v[c].x >> 2) & (v[c].x >> 3) & (v[c].x >> 4) & (v[c].x >> 5) &
+                           (v[c].x >> 6) & (v[c].x >> 7) & 0x01010101u) |
+                          (v[c].y & (v[c].y >> 1) & (v[c].y >> 2) & (v[c].y >> 3) & (v[c].y >> 4) & (v[c].y >> 5) &
+                           (v[c].y >> 6) & (v[c].y >> 7) & 0x01010101u);
+                if (ff) raise_status(a.status, MOE_ERR_BAD_SCALE, a.layer * 65536);   // scale byte 0xFF (NaN)
+                b0 = 2 + w;
+                b1 = 4 + w;
+                *reinterpret_cast<uint4*>(at + b0 * 512 + lane * 16) = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+                *reinterpret_cast<uint4*>(at + b1 * 512 + lane * 16) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+            } else {   // activation rows lane and 32 + lane (row 8p + j; sg = stage within the scale group)
+                const int sg = m.sc_off / 8;
+                uint2 v[2];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int row = 32 * c + lane;
+                    const int off = m.kind == kItemGateUp ? (row >> 3) * m.pad * 64 + sg * 64 + (row & 7) * 8
+                                                          : sg * 512 + row * 8;
+                    v[c] = *reinterpret_cast<const uint2*>(ent + kScaleSfa + off);
+                }
+                b0 = 0;
+                b1 = 1;
+                *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(v[0].x, v[1].x, 0u, 0u);
+                *reinterpret_cast<uint4*>(at + 512 + lane * 16) = make_uint4(v[0].y, v[1].y, 0u, 0u);
             }
             fence_proxy_async_shared();   // read next by tcgen05.cp
             __syncwarp();
-            if (m.sc_last && lane == 0) mbar_arrive(&s.sempty[se]);
+            if (lane == 0) {
+                if (m.sc_last) mbar_arrive(&s.sempty[se]);
+                const uint32_t sl = smem_u32(s.slots) + (uint32_t)slot * kTcSlotBytes + kSlotAtoms;
+                const uint32_t sf = tmem + kTmemSf + kTmemSfSlot * slot;
+                tc_cp_32x128_x4(sf + 4 * b0, smem_desc_rows16(sl + 512 * b0));
+                tc_cp_32x128_x4(sf + 4 * b1, smem_desc_rows16(sl + 512 * b1));
+                tc_commit(&s.sfc[slot]);
+            }
+        } else if (lane == 0) {
+            mbar_arrive(&s.sfc[slot]);   // END: keeps the barrier's phases in step
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.sfr[slot]);
         if (w == 0 && lane == 0) tc_trace(a, 2, rs.it);
         ++rs.it;
         if (m.kind < 0) break;
@@ -704,7 +818,7 @@ __device__ __forceinline__ void tc_phase(const TcMaps& maps, const TcArgs& a, co
     } else if (warp == kTcWarpMma) {
         if (lane == 0) tc_mma(a, s, tmem, rs, deadline);
     } else if (tc_is_sf_warp(warp)) {
-        tc_sf(a, s, rs, (warp == 6) ? 0 : (warp == 7) ? 1 : (warp == 10) ? 2 : 3, lane, deadline);
+        tc_sf(a, s, tmem, rs, (warp == 6) ? 0 : (warp == 7) ? 1 : 2, lane, deadline);
     } else if (tc_is_epi_warp(warp)) {
         tc_epilogue(a, s, tmem, rs, warp, lane, deadline);
     }
@@ -732,6 +846,10 @@ __device__ __forceinline__ void tc_teardown(const TcSmem& s, uint32_t tmem, unsi
     if (warp == kTcWarpMma && lane == 0) {
         tc_commit(s.drain);
         drain_phase(s.drain, 0, globaltimer_ns() + timeout_ns);
+    }
+    if (tc_is_sf_warp(warp) && lane == 0) {   // the scale-factor warps' tensor-memory copies
+        tc_commit(s.drain2);
+        drain_phase(s.drain2, 0, globaltimer_ns() + timeout_ns);
     }
     tc_fence_before();
     __syncthreads();

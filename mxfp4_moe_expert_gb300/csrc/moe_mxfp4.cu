@@ -74,12 +74,13 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     L.xb4 = take(moe::xb4_bytes(T, (int)H));
     L.xsf = take(moe::xsf_bytes(T, (int)H));
     L.ss = take((size_t)T * (H / 1024 + 1) * 4);
-    L.tickets = take((size_t)moe::kMaxPersistLayers * (1 + chunks) * 4);   // per-layer queue + per-chunk done counters
+    // per layer: expert-phase queue, per-chunk done counters, per-expert-group router counters
+    L.tickets = take((size_t)moe::kMaxPersistLayers * (1 + chunks + 32) * 4);
     L.hb4 = take(chunks * moe::hb4_chunk_bytes((int)I));
     L.hsf = take(chunks * moe::hsf_chunk_bytes((int)I));
     L.items = take(max_items(c, T) * sizeof(moe::ItemRec));
     L.sync = take((8 + chunks) * 4);   // n_items[2], queue, abort, ..., done[chunks]
-    L.rpart = take((size_t)(H / 512 + 1) * T * E * 4);   // router partials per 512- or 1024-column slice
+    L.rpart = take((size_t)(H / 256 + 1) * T * E * 4);   // router partials per column slice (>= 256 columns)
     L.total = o;
     return L;
 }
@@ -323,6 +324,15 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     p.chunk_stride = chunks;
     p.queues = reinterpret_cast<int*>(ws + L.tickets);
     p.dones = p.queues + moe::kMaxPersistLayers;
+    p.rcnt = p.dones + (size_t)moe::kMaxPersistLayers * chunks;
+    // router unit width: the widest slice that still gives every other SM a unit
+    p.rslice = 256;
+    for (int w = 1024; w >= 512; w /= 2) {
+        if (H % w == 0 && ((E + moe::kPRouteExperts - 1) / moe::kPRouteExperts) * (H / w) >= h->persist_grid / 2) {
+            p.rslice = w;
+            break;
+        }
+    }
     p.bar = reinterpret_cast<unsigned*>(ws + L.status + 16);
     p.route_flag = reinterpret_cast<int*>(ws + L.status + 20);
     p.tstamp = reinterpret_cast<unsigned long long*>(ws + L.status + 64);
@@ -348,7 +358,8 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
             p.layer[l].norm_w = reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev);
         }
         if (l0 > 0 && cudaMemsetAsync(ws + L.status + 16, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
-        if (cudaMemsetAsync(ws + L.tickets, 0, (size_t)moe::kMaxPersistLayers * (1 + chunks) * 4, st) != cudaSuccess)
+        if (cudaMemsetAsync(ws + L.tickets, 0, (size_t)moe::kMaxPersistLayers * (1 + chunks + 32) * 4, st) !=
+            cudaSuccess)
             return MOE_ERR_CUDA;
         void* kargs[] = {&p};
         if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(moe::persist_kernel), dim3(h->persist_grid),

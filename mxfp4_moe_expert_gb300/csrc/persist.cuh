@@ -4,14 +4,16 @@
 // guide "关键实现细节" item 3: per-launch gaps of 5-10 us and 10-30% operator-boundary
 // overhead at high token rates).  One CTA per SM, the expert kernel's block
 // shape (16 warps) and tensor-memory allocation.  Per layer:
-//   [router]           all CTAs, (32 experts x 1024 columns) units: partial logits
-//                      and the layer input as the experts' E4M3-term operand
+//   [router]           all CTAs, (32 experts x 256..1024 columns) units: partial
+//                      logits, completed per expert group by the group's last unit;
+//                      every warp of the grid: the layer input as the experts'
+//                      operand (8 E2M1 terms per MX block)
 //   -- grid barrier --
-//   [route]            small blocks (T*k <= 64): every CTA sums the slice partials
-//                      (in order), takes the top-k and groups the pairs in its own
-//                      shared memory (identical results everywhere; CTA 0 also
-//                      publishes them); larger blocks: CTA 0 builds a global work
-//                      list while the other CTAs wait on a release flag
+//   [route]            small blocks (T*k <= 64): every CTA takes the top-k and groups
+//                      the pairs in its own shared memory (identical results
+//                      everywhere; CTA 0 publishes them after its expert phase);
+//                      larger blocks: CTA 0 builds a global work list while the
+//                      other CTAs wait on a release flag
 //   [experts]          the work-queue expert phase of expert_tc.cuh
 //   -- grid barrier --
 //   [combine]          all CTAs, (token, 1024 columns) units: gate-weighted sum of
@@ -65,7 +67,9 @@ struct PersistParams {
     uint8_t* xb4;      // expert operand of the layer input (expert_tc.cuh layouts)
     uint8_t* xsf;
     float* ss;         // [T, ceil(H / 1024)] sums of squares of the residual per column chunk
-    float* rpart;      // [H / 512, T, E]
+    float* rpart;      // [H / rslice, T, E] router slice partials
+    int rslice;        // columns per router unit (256, 512 or 1024; divides H)
+    int* rcnt;         // [kMaxPersistLayers, 32] finished router units per expert group (zeroed per launch)
     unsigned long long* tstamp;   // CTA 0's %globaltimer at phase ends (or NULL)
     TcArgs ta;         // expert phase: operands, partial, status, timeout (per-layer fields set per layer)
     RouteBufs rb;
@@ -167,286 +171,495 @@ __device__ __forceinline__ float inv_rms(const PersistParams& p, int t) {
     return 1.0f / sqrtf(tot / (float)p.H + p.eps);
 }
 
-// Router unit u = (expert group g of 32, column slice s of 1024): partial logits of
-// the group over the slice for every token, 8 tokens at a time.  Each warp loads its
-// 2 expert rows over the slice once; the slice of the layer input (x, or RMSNorm of
-// the residual for a stack) is staged in shared memory once per token group; units
-// of group 0 also write it as the expert phase's operand (8 E2M1 terms per block).
-__device__ __noinline__ void router_unit(const PersistParams& p, const PersistLayer& ly, int u, float* xs /*[8][512]*/,
-                                         float* sinv /*[8]*/) {
-    const int H = p.H, E = p.E, T = p.T;
-    const int n_sl = (H + kPRouteSlice - 1) / kPRouteSlice;
+// Router-weight copies: the weight rows of one router unit (up to 32 experts x
+// rslice columns, bf16) land in shared memory (kRouterW bytes into the slot area,
+// rows padded by 16 bytes) through bulk copies completing on sm.rw, one row per lane
+// of the issuing warp.  State in shared memory (rstate): [0] copies issued (mbarrier
+// phases), [1] phases waited for, [2] / [3] unit / layer whose copies were issued
+// ahead of time (-1: none).
+constexpr int kRouterW = 65536;
+__device__ __forceinline__ void router_issue(const PersistParams& p, const PersistLayer& ly, int u,
+                                             const TcSmem& sm, int* rstate, int lane) {   // whole warp
+    const int n_sl = p.H / p.rslice;
     const int eg = u / n_sl, sl = u % n_sl;
-    const int c0 = sl * kPRouteSlice;
-    const int ncols = min(kPRouteSlice, H - c0);   // 1024 or 512
+    const int ne = min(kPRouteExperts, p.E - eg * kPRouteExperts);
+    const uint32_t row = (uint32_t)p.rslice * 2, stride = row + 16;
+    if (lane == 0) {
+        fence_proxy_async_shared();   // earlier generic accesses of the slot area come first
+        mbar_arrive_expect_tx(sm.rw, row * ne);
+    }
+    __syncwarp();
+    if (lane < ne)
+        bulk_load(sm.slots + kRouterW + lane * stride,
+                  ly.router_w + (size_t)(eg * kPRouteExperts + lane) * p.H + sl * p.rslice, row, sm.rw);
+    if (lane == 0) rstate[0] += 1;
+}
+
+// x = hi + mid + lo with each term a bf16 (round to nearest): the remainder is below
+// 2^-24 |x|, and every product with a bf16 weight is exact in fp32.
+__device__ __forceinline__ void split_bf16x3(float x, uint16_t& hi, uint16_t& mid, uint16_t& lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(h);
+    const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(m);
+    const __nv_bfloat16 l = __float2bfloat16_rn(r2);
+    hi = __bfloat16_as_ushort(h);
+    mid = __bfloat16_as_ushort(m);
+    lo = __bfloat16_as_ushort(l);
+}
+
+// Router unit u = (expert group g of 32, column slice s of p.rslice columns): partial
+// logits of the group over the slice for every token, 8 tokens at a time, on the
+// tensor cores: D [32 experts x 24] = W [32 x K] . X^T where the 24 columns of X are
+// the bf16 terms hi / mid / lo of the 8 tokens' inputs (fp32 accumulation; the
+// three terms carry the fp32 input to within 2^-24).  Warp w multiplies the K range
+// [w K/16, (w+1) K/16); the warps' results are summed in a fixed order.  The
+// weight rows come into shared memory by bulk copies (issued ahead of time where
+// possible); the slice of the layer input (x, or RMSNorm of the residual for a
+// stack) is staged as its three terms.  The unit that finishes a group last (a
+// counter per group) sums the group's slice partials in slice order and writes its
+// logits (+ bias): the result does not depend on which unit comes last.  Returns
+// false (every thread) when the weight copies time out.
+__device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLayer& ly, int l, int u,
+                                         const TcSmem& sm, int* rstate, unsigned long long deadline) {
+    const int H = p.H, E = p.E, T = p.T;
+    const int n_sl = H / p.rslice;
+    const int eg = u / n_sl, sl = u % n_sl;
+    const int c0 = sl * p.rslice;
+    const int ncols = p.rslice;                  // 256, 512 or 1024
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool computes = warp < 16;
-    const int e0 = eg * kPRouteExperts + warp * 2;
-    const int nsub = ncols / kPRouteSub;
+    const int ne = min(kPRouteExperts, E - eg * kPRouteExperts);
+    const uint32_t stride = (uint32_t)ncols * 2 + 16;   // bytes per staged row (x terms and weights)
+    uint8_t* xt = sm.slots;                              // [24][stride]: row 8 q + t = term q of token t
+    float* red = reinterpret_cast<float*>(sm.slots);     // [16 warps][32 experts][24] after the MMAs
+    float* sinv = sm.red + 32;                           // [8]
+    int* flag = rstate + 4;
     auto rs = [&](int i) {   // router timestamps of CTA 0's first unit (profiling)
-        if (u == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[48 + i] = globaltimer_ns();
+        if (u == 0 && l == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[48 + i] = globaltimer_ns();
     };
     rs(0);
-    // this warp's 2 expert rows over the slice, loaded once (8 bf16 per lane per sub-chunk)
-    uint4 wreg[kPRouteSlice / kPRouteSub][2];
-#pragma unroll
-    for (int c = 0; c < kPRouteSlice / kPRouteSub; ++c)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int e = e0 + q;
-            wreg[c][q] = (computes && e < E && c < nsub)
-                             ? __ldg(reinterpret_cast<const uint4*>(ly.router_w + (size_t)e * H + c0 + c * kPRouteSub +
-                                                                    lane * 8))
-                             : make_uint4(0u, 0u, 0u, 0u);
-        }
+    fence_proxy_async_shared();
+    __syncthreads();   // earlier users of the slot area are done
+    if (warp == 0) {
+        const bool pre = rstate[2] == u && rstate[3] == l;
+        __syncwarp();
+        if (!pre) router_issue(p, ly, u, sm, rstate, lane);
+        __syncwarp();
+        if (lane == 0) rstate[2] = rstate[3] = -1;
+    }
+    __syncthreads();
+    const uint32_t parity = (uint32_t)(rstate[0] - 1) & 1u;
+    const uint32_t xs_a = smem_u32(xt), ws_a = smem_u32(sm.slots + kRouterW);
+    bool have_w = false;
     for (int t0 = 0; t0 < T; t0 += kPRouteTok) {
         const int nt = min(kPRouteTok, T - t0);
-        __syncthreads();
+        if (t0 > 0) __syncthreads();   // the previous group's sums have been read
         if (t0 == 0) rs(1);
         if (p.norm && warp < nt) {
             const float v = inv_rms(p, t0 + warp);
             if (lane == 0) sinv[warp] = v;
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < nt * (ncols / 4); i += blockDim.x) {
-            const int t = i / (ncols / 4), c = (i % (ncols / 4)) * 4;
-            const size_t o = (size_t)(t0 + t) * H + c0 + c;
-            float4 v;
-            if (p.norm) {
-                const float4 r = __ldcg(reinterpret_cast<const float4*>(p.resid + o));
-                const uint2 wv = __ldg(reinterpret_cast<const uint2*>(ly.norm_w + c0 + c));
-                const float iv = sinv[t];
-                v = make_float4(r.x * iv * bf16_lo(wv.x), r.y * iv * bf16_hi(wv.x), r.z * iv * bf16_lo(wv.y),
-                                r.w * iv * bf16_hi(wv.y));
-            } else {
-                const uint2 xv = __ldg(reinterpret_cast<const uint2*>(p.x + o));
-                v = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
+        // stage the three bf16 terms of the 8 tokens' inputs (tokens >= nt: zero)
+        const int n4 = ncols / 4;
+        for (int i0 = threadIdx.x; i0 < kPRouteTok * n4; i0 += 4 * blockDim.x) {
+            float4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {   // loads first (in flight together), then the stores
+                const int i = i0 + j * blockDim.x;
+                const int t = i / n4, c = (i % n4) * 4;
+                v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < kPRouteTok * n4 && t < nt) {
+                    const size_t o = (size_t)(t0 + t) * H + c0 + c;
+                    if (p.norm) {
+                        const float4 r = __ldcg(reinterpret_cast<const float4*>(p.resid + o));
+                        const uint2 wv = __ldg(reinterpret_cast<const uint2*>(ly.norm_w + c0 + c));
+                        const float iv = sinv[t];
+                        v[j] = make_float4(r.x * iv * bf16_lo(wv.x), r.y * iv * bf16_hi(wv.x),
+                                           r.z * iv * bf16_lo(wv.y), r.w * iv * bf16_hi(wv.y));
+                    } else {
+                        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(p.x + o));
+                        v[j] = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
+                    }
+                }
             }
-            *reinterpret_cast<float4*>(xs + t * kPRouteSlice + c) = v;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * blockDim.x;
+                if (i >= kPRouteTok * n4) continue;
+                const int t = i / n4, c = (i % n4) * 4;
+                uint16_t h[4], m[4], lo[4];
+                split_bf16x3(v[j].x, h[0], m[0], lo[0]);
+                split_bf16x3(v[j].y, h[1], m[1], lo[1]);
+                split_bf16x3(v[j].z, h[2], m[2], lo[2]);
+                split_bf16x3(v[j].w, h[3], m[3], lo[3]);
+                uint8_t* base = xt + (size_t)t * stride + c * 2;
+                *reinterpret_cast<uint2*>(base) =
+                    make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+                *reinterpret_cast<uint2*>(base + 8 * stride) =
+                    make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
+                *reinterpret_cast<uint2*>(base + 16 * stride) =
+                    make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+            }
         }
-        __syncthreads();
+        if (!have_w) {   // the weight rows have landed (bounded wait)
+            const int ok = wait_phase(sm.rw, parity, deadline, p.wl.abort) ? 1 : 0;
+            if (__syncthreads_and(ok) == 0) {
+                if (threadIdx.x == 0 && atomicExch(p.wl.abort, 1) == 0) raise_status(p.ta.status, MOE_ERR_TIMEOUT, -3);
+                return false;
+            }
+            if (threadIdx.x == 0) rstate[1] = rstate[0];
+            have_w = true;
+        } else {
+            __syncthreads();
+        }
         if (t0 == 0) rs(2);
-        if (eg == 0) {
-            // expert operand of this slice: 8 E2M1 terms per MX block (token, 32 columns)
-            const int nb = ncols / 32;
-            for (int i = warp; i < nt * nb; i += blockDim.x >> 5) {
-                const int t = i / nb, kbl = i % nb;
-                uint32_t sb0, sb1;
-                const uint32_t codes = split_e2m1_terms(xs[t * kPRouteSlice + kbl * 32 + lane], sb0, sb1);
-                store_act_terms(p.xb4, p.xsf, H, t0 + t, c0 / 32 + kbl, lane, codes, sb0, sb1);
+        // this warp's K range: ncols / 16 columns = 1, 2 or 4 steps of 16
+        float d[2][3][4];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int b = 0; b < 3; ++b)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) d[a][b][q] = 0.0f;
+        const int kw = ncols / 16;
+        for (int ks = 0; ks < kw; ks += 16) {
+            const int k0 = warp * kw + ks;
+            uint32_t af[2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+                ldmatrix_x4(ws_a + (uint32_t)(mt * 16 + (lane & 15)) * stride + (uint32_t)(k0 + (lane >> 4) * 8) * 2,
+                            af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
+            uint32_t b0, b1, b2, b3, b4, b5;
+            ldmatrix_x4(xs_a + (uint32_t)((lane >> 4) * 8 + (lane & 7)) * stride +
+                            (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2,
+                        b0, b1, b2, b3);
+            ldmatrix_x2(xs_a + (uint32_t)(16 + (lane & 7)) * stride + (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2, b4,
+                        b5);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                mma_bf16_16816(d[mt][0], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b0, b1);
+                mma_bf16_16816(d[mt][1], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b2, b3);
+                mma_bf16_16816(d[mt][2], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b4, b5);
             }
         }
-        float accp[kPRouteTok][2];
+        __syncthreads();   // every warp's reads of the x terms are done: red overwrites them
 #pragma unroll
-        for (int t = 0; t < kPRouteTok; ++t)
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int q = 0; q < 2; ++q) accp[t][q] = 0.0f;
-        if (computes) {
-#pragma unroll
-            for (int c = 0; c < kPRouteSlice / kPRouteSub; ++c) {
-                if (c >= nsub) break;
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    float w[8];
-                    const uint32_t* v = reinterpret_cast<const uint32_t*>(&wreg[c][q]);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        w[2 * i] = bf16_lo(v[i]);
-                        w[2 * i + 1] = bf16_hi(v[i]);
-                    }
-#pragma unroll
-                    for (int t = 0; t < kPRouteTok; ++t) {
-                        if (t < nt) {
-                            const float4* xp =
-                                reinterpret_cast<const float4*>(xs + t * kPRouteSlice + c * kPRouteSub + lane * 8);
-                            const float4 xa = xp[0], xb = xp[1];
-                            float a = accp[t][q];
-                            a = fmaf(xa.x, w[0], a); a = fmaf(xa.y, w[1], a);
-                            a = fmaf(xa.z, w[2], a); a = fmaf(xa.w, w[3], a);
-                            a = fmaf(xb.x, w[4], a); a = fmaf(xb.y, w[5], a);
-                            a = fmaf(xb.z, w[6], a); a = fmaf(xb.w, w[7], a);
-                            accp[t][q] = a;
-                        }
-                    }
-                }
+            for (int nb = 0; nb < 3; ++nb) {
+                const int e = mt * 16 + (lane >> 2), n = nb * 8 + 2 * (lane & 3);
+                float* r = red + warp * 768;
+                r[e * 24 + n] = d[mt][nb][0];
+                r[e * 24 + n + 1] = d[mt][nb][1];
+                r[(e + 8) * 24 + n] = d[mt][nb][2];
+                r[(e + 8) * 24 + n + 1] = d[mt][nb][3];
             }
-#pragma unroll
-            for (int t = 0; t < kPRouteTok; ++t)
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const float v = warp_sum(accp[t][q]);
-                    if (lane == q && t < nt && e0 + q < E) p.rpart[((size_t)sl * T + t0 + t) * E + e0 + q] = v;
-                }
+        __syncthreads();
+        if (threadIdx.x < kPRouteExperts * kPRouteTok) {   // (expert, token): warps in order, then the terms
+            const int e = threadIdx.x >> 3, t = threadIdx.x & 7;
+            float sh = 0.0f, sm_ = 0.0f, slo = 0.0f;
+            for (int w = 0; w < 16; ++w) {
+                const float* r = red + w * 768 + e * 24;
+                sh += r[t];
+                sm_ += r[8 + t];
+                slo += r[16 + t];
+            }
+            if (t < nt && e < ne) p.rpart[((size_t)sl * T + t0 + t) * E + eg * kPRouteExperts + e] = sh + (sm_ + slo);
         }
         if (t0 == 0) rs(3);
     }
+    // the last unit of the group turns the slice partials into logits
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int old = atomicAdd(p.rcnt + l * 32 + eg, 1);
+        *flag = old == n_sl - 1;
+        __threadfence();
+    }
+    __syncthreads();
+    if (*flag) {
+        for (int i = threadIdx.x; i < T * kPRouteExperts; i += blockDim.x) {
+            const int t = i / kPRouteExperts, e = eg * kPRouteExperts + i % kPRouteExperts;
+            if (i % kPRouteExperts >= ne) continue;
+            const float* src = p.rpart + (size_t)t * E + e;
+            float z = 0.0f;
+            for (int s0 = 0; s0 < n_sl; s0 += 8) {   // 8 loads in flight, summed in slice order
+                float a[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) a[q] = s0 + q < n_sl ? __ldcg(src + (size_t)(s0 + q) * T * E) : 0.0f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (s0 + q < n_sl) z += a[q];
+            }
+            p.rb.logits[(size_t)t * E + e] = z + (ly.router_b ? __ldg(ly.router_b + e) : 0.0f);
+        }
+    }
+    rs(4);
+    return true;
+}
+
+// The expert operand of the layer input: task i = (token t, MX block kb) splits the
+// block's 32 values (x, or RMSNorm of the residual) into 8 E2M1 terms.  Whole warps;
+// the tasks are spread over every warp of the grid, starting from the last CTA
+// (the first CTAs run the router units).
+__device__ __noinline__ void operand_tasks(const PersistParams& p, const PersistLayer& ly) {
+    const int H = p.H, nb = H / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int gw = (gridDim.x - 1 - blockIdx.x) * nw + warp;
+    for (int i = gw; i < p.T * nb; i += gridDim.x * nw) {
+        const int t = i / nb, kb = i % nb;
+        const size_t o = (size_t)t * H + kb * 32 + lane;
+        float v;
+        if (p.norm) {
+            const float iv = inv_rms(p, t);
+            v = __ldcg(p.resid + o) * iv * __bfloat162float(ly.norm_w[kb * 32 + lane]);
+        } else {
+            v = __bfloat162float(p.x[o]);
+        }
+        uint32_t sb0, sb1;
+        const uint32_t codes = split_e2m1_terms(v, sb0, sb1);
+        store_act_terms(p.xb4, p.xsf, H, t, kb, lane, codes, sb0, sb1);
+    }
+    fence_proxy_async_global();   // read next by the expert phase's bulk copies
+}
+
+// Orderable key of a logit for unsigned max: larger logits give larger keys; NaN
+// ranks with -inf.  Key 0 is below every logit (used for taken / absent entries).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    uint32_t u = __float_as_uint(v);
+    if (v != v) u = 0xFF800000u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // Routing of a small verify block (T*k <= 64, T*E <= 8192) by every CTA into its own
-// shared memory: logits from the slice partials (slice order), top-k + gates, and
-// the grouping as a routing table for the expert phase.  All CTAs compute the same
-// values; CTA 0 also publishes idx / gates / grouping for the combine and the
-// debug copies.  scratch: >= T*E + 2*T*k + 2*E + 64 ints of shared memory.
-__device__ __noinline__ void route_local(const PersistParams& p, const PersistLayer& ly, int l, int* scratch,
-                                         RouteTable* rt) {
-    const int T = p.T, E = p.E, k = p.k, H = p.H;
-    const RouteBufs& rb = p.rb;
+// shared memory: the layer's logits, top-k + gates, and the grouping as a routing
+// table for the expert phase and the combine.  Every CTA computes the same values.
+// scratch: >= T*E + 2*E + 64 ints of shared memory.
+__device__ __noinline__ void route_small(const PersistParams& p, int l, int* scratch, RouteTable* rt) {
+    const int T = p.T, E = p.E, k = p.k;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     auto sub = [&](int i) {   // sub-step timestamps of the first layer, CTA 0 (profiling)
         if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[40 + i] = globaltimer_ns();
     };
     sub(0);
     float* lg = reinterpret_cast<float*>(scratch);   // [T * E]
-    int* sidx = scratch + T * E;                     // [T * k]
-    float* sgate = reinterpret_cast<float*>(sidx + T * k);
-    int* cnt = sidx + 2 * T * k;                     // [E]
-    int* fill = cnt + E;                             // [E]
-    const int n_sl = (H + kPRouteSlice - 1) / kPRouteSlice;   // <= 16
-    for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
-        float a[16];
+    int* cnt = scratch + T * E;                      // [E]
+    int* off = cnt + E;                              // [E]
+    int* wsum = off + E;                             // [32 + 4]
+    const int n = T * E;
+    for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {   // 8 loads in flight per thread
+        float v[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) a[q] = q < n_sl ? __ldcg(p.rpart + (size_t)q * T * E + i) : 0.0f;
-        float z = 0.0f;
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * blockDim.x;
+            v[q] = i < n ? __ldcg(p.rb.logits + i) : 0.0f;
+        }
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-            if (q < n_sl) z += a[q];
-        lg[i] = z + (ly.router_b ? __ldg(ly.router_b + i % E) : 0.0f);
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * blockDim.x;
+            if (i < n) lg[i] = v[q];
+        }
     }
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     sub(1);
+    // top-k + gates, one warp per token: lane l owns experts l, l + 32, ...; each
+    // round takes the largest key (redux max), the lowest expert among equal keys
+    // (redux min), and the winning lane moves to its next candidate.  For k <= 8
+    // every lane keeps its own 8 best (key desc, expert asc) sorted in registers;
+    // for larger k the winning lane rescans its experts.
     for (int t = warp; t < T; t += nw) {
-        const float* lrow = lg + (size_t)t * E;
-        float lv[kMaxExperts / 32];
+        const float* row = lg + (size_t)t * E;
+        uint32_t mine = 0u;
+        if (k <= 8) {
+            uint32_t kk[8], ee[8];
 #pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
-            const int e = lane + 32 * i;
-            float v = e < E ? lrow[e] : __int_as_float(0xFF800000);
-            if (v != v) v = __int_as_float(0xFF800000);
-            lv[i] = v;
-        }
-        float prev_v = __int_as_float(0x7F800000);
-        int prev_e = -1;
-        float my_sel = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            float bv = __int_as_float(0xFF800000);
-            int be = 0x7FFFFFFF;
+            for (int i = 0; i < 8; ++i) { kk[i] = 0u; ee[i] = 0xFFFFFFFFu; }
+#pragma unroll 4
+            for (int e = lane; e < E; e += 32) {
+                uint32_t ck = logit_key(row[e]), ce = (uint32_t)e;
 #pragma unroll
-            for (int i = 0; i < kMaxExperts / 32; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && route_before(prev_v, prev_e, lv[i], e) && route_before(lv[i], e, bv, be)) {
-                    bv = lv[i];
-                    be = e;
+                for (int i = 0; i < 8; ++i) {   // keep the larger here, carry the smaller down
+                    const bool gt = ck > kk[i];
+                    const uint32_t tk = gt ? kk[i] : ck, te = gt ? ee[i] : ce;
+                    kk[i] = gt ? ck : kk[i];
+                    ee[i] = gt ? ce : ee[i];
+                    ck = tk;
+                    ce = te;
                 }
             }
+            for (int j = 0; j < k; ++j) {
+                const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, kk[0]);
+                const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, kk[0] == kmax ? ee[0] : 0xFFFFFFFFu);
+                if (lane == j) mine = emin;
+                if (ee[0] == emin) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-                if (route_before(ov, oe, bv, be)) { bv = ov; be = oe; }
+                    for (int i = 0; i < 7; ++i) { kk[i] = kk[i + 1]; ee[i] = ee[i + 1]; }
+                    kk[7] = 0u;
+                    ee[7] = 0xFFFFFFFFu;
+                }
             }
-            prev_v = bv;
-            prev_e = be;
-            if (lane == j) my_sel = bv;
-            if (lane == 0) sidx[t * k + j] = be;
+        } else {
+            uint32_t taken = 0u;
+            uint32_t bk = 0u;
+            uint32_t be = 0xFFFFFFFFu;
+            auto rescan = [&]() {
+                bk = 0u;
+                be = 0xFFFFFFFFu;
+                for (int i = 0, e = lane; e < E; ++i, e += 32) {
+                    const uint32_t kk = ((taken >> i) & 1u) ? 0u : logit_key(row[e]);
+                    if (kk > bk) { bk = kk; be = (uint32_t)e; }
+                }
+            };
+            rescan();
+            for (int j = 0; j < k; ++j) {
+                const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
+                const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, bk == kmax ? be : 0xFFFFFFFFu);
+                if (lane == j) mine = emin;
+                if ((int)(emin & 31u) == lane) {
+                    taken |= 1u << (emin >> 5);
+                    rescan();
+                }
+            }
         }
-        const float m = __shfl_sync(0xFFFFFFFFu, my_sel, 0);
-        const float ex = lane < k ? expf(my_sel - m) : 0.0f;
+        float v = lane < k ? row[mine] : 0.0f;
+        if (v != v) v = __int_as_float(0xFF800000);
+        const float m = __shfl_sync(0xFFFFFFFFu, v, 0);
+        const float ex = lane < k ? expf(v - m) : 0.0f;
         const float den = warp_sum(ex);
-        if (lane < k) sgate[t * k + lane] = ex / den;
+        if (lane < k) {
+            rt->idx[t * k + lane] = (int)mine;
+            rt->gate[t * k + lane] = ex / den;
+        }
     }
     __syncthreads();
     sub(2);
     const int npairs = T * k;
-    if (warp == 0) {
-        // counts -> offsets (scan over E) and the routed experts in ascending id
-        for (int s = lane; s < npairs; s += 32) {
-            const int e = sidx[s];
-            if (e >= p.e_begin && e < p.e_end) atomicAdd(&cnt[e], 1);
+    for (int s = threadIdx.x; s < npairs; s += blockDim.x) {
+        const int e = rt->idx[s];
+        if (e >= p.e_begin && e < p.e_end) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    // exclusive scans over the experts of (pairs, routed flag), packed in 16-bit
+    // halves (both totals <= 64); thread i owns experts 2i and 2i + 1
+    {
+        const int ea = 2 * threadIdx.x, eb = ea + 1;
+        const int ca = ea < E ? cnt[ea] : 0, cb = eb < E ? cnt[eb] : 0;
+        const int va = (ca << 16) | (ca > 0 ? 1 : 0), vb = (cb << 16) | (cb > 0 ? 1 : 0);
+        int incl = va + vb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += u;
         }
-        __syncwarp();
-        for (int e = lane; e < E; e += 32) fill[e] = cnt[e] > 0 ? 1 : 0;
-        __syncwarp();
-        const int n_active = warp_excl_scan(fill, E);   // fill -> position among the routed experts
-        __syncwarp();
-        for (int e = lane; e < E; e += 32)
-            if (cnt[e] > 0) rt->e[fill[e]] = e;
-        __syncwarp();
-        // per routed expert: first perm position (its pairs in (t, j) order) and chunks
-        int run = 0, chunks = 0;
-        for (int a0 = 0; a0 < n_active; a0 += 32) {
-            const int a = a0 + lane;
-            const int c = a < n_active ? cnt[rt->e[a]] : 0;
-            const int ch = (c + kTmaTok - 1) / kTmaTok;
-            int ic = c, ich = ch;
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int s = lane < nw ? wsum[lane] : 0;
+            int si = s;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xFFFFFFFFu, ic, o);
-                const int v = __shfl_up_sync(0xFFFFFFFFu, ich, o);
-                if (lane >= o) { ic += u; ich += v; }
+                const int u = __shfl_up_sync(0xFFFFFFFFu, si, o);
+                if (lane >= o) si += u;
             }
-            if (a < n_active) {
-                rt->beg[a] = run + ic - c;
-                rt->cnt[a] = c;
-                rt->chunk0[a] = chunks + ich - ch;
-                fill[rt->e[a]] = run + ic - c;   // running fill position of the expert
-            }
-            run += __shfl_sync(0xFFFFFFFFu, ic, 31);
-            chunks += __shfl_sync(0xFFFFFFFFu, ich, 31);
+            if (lane < nw) wsum[lane] = si - s;
+            if (lane == 31) wsum[32] = si;
         }
-        __syncwarp();
-        if (lane == 0) {
-            rt->n_active = n_active;
-            rt->n_chunks = chunks;
-            rt->pad0 = run;   // pairs routed into the shard
-            for (int s = 0; s < npairs; ++s) {   // pairs in (t, j) order
-                const int e = sidx[s];
-                if (e < p.e_begin || e >= p.e_end) continue;
-                const int pos = fill[e]++;
-                rt->tok[pos] = s / k;
-                rt->pair[pos] = s;
+        __syncthreads();
+        const int xa = wsum[warp] + incl - va - vb, xb = xa + va;
+        if (ea < E) {
+            off[ea] = xa >> 16;
+            if (ca > 0) {
+                rt->e[xa & 0xFFFF] = ea;
+                rt->beg[xa & 0xFFFF] = xa >> 16;
+                rt->cnt[xa & 0xFFFF] = ca;
+            }
+        }
+        if (eb < E) {
+            off[eb] = xb >> 16;
+            if (cb > 0) {
+                rt->e[xb & 0xFFFF] = eb;
+                rt->beg[xb & 0xFFFF] = xb >> 16;
+                rt->cnt[xb & 0xFFFF] = cb;
             }
         }
     }
     __syncthreads();
     sub(3);
-    if (blockIdx.x == 0) {   // publish for the combine, the down epilogue's caller and the debug copies
-        for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
-            rb.idx[i] = sidx[i];
-            rb.gate[i] = sgate[i];
+    const int n_active = wsum[32] & 0xFFFF, n_in = wsum[32] >> 16;
+    if (warp == 0) {   // first chunk of each routed expert (<= 64 of them; lane owns 2)
+        const int a0 = 2 * lane, a1 = a0 + 1;
+        const int h0 = a0 < n_active ? (rt->cnt[a0] + kTmaTok - 1) / kTmaTok : 0;
+        const int h1 = a1 < n_active ? (rt->cnt[a1] + kTmaTok - 1) / kTmaTok : 0;
+        int incl = h0 + h1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += u;
         }
-        for (int i = threadIdx.x; i < T * E; i += blockDim.x) rb.logits[i] = lg[i];
-        const int na = rt->n_active;
-        for (int e = threadIdx.x; e < E; e += blockDim.x) rb.counts[e] = cnt[e];
-        for (int i = threadIdx.x; i < npairs; i += blockDim.x) rb.perm[i] = i < rt->pad0 ? rt->pair[i] : -1;
-        for (int a = threadIdx.x; a < na; a += blockDim.x) rb.active[1 + a] = rt->e[a];
-        if (threadIdx.x == 0) rb.active[0] = na;
-        __syncthreads();
-        // offsets: exclusive prefix of counts
-        if (warp == 0) {
-            for (int e = lane; e < E; e += 32) fill[e] = cnt[e];
-            __syncwarp();
-            const int total = warp_excl_scan(fill, E);
-            __syncwarp();
-            for (int e = lane; e <= E; e += 32) rb.offsets[e] = e < E ? fill[e] : total;
+        if (a0 < n_active) rt->chunk0[a0] = incl - h0 - h1;
+        if (a1 < n_active) rt->chunk0[a1] = incl - h1;
+        if (lane == 31) {
+            rt->n_active = n_active;
+            rt->n_chunks = incl;
+            rt->pad0 = n_in;   // pairs routed into the shard
         }
-        __syncthreads();
-        const int lgi = p.layer_base + l;
-        if (p.dbg.idx) for (int i = threadIdx.x; i < npairs; i += blockDim.x) p.dbg.idx[(size_t)lgi * npairs + i] = sidx[i];
-        if (p.dbg.gate) for (int i = threadIdx.x; i < npairs; i += blockDim.x) p.dbg.gate[(size_t)lgi * npairs + i] = sgate[i];
-        if (p.dbg.perm) for (int i = threadIdx.x; i < npairs; i += blockDim.x) p.dbg.perm[(size_t)lgi * npairs + i] = rb.perm[i];
-        if (p.dbg.counts) for (int i = threadIdx.x; i < E; i += blockDim.x) p.dbg.counts[(size_t)lgi * E + i] = cnt[i];
-        if (p.dbg.offsets)
-            for (int i = threadIdx.x; i <= E; i += blockDim.x) p.dbg.offsets[(size_t)lgi * (E + 1) + i] = rb.offsets[i];
     }
+    // perm position of pair s: its expert's offset + the same-expert pairs before it
+    for (int s = threadIdx.x; s < npairs; s += blockDim.x) {
+        const int e = rt->idx[s];
+        if (e < p.e_begin || e >= p.e_end) continue;
+        int r = 0;
+        for (int q = 0; q < s; ++q) r += rt->idx[q] == e ? 1 : 0;
+        rt->tok[off[e] + r] = s / k;
+        rt->pair[off[e] + r] = s;
+    }
+    __syncthreads();
     sub(4);
+}
+
+// The routing of a small verify block, published by one CTA from its routing table:
+// idx / gates / counts / offsets / perm / active list (the logits are already in the
+// workspace), and the optional per-layer copies.  Called after that CTA's expert phase.
+__device__ __noinline__ void publish_small(const PersistParams& p, int l, const RouteTable* rt) {
+    const int T = p.T, E = p.E, k = p.k, npairs = T * k;
+    const RouteBufs& rb = p.rb;
+    const int na = rt->n_active, n_in = rt->pad0;
+    const int lgi = p.layer_base + l;
+    for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
+        const int perm = i < n_in ? rt->pair[i] : -1;
+        rb.idx[i] = rt->idx[i];
+        rb.gate[i] = rt->gate[i];
+        rb.perm[i] = perm;
+        if (p.dbg.idx) p.dbg.idx[(size_t)lgi * npairs + i] = rt->idx[i];
+        if (p.dbg.gate) p.dbg.gate[(size_t)lgi * npairs + i] = rt->gate[i];
+        if (p.dbg.perm) p.dbg.perm[(size_t)lgi * npairs + i] = perm;
+    }
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        int lo = 0, hi = na;   // first routed expert with id >= e
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (rt->e[mid] < e) lo = mid + 1; else hi = mid;
+        }
+        const int offs = lo < na ? rt->beg[lo] : n_in;
+        const int c = (e < E && lo < na && rt->e[lo] == e) ? rt->cnt[lo] : 0;
+        rb.offsets[e] = offs;
+        if (p.dbg.offsets) p.dbg.offsets[(size_t)lgi * (E + 1) + e] = offs;
+        if (e < E) {
+            rb.counts[e] = c;
+            if (p.dbg.counts) p.dbg.counts[(size_t)lgi * E + e] = c;
+        }
+    }
+    for (int a = threadIdx.x; a < na; a += blockDim.x) rb.active[1 + a] = rt->e[a];
+    if (threadIdx.x == 0) rb.active[0] = na;
 }
 
 // Combine unit (token t, column chunk c of 1024): out = sum_j gate[t, j] *
 // partial[t*k + j] (slots in order, pairs outside the expert shard skipped); with a
 // residual stack r += out and the chunk's sum of squares of r is kept for the next
 // RMSNorm.  The last layer writes y.
-__device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, float* red) {
+__device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, float* red, const RouteTable* rt) {
     const int H = p.H, k = p.k;
     const int nc = (H + kCombineChunk - 1) / kCombineChunk;
     const int t = u / nc, c = u % nc;
@@ -459,8 +672,9 @@ __device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, 
     for (int j = 0; j < kMaxTopK; ++j) {   // gates of the slots in the shard (0 outside)
         gj[j] = 0.0f;
         if (j < k) {
-            const int e = __ldcg(rb.idx + t * k + j);
-            gj[j] = (e >= p.e_begin && e < p.e_end) ? __ldcg(rb.gate + t * k + j) : 0.0f;
+            const int e = rt ? rt->idx[t * k + j] : __ldcg(rb.idx + t * k + j);
+            const float g = rt ? rt->gate[t * k + j] : __ldcg(rb.gate + t * k + j);
+            gj[j] = (e >= p.e_begin && e < p.e_end) ? g : 0.0f;
         }
     }
     float ssl = 0.0f;
@@ -468,13 +682,26 @@ __device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, 
     if (h < ncols) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            if (j >= k || gj[j] == 0.0f) continue;
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ta.partial + (size_t)(t * k + j) * H + c0 + h));
-            acc.x = fmaf(gj[j], v.x, acc.x);
-            acc.y = fmaf(gj[j], v.y, acc.y);
-            acc.z = fmaf(gj[j], v.z, acc.z);
-            acc.w = fmaf(gj[j], v.w, acc.w);
+        for (int j0 = 0; j0 < kMaxTopK; j0 += 8) {   // 8 slots' loads in flight, summed in slot order
+            if (j0 >= k) break;
+            float4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int j = j0 + q;
+                v[q] = (j < k && gj[j] != 0.0f)
+                           ? __ldcg(reinterpret_cast<const float4*>(p.ta.partial + (size_t)(t * k + j) * H + c0 + h))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int j = j0 + q;
+                if (j < k && gj[j] != 0.0f) {
+                    acc.x = fmaf(gj[j], v[q].x, acc.x);
+                    acc.y = fmaf(gj[j], v[q].y, acc.y);
+                    acc.z = fmaf(gj[j], v[q].z, acc.z);
+                    acc.w = fmaf(gj[j], v[q].w, acc.w);
+                }
+            }
         }
         if (p.norm) {
             const float4 r = __ldcg(reinterpret_cast<const float4*>(p.resid + o + h));
@@ -532,20 +759,7 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
         if (l == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[40 + i] = globaltimer_ns();
     };
     sub(0);
-    // ---- logits: the slice partials summed in slice order; all slices of an
-    // element are loaded together (H / 512 <= 32)
-    const int n_sl = (H + kPRouteSlice - 1) / kPRouteSlice;   // <= 16
-    for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
-        float a[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) a[q] = q < n_sl ? __ldcg(p.rpart + (size_t)q * T * E + i) : 0.0f;
-        float z = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-            if (q < n_sl) z += a[q];
-        rb.logits[i] = z + (ly.router_b ? ly.router_b[i % E] : 0.0f);
-    }
-    __syncthreads();
+    // (the logits were completed by the router units)
     // ---- top-k + gates, one warp per token (logits of lane l: experts l, l+32, ...)
     for (int t = warp; t < T; t += nw) {
         const float* lrow = rb.logits + (size_t)t * E;
@@ -743,18 +957,37 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     int* abort = p.wl.abort;
     int* status = p.ta.status;
     float* red = sm.red;                                   // block reductions (<= 32 floats)
-    float* xs = reinterpret_cast<float*>(sm.slots);        // router staging / routing scratch
-    float* sinv = sm.red + 32;                             // [8]
+    float* xs = reinterpret_cast<float*>(sm.slots);        // routing scratch
     unsigned epoch = 0;
     TcRoleState rs{0u, 0u, 0u, 0u};
-    const int n_sl = (p.H + kPRouteSlice - 1) / kPRouteSlice;
-    const int units = ((p.E + kPRouteExperts - 1) / kPRouteExperts) * n_sl;
+    int* rstate = reinterpret_cast<int*>(sm.red + 40);     // router-weight copy state (router_issue)
+    const int units = ((p.E + kPRouteExperts - 1) / kPRouteExperts) * (p.H / p.rslice);
     const int cunits = p.T * ((p.H + kCombineChunk - 1) / kCombineChunk);
     const bool small = p.T * p.k <= kRtMaxPairs && p.T * p.E <= 8192;
     auto stamp = [&](int i) {
         if (blockIdx.x == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[i] = globaltimer_ns();
     };
     stamp(0);
+    if (threadIdx.x < 32) {   // warp 0: this CTA's first router unit, weights into shared memory, x into L2
+        const int lane = threadIdx.x;
+        if (lane == 0) {
+            rstate[0] = rstate[1] = 0;
+            rstate[2] = rstate[3] = -1;
+        }
+        __syncwarp();
+        if (blockIdx.x < units) {
+            router_issue(p, p.layer[0], blockIdx.x, sm, rstate, lane);
+            if (lane == 0) {
+                rstate[2] = blockIdx.x;
+                rstate[3] = 0;
+            }
+            if (!p.norm) {
+                const int c0 = (blockIdx.x % (p.H / p.rslice)) * p.rslice;
+                for (int t = lane; t < min(p.T, 64); t += 32)
+                    prefetch_l2(p.x + (size_t)t * p.H + c0, (uint32_t)p.rslice * 2);
+            }
+        }
+    }
     if (p.norm && p.init_from_x) {
         for (int u = blockIdx.x; u < cunits; u += gridDim.x) stack_init_unit(p, u, red);
         if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
@@ -763,13 +996,14 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
 
     for (int l = 0; l < p.L; ++l) {
         const PersistLayer& ly = p.layer[l];
-        for (int u = blockIdx.x; u < units; u += gridDim.x) router_unit(p, ly, u, xs, sinv);
+        for (int u = blockIdx.x; u < units; u += gridDim.x)
+            if (!router_unit(p, ly, l, u, sm, rstate, deadline)) return;
+        operand_tasks(p, ly);
         const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
         if (!grid_sync(p.bar, epoch, deadline, abort, status, withhold)) return;
         stamp(2 + 4 * l);
         if (small) {
-            route_local(p, ly, l, reinterpret_cast<int*>(xs), sm.rt);
-            __syncthreads();
+            route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
             stamp(3 + 4 * l);
         } else if (blockIdx.x == 0) {
             route_phase(p, ly, l, reinterpret_cast<int*>(xs));
@@ -803,9 +1037,21 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         ta.rt = small ? sm.rt : nullptr;
         if (l != 0 || p.layer_base != 0) ta.trace = nullptr;
         persist_expert_phase(ta, &ly.maps, smem_raw, tmem, &rs, deadline);
+        if (l + 1 < p.L && blockIdx.x < units) {   // the next layer's first router unit, ahead of time
+            fence_proxy_async_shared();
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                router_issue(p, p.layer[l + 1], blockIdx.x, sm, rstate, threadIdx.x);
+                if (threadIdx.x == 0) {
+                    rstate[2] = blockIdx.x;
+                    rstate[3] = l + 1;
+                }
+            }
+        }
+        if (small && blockIdx.x == 0) publish_small(p, l, sm.rt);
         if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
         stamp(4 + 4 * l);
-        for (int u = blockIdx.x; u < cunits; u += gridDim.x) combine_unit(p, u, l, red);
+        for (int u = blockIdx.x; u < cunits; u += gridDim.x) combine_unit(p, u, l, red, small ? sm.rt : nullptr);
         stamp(5 + 4 * l);
         if (l + 1 < p.L && !grid_sync(p.bar, epoch, deadline, abort, status)) return;
     }
@@ -817,6 +1063,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_con
     const uint32_t tmem = tc_setup(sm);
     const unsigned long long deadline = globaltimer_ns() + p.ta.timeout_ns;
     persist_layers(p, smem_raw, tmem, deadline);
+    __syncthreads();
+    if (threadIdx.x == 0) {   // router-weight copies still in flight (a run cut short) land before exit
+        const int* rstate = reinterpret_cast<const int*>(sm.red + 40);
+        if (rstate[0] > rstate[1]) drain_phase(sm.rw, (uint32_t)(rstate[0] - 1) & 1u, globaltimer_ns() + p.ta.timeout_ns);
+    }
     tc_teardown(sm, tmem, p.ta.timeout_ns);
 }
 

@@ -44,6 +44,8 @@ struct RouteTable {
     int chunk0[kRtMaxPairs];   // index of its first chunk
     int tok[kRtMaxPairs];      // per perm position: token
     int pair[kRtMaxPairs];     // per perm position: pair id t*k + j
+    int idx[kRtMaxPairs];      // per pair t*k + j: routed expert
+    float gate[kRtMaxPairs];   // per pair t*k + j: gate
 };
 
 // Per-forward work list (workspace).
