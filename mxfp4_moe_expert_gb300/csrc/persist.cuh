@@ -190,8 +190,9 @@ __device__ __forceinline__ void router_issue(const PersistParams& p, const Persi
     }
     __syncwarp();
     if (lane < ne)
-        bulk_load(sm.slots + kRouterW + lane * stride,
-                  ly.router_w + (size_t)(eg * kPRouteExperts + lane) * p.H + sl * p.rslice, row, sm.rw);
+        bulk_load_stream(sm.slots + kRouterW + lane * stride,
+                         ly.router_w + (size_t)(eg * kPRouteExperts + lane) * p.H + sl * p.rslice, row, sm.rw,
+                         l2_evict_first_policy());
     if (lane == 0) rstate[0] += 1;
 }
 
