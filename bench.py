@@ -227,12 +227,14 @@ def run_gpu(args):
         sampler.__enter__()
         time.sleep(0.1)
     t_wall = time.perf_counter()
+    torch.cuda.profiler.start()   # a profiler started with --profile-from-start off sees the timed region only
     for i in range(args.steps):
         flush_l2(i)
         ev[i][0].record(stream)
         moe.forward(x, y, wsp, st, kdbg[i])
         ev[i][1].record(stream)
     torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
     wall = time.perf_counter() - t_wall
     if ws > 1:
         torch.distributed.barrier()
@@ -303,7 +305,8 @@ def run_gpu(args):
         "hbm_gbs": round(gbs, 1),
         "implied_tokens_per_s": round(ACCEPTANCE_LENGTH / (us * 1e-6), 1),
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(kern_gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "frac": round(kern_gbs / peak, 4),
+                     "traffic": measured_traffic(wl.name) if persistent else None, "peak_kind": peak_kind,
                      "kernel": "persistent forward kernel" if persistent else "expert FFN kernel",
                      "kernel_us_per_layer": round(kern_us, 2),
                      "kernel_bytes_per_layer": int(kern_bytes)},
@@ -326,6 +329,30 @@ FLUSH_DESC = {
              "(cold, clean L2); inputs also larger than L2",
     "none": "not flushed; inputs larger than L2",
 }
+
+
+def kernel_sources_sha256():
+    """Hash of the library's kernel sources (the same recipe as profiles/dram_traffic.json)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "mxfp4_moe_expert_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)) + [os.path.join(ROOT, "include", "moe_mxfp4.h")]
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload):
+    """DRAM bytes per launch of the timed kernel from the committed ncu capture of this
+    workload, or None when there is none or the kernel sources changed since."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    e = json.load(open(p)).get(workload)
+    if not e or e.get("source_sha256") != kernel_sources_sha256():
+        return None
+    return int(e["dram_read_bytes"] + e["dram_write_bytes"])
 
 
 def moe_tma(wl):
