@@ -141,7 +141,8 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
 /* Bytes of device workspace a forward over num_tokens tokens needs.  The first 512
  * bytes hold the status words; in a persistent forward, bytes 64..335 receive CTA 0's
  * %globaltimer (uint64 ns) at the end of each phase (start, input staging, and per
- * layer l: router 2+4l, routing 3+4l, experts 4+4l, combine 5+4l), for profiling.
+ * layer l: router 2+4l, routing 3+4l, experts 4+4l, combine 5+4l), for profiling, and
+ * bytes 512..2559 receive each CTA's %globaltimer when it finished (CTA i at 512 + 8 i).
  * With MOE_FLAG_TRACE, bytes 4096..16383 receive the first layer's expert-phase
  * timestamps of CTA 0 as 6 arrays of 256 uint64 (ns, ring stage or item i < 256):
  * producer issues stage i, scale-factor warp sees it land, scale factors written,

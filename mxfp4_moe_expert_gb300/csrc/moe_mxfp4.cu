@@ -51,12 +51,21 @@ size_t max_items(const moe_mxfp4_config& c, int T) {
     return max_chunks(c, T) * (size_t)(c.inter / moe::kTmaRows + c.hidden / moe::kTmaRows);
 }
 
+// Per-launch counters of the persistent forward: per layer the expert-phase queue,
+// per-chunk done counters and per-expert-group router counters.
+size_t tickets_bytes(const moe_mxfp4_config& c, int T) {
+    return (size_t)moe::kMaxPersistLayers * (1 + max_chunks(c, T) + 32) * 4;
+}
+
 WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     WsLayout L{};
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     const size_t H = (size_t)c.hidden, I = (size_t)c.inter, E = (size_t)c.num_experts, k = (size_t)c.top_k;
     L.status = take(16384);   // status words, grid-barrier counters, phase timestamps, expert-phase trace
+    // the persistent forward's per-launch counters follow directly, so that one memset
+    // clears the status words and the counters
+    L.tickets = take(tickets_bytes(c, T));
     L.xstage = take((size_t)T * H * 2);
     L.ystage = take((size_t)T * H * 4);
     L.act = take((size_t)T * H * 4);
@@ -73,9 +82,7 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     const size_t chunks = max_chunks(c, T);
     L.xb4 = take(moe::xb4_bytes(T, (int)H));
     L.xsf = take(moe::xsf_bytes(T, (int)H));
-    L.ss = take((size_t)T * (H / 1024 + 1) * 4);
-    // per layer: expert-phase queue, per-chunk done counters, per-expert-group router counters
-    L.tickets = take((size_t)moe::kMaxPersistLayers * (1 + chunks + 32) * 4);
+    L.ss = take((size_t)T * (H / 256 + 1) * 4);
     L.hb4 = take(chunks * moe::hb4_chunk_bytes((int)I));
     L.hsf = take(chunks * moe::hsf_chunk_bytes((int)I));
     L.items = take(max_items(c, T) * sizeof(moe::ItemRec));
@@ -318,6 +325,7 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     p.ta = tc_args(h, T, ws, L);
     p.ta.items = p.wl.items;
     p.ta.n_items = p.wl.n_items;
+    p.wl.abort = reinterpret_cast<int*>(ws + L.status + 24);   // cleared with the status words
     p.ta.abort = p.wl.abort;
     if (c.flags & MOE_FLAG_TRACE) p.ta.trace = reinterpret_cast<unsigned long long*>(ws + L.status + 4096);
     const int chunks = (int)max_chunks(c, T);
@@ -343,7 +351,9 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
         p.dbg.offsets = dbg->expert_offsets_dev;
         p.dbg.perm = dbg->perm_dev;
     }
-    if (cudaMemsetAsync(p.wl.abort, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    // one memset: status words, abort flag, grid-barrier counter and the first launch's counters
+    if (cudaMemsetAsync(ws + L.status, 0, (L.tickets - L.status) + tickets_bytes(c, T), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
     for (int l0 = 0; l0 < c.num_layers; l0 += moe::kMaxPersistLayers) {
         const int nl = std::min(moe::kMaxPersistLayers, c.num_layers - l0);
         p.L = nl;
@@ -357,9 +367,8 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
             p.layer[l].router_b = ly.router_b_dev;
             p.layer[l].norm_w = reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev);
         }
-        if (l0 > 0 && cudaMemsetAsync(ws + L.status + 16, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
-        if (cudaMemsetAsync(ws + L.tickets, 0, (size_t)moe::kMaxPersistLayers * (1 + chunks + 32) * 4, st) !=
-            cudaSuccess)
+        if (l0 > 0 && (cudaMemsetAsync(ws + L.status + 16, 0, 8, st) != cudaSuccess ||
+                        cudaMemsetAsync(ws + L.tickets, 0, tickets_bytes(c, T), st) != cudaSuccess))
             return MOE_ERR_CUDA;
         void* kargs[] = {&p};
         if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(moe::persist_kernel), dim3(h->persist_grid),
@@ -472,14 +481,15 @@ int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens
         return MOE_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace_dev);
-    if (cudaMemsetAsync(ws + L.status, 0, 64, st) != cudaSuccess) return MOE_ERR_CUDA;
     // the TMA work-item code holds up to 512 token chunks of 8 per expert
     if (h->tma && num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok) {
         const bool events = dbg && dbg->expert_events;
         if (h->persist_grid > 0 && !(h->cfg.flags & MOE_FLAG_MULTI_KERNEL) && !events)
-            return forward_persistent(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
-        return forward_tma(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
+            return forward_persistent(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);   // clears the status itself
     }
+    if (cudaMemsetAsync(ws + L.status, 0, 64, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (h->tma && num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok)
+        return forward_tma(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
     return forward_multi_kernel(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
 }
 

@@ -34,7 +34,7 @@ constexpr int kPRouteExperts = 32;   // 16 warps x 2 expert rows
 constexpr int kPRouteSlice = 1024;   // columns per router unit: 4 sub-chunks of 256 (8 per lane)
 constexpr int kPRouteSub = 256;
 constexpr int kPRouteTok = 8;        // tokens per round
-constexpr int kCombineChunk = 1024;  // columns per combine unit
+constexpr int kCombineChunk = 256;   // columns per combine unit (and per sum-of-squares block)
 
 struct PersistLayer {
     TcMaps maps;
@@ -66,7 +66,7 @@ struct PersistParams {
     float* resid;      // [T, H] (stack)
     uint8_t* xb4;      // expert operand of the layer input (expert_tc.cuh layouts)
     uint8_t* xsf;
-    float* ss;         // [T, ceil(H / 1024)] sums of squares of the residual per column chunk
+    float* ss;         // [T, H / 256] sums of squares of the residual per column block
     float* rpart;      // [H / rslice, T, E] router slice partials
     int rslice;        // columns per router unit (256, 512 or 1024; divides H)
     int* rcnt;         // [kMaxPersistLayers, 32] finished router units per expert group (zeroed per launch)
@@ -160,14 +160,15 @@ __device__ __forceinline__ int warp_excl_scan(int* v, int n) {
     return __shfl_sync(0xFFFFFFFFu, incl, 31);
 }
 
-// 1/sqrt(mean(r^2) + eps) of token t from the chunk sums of squares (summed in
-// chunk order by one warp: every caller gets the same value).
+// 1/sqrt(mean(r^2) + eps) of token t from the block sums of squares (summed in
+// block order by one warp: every caller gets the same value).
 __device__ __forceinline__ float inv_rms(const PersistParams& p, int t) {
     const int lane = threadIdx.x & 31;
-    const int nc = (p.H + kCombineChunk - 1) / kCombineChunk;
-    float v = lane < nc ? __ldcg(p.ss + (size_t)t * nc + lane) : 0.0f;
+    const int nc = p.H / kCombineChunk;   // <= 64
+    const float v0 = lane < nc ? __ldcg(p.ss + (size_t)t * nc + lane) : 0.0f;
+    const float v1 = lane + 32 < nc ? __ldcg(p.ss + (size_t)t * nc + lane + 32) : 0.0f;
     float tot = 0.0f;
-    for (int c = 0; c < nc; ++c) tot += __shfl_sync(0xFFFFFFFFu, v, c);
+    for (int c = 0; c < nc; ++c) tot += c < 32 ? __shfl_sync(0xFFFFFFFFu, v0, c) : __shfl_sync(0xFFFFFFFFu, v1, c - 32);
     return 1.0f / sqrtf(tot / (float)p.H + p.eps);
 }
 
@@ -656,15 +657,17 @@ __device__ __noinline__ void publish_small(const PersistParams& p, int l, const 
     if (threadIdx.x == 0) rb.active[0] = na;
 }
 
-// Combine unit (token t, column chunk c of 1024): out = sum_j gate[t, j] *
-// partial[t*k + j] (slots in order, pairs outside the expert shard skipped); with a
-// residual stack r += out and the chunk's sum of squares of r is kept for the next
-// RMSNorm.  The last layer writes y.
-__device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, float* red, const RouteTable* rt) {
+// Combine unit (token t, 256-column block c): out = sum_j gate[t, j] * partial[t*k + j]
+// (slots in order, pairs outside the expert shard skipped); with a residual stack
+// r += out and the block's sum of squares of r is kept for the next RMSNorm.  The last
+// layer writes y.
+// dry: read everything but store nothing (runs the code once to bring it into the caches).
+__device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, float* red, const RouteTable* rt,
+                                          bool dry = false) {
     const int H = p.H, k = p.k;
-    const int nc = (H + kCombineChunk - 1) / kCombineChunk;
+    const int nc = H / kCombineChunk;
     const int t = u / nc, c = u % nc;
-    const int c0 = c * kCombineChunk, ncols = min(kCombineChunk, H - c0);
+    const int c0 = c * kCombineChunk, ncols = kCombineChunk;
     const RouteBufs& rb = p.rb;
     const bool last = l == p.L - 1;
     const size_t o = (size_t)t * H + c0;
@@ -707,10 +710,10 @@ __device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, 
         if (p.norm) {
             const float4 r = __ldcg(reinterpret_cast<const float4*>(p.resid + o + h));
             acc.x += r.x; acc.y += r.y; acc.z += r.z; acc.w += r.w;
-            *reinterpret_cast<float4*>(p.resid + o + h) = acc;
+            if (!dry) *reinterpret_cast<float4*>(p.resid + o + h) = acc;
             ssl = acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
         }
-        if (last && p.write_y) {
+        if (last && p.write_y && !dry) {
             if (p.y_bf16) {
                 __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b = __floats2bfloat162_rn(acc.z, acc.w);
                 uint2 v;
@@ -724,7 +727,7 @@ __device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, 
     }
     if (p.norm) {
         const float tot = block_sum(ssl, red);
-        if (threadIdx.x == 0) p.ss[(size_t)t * nc + c] = tot;
+        if (threadIdx.x == 0 && !dry) p.ss[(size_t)t * nc + c] = tot;
     }
 }
 
@@ -963,7 +966,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     TcRoleState rs{0u, 0u, 0u, 0u};
     int* rstate = reinterpret_cast<int*>(sm.red + 40);     // router-weight copy state (router_issue)
     const int units = ((p.E + kPRouteExperts - 1) / kPRouteExperts) * (p.H / p.rslice);
-    const int cunits = p.T * ((p.H + kCombineChunk - 1) / kCombineChunk);
+    const int cunits = p.T * (p.H / kCombineChunk);
     const bool small = p.T * p.k <= kRtMaxPairs && p.T * p.E <= 8192;
     auto stamp = [&](int i) {
         if (blockIdx.x == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[i] = globaltimer_ns();
@@ -1000,6 +1003,13 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         for (int u = blockIdx.x; u < units; u += gridDim.x)
             if (!router_unit(p, ly, l, u, sm, rstate, deadline)) return;
         operand_tasks(p, ly);
+        if (small && blockIdx.x >= units) {
+            // a CTA without a router unit would only wait at the barrier: it runs the routing
+            // code (results discarded; shared memory only) or, on every other such CTA, the
+            // combine code (nothing stored), so that code is in L2 when the whole grid needs it
+            if (((blockIdx.x - units) & 1) == 0 || l + 1 < p.L) route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
+            else combine_unit(p, blockIdx.x % cunits, l, red, nullptr, true);
+        }
         const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
         if (!grid_sync(p.bar, epoch, deadline, abort, status, withhold)) return;
         stamp(2 + 4 * l);
@@ -1065,6 +1075,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_con
     const unsigned long long deadline = globaltimer_ns() + p.ta.timeout_ns;
     persist_layers(p, smem_raw, tmem, deadline);
     __syncthreads();
+    if (threadIdx.x == 0 && p.tstamp && blockIdx.x < 256)   // when each CTA finished (profiling)
+        p.tstamp[56 + blockIdx.x] = globaltimer_ns();
     if (threadIdx.x == 0) {   // router-weight copies still in flight (a run cut short) land before exit
         const int* rstate = reinterpret_cast<const int*>(sm.red + 40);
         if (rstate[0] > rstate[1]) drain_phase(sm.rw, (uint32_t)(rstate[0] - 1) & 1u, globaltimer_ns() + p.ta.timeout_ns);

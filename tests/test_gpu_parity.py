@@ -173,8 +173,11 @@ def test_tma_and_multi_kernel_paths_agree(wl):
     assert_rows_close(a.double().cpu().numpy(), b.double().cpu().numpy(), what="paths")
 
 
-def test_expert_shards_sum_to_full_layer():
-    wl = SMALL[1]
+@pytest.mark.parametrize("wl", [SMALL[1], SMALL[5]], ids=lambda w: w.name)
+def test_expert_shards_sum_to_full_layer(wl):
+    """Expert-parallel shards (disjoint expert ranges) sum to the full layer; in the
+    persistent forward (SMALL[5]) some tokens have no slot in a shard, whose output rows
+    no down item writes."""
     inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
     x = inputs.x.to(DEV)
     full = _moe(wl, layers).forward(x, check=True)
