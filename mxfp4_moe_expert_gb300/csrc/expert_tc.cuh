@@ -456,8 +456,13 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                 uint8_t* sdst = s.scales + se * kTcScaleEntry;
                 const uint32_t sfa_bytes = gu ? (uint32_t)ntok * spb * 64 : (uint32_t)spb * 512;
                 mbar_arrive_expect_tx(&s.sfull[se], 2u * (uint32_t)sw * kTmaRows + sfa_bytes);
-                tma_load_2d_stream(sdst, ms0, st * 8, r0, &s.sfull[se], pol);
-                tma_load_2d_stream(sdst + kScaleBox1, ms1, st * 8, r1, &s.sfull[se], pol);
+                if (cur.pad[0] > 1) {
+                    tma_load_2d(sdst, ms0, st * 8, r0, &s.sfull[se]);
+                    tma_load_2d(sdst + kScaleBox1, ms1, st * 8, r1, &s.sfull[se]);
+                } else {
+                    tma_load_2d_stream(sdst, ms0, st * 8, r0, &s.sfull[se], pol);
+                    tma_load_2d_stream(sdst + kScaleBox1, ms1, st * 8, r1, &s.sfull[se], pol);
+                }
                 if (gu) {   // per pair: the group's stages of its token (contiguous in xsf)
                     for (int p = 0; p < ntok; ++p)
                         bulk_load(sdst + kScaleSfa + p * spb * 64,
@@ -478,8 +483,13 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
             tc_trace(a, 0, rs.it);
             ++rs.it;   // this slot now has copies in flight
             uint8_t* dst = s.slots + (size_t)slot * kTcSlotBytes;
-            tma_load_2d_stream(dst + kSlotB, mq0, st * 128, r0, &s.full[slot], pol);
-            tma_load_2d_stream(dst + kSlotB + 16384, mq1, st * 128, r1, &s.full[slot], pol);
+            if (cur.pad[0] > 1) {   // rows shared by several chunks: kept in L2 for the other chunks
+                tma_load_2d(dst + kSlotB, mq0, st * 128, r0, &s.full[slot]);
+                tma_load_2d(dst + kSlotB + 16384, mq1, st * 128, r1, &s.full[slot]);
+            } else {
+                tma_load_2d_stream(dst + kSlotB, mq0, st * 128, r0, &s.full[slot], pol);
+                tma_load_2d_stream(dst + kSlotB + 16384, mq1, st * 128, r1, &s.full[slot], pol);
+            }
             if (kPfStages > 0) {   // kPfStages ahead into L2: later in this item, else the start of the next one
                 const int ps = st + kPfStages;
                 if (ps < nk) {

@@ -905,13 +905,14 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
         const bool down = i >= n_gu;
         const int j = down ? i - n_gu : i;
         const int nrb = down ? rbd : rbu;
-        const int chunk = j / nrb, rbi = j % nrb;
-        int lo = 0, hi = n_active - 1;
+        int lo = 0, hi = n_active - 1;   // the routed expert whose items contain j
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (chunk0[mid] <= chunk) lo = mid; else hi = mid - 1;
+            if (chunk0[mid] * nrb <= j) lo = mid; else hi = mid - 1;
         }
-        const int tc = chunk - chunk0[lo];
+        const int nch = (s_cnt[lo] + kTmaTok - 1) / kTmaTok;
+        const int rr = j - chunk0[lo] * nrb, rbi = rr / nch, tc = rr % nch;   // row block major, chunk minor
+        const int chunk = chunk0[lo] + tc;
         ItemRec r;
         r.code = item_code(down ? kItemDown : kItemGateUp, rbi, tc, lo);
         r.e = s_act[lo];
@@ -920,8 +921,8 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
 #pragma unroll
         for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? s_perm[r.beg + q] : s_perm[r.beg + q] / k) : 0;
         r.chunk = chunk;
-#pragma unroll
-        for (int q = 0; q < 3; ++q) r.pad[q] = 0;
+        r.pad[0] = nch;
+        r.pad[1] = r.pad[2] = 0;
         wl.items[i] = r;
     }
     sub(4);

@@ -2,7 +2,10 @@
 // expert (perm order: each expert's pairs in (token, slot) order) and cut into
 // chunks of at most 8 pairs.  For every chunk there are I/128 gate/up items (a
 // 128-row block of the gate and of the up matrix over all of K = H) and H/256 down
-// items (a 256-row block of the down matrix over all of K = I).
+// items (a 256-row block of the down matrix over all of K = I).  Within an expert the
+// items are ordered row block major, chunk minor: the chunks that read the same
+// weight rows are claimed one after another, so those rows are streamed from HBM
+// once and served from L2 to the other chunks.
 #pragma once
 
 #include "common.cuh"
@@ -30,7 +33,7 @@ struct __align__(16) ItemRec {
     int ntok;          // pairs in the chunk (1..8)
     int tok[kTmaTok];  // gate/up items: token of each pair; down items: pair id (t*k + j)
     int chunk;         // chunk index within the layer
-    int pad[3];
+    int pad[3];        // pad[0]: chunks of the expert (the items of one row block are adjacent)
 };
 
 // Routing state of one layer kept in shared memory by every CTA when the verify
@@ -63,13 +66,14 @@ __device__ __forceinline__ ItemRec table_item(const RouteTable* rt, int idx, int
     const bool down = idx >= n_gu;
     const int j = down ? idx - n_gu : idx;
     const int nrb = down ? rbd : rbu;
-    const int chunk = j / nrb, rbi = j % nrb;
-    int lo = 0, hi = rt->n_active - 1;
+    int lo = 0, hi = rt->n_active - 1;   // the routed expert whose items contain j
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (rt->chunk0[mid] <= chunk) lo = mid; else hi = mid - 1;
+        if (rt->chunk0[mid] * nrb <= j) lo = mid; else hi = mid - 1;
     }
-    const int tc = chunk - rt->chunk0[lo];
+    const int nch = (rt->cnt[lo] + kTmaTok - 1) / kTmaTok;
+    const int rr = j - rt->chunk0[lo] * nrb, rbi = rr / nch, tc = rr % nch;   // row block major, chunk minor
+    const int chunk = rt->chunk0[lo] + tc;
     ItemRec r;
     r.code = item_code(down ? kItemDown : kItemGateUp, rbi, tc, lo);
     r.e = rt->e[lo];
@@ -78,8 +82,8 @@ __device__ __forceinline__ ItemRec table_item(const RouteTable* rt, int idx, int
 #pragma unroll
     for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? rt->pair[r.beg + q] : rt->tok[r.beg + q]) : 0;
     r.chunk = chunk;
-#pragma unroll
-    for (int q = 0; q < 3; ++q) r.pad[q] = 0;
+    r.pad[0] = nch;
+    r.pad[1] = r.pad[2] = 0;
     return r;
 }
 
@@ -130,13 +134,15 @@ __global__ void __launch_bounds__(1024) build_items_kernel(RouteBufs rb, int H, 
         const bool down = i >= n_gu;
         const int j = down ? i - n_gu : i;
         const int nrb = down ? rbd : rbu;
-        const int chunk = j / nrb, rbi = j % nrb;
-        int lo = 0, hi = n_active - 1;          // last aa with s_gu[aa] <= chunk
+        int lo = 0, hi = n_active - 1;          // the routed expert whose items contain j
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (s_gu[mid] <= chunk) lo = mid; else hi = mid - 1;
+            if (s_gu[mid] * nrb <= j) lo = mid; else hi = mid - 1;
         }
-        const int aa = lo, tc = chunk - s_gu[aa];
+        const int aa = lo;
+        const int nch = (s_cnt[aa] + kTmaTok - 1) / kTmaTok;
+        const int rr = j - s_gu[aa] * nrb, rbi = rr / nch, tc = rr % nch;   // row block major, chunk minor
+        const int chunk = s_gu[aa] + tc;
         ItemRec r;
         r.code = item_code(down ? kItemDown : kItemGateUp, rbi, tc, aa);
         r.e = s_act[aa];
@@ -145,8 +151,8 @@ __global__ void __launch_bounds__(1024) build_items_kernel(RouteBufs rb, int H, 
 #pragma unroll
         for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? s_perm[r.beg + q] : s_perm[r.beg + q] / k) : 0;
         r.chunk = chunk;
-#pragma unroll
-        for (int q = 0; q < 3; ++q) r.pad[q] = 0;
+        r.pad[0] = nch;
+        r.pad[1] = r.pad[2] = 0;
         wl.items[i] = r;
     }
 }

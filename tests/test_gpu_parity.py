@@ -110,6 +110,8 @@ SMALL = [
     Workload("tma_k_eq_E", T=3, H=512, I=1024, E=4, k=4, seed=0x5EED0112),
     Workload("tma_one_token", T=1, H=1536, I=512, E=32, k=8, seed=0x5EED0113),
     Workload("tma_many_tokens", T=40, H=512, I=512, E=4, k=2, seed=0x5EED0114),
+    # 64 pairs over 4 experts: several 8-pair chunks per expert in the shared-memory routing path
+    Workload("tma_multi_chunk", T=32, H=512, I=512, E=4, k=2, seed=0x5EED0116),
 ]
 
 
