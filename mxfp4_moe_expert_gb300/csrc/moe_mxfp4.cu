@@ -38,7 +38,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // Byte offsets of the workspace sections for T tokens.
 struct WsLayout {
     size_t status, xstage, ystage, act, resid, logits, idx, gate, counts, offsets, perm, active, hbuf, partial;
-    size_t xb4, xsf, ss, tickets, hb4, hsf, items, sync, rpart, total;
+    size_t xb4, xsf, ss, tickets, hb4, hsf, items, sync, rpart, chunk0, total;
 };
 
 // Upper bound of the chunks of one layer: every routed expert contributes
@@ -88,6 +88,7 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     L.items = take(max_items(c, T) * sizeof(moe::ItemRec));
     L.sync = take((8 + chunks) * 4);   // n_items[2], queue, abort, ..., done[chunks]
     L.rpart = take((size_t)(H / 256 + 1) * T * E * 4);   // router partials per column slice (>= 256 columns)
+    L.chunk0 = take((E + 1) * 4);
     L.total = o;
     return L;
 }
@@ -228,6 +229,7 @@ moe::WorkList work_list(char* ws, const WsLayout& L) {
     wl.queue = sync + 2;
     wl.abort = sync + 3;
     wl.done = sync + 8;
+    wl.chunk0 = reinterpret_cast<int*>(ws + L.chunk0);
     return wl;
 }
 

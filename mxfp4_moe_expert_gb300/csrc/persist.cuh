@@ -434,6 +434,90 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Top-k + gates of one token's logits row, by one warp: lane l owns experts l, l + 32,
+// ...; each round takes the largest key (redux max), the lowest expert among equal keys
+// (redux min), and the winning lane moves to its next candidate.  For k <= 8 every lane
+// keeps its own 8 best (key desc, expert asc) sorted in registers; for larger k the
+// winning lane rescans its experts.  Lane j < k returns pick j and its gate (softmax
+// over the k selected logits).  kGlobal: the row is in global memory (read from L2).
+template <bool kGlobal>
+__device__ __forceinline__ void topk_warp(const float* row, int E, int k, int lane, uint32_t& mine, float& gate) {
+    auto ld = [&](int e) -> float { return kGlobal ? __ldcg(row + e) : row[e]; };
+    mine = 0u;
+    if (k <= 8) {
+        uint32_t kk[8], ee[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { kk[i] = 0u; ee[i] = 0xFFFFFFFFu; }
+#pragma unroll 4
+        for (int e = lane; e < E; e += 32) {
+            uint32_t ck = logit_key(ld(e)), ce = (uint32_t)e;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {   // keep the larger here, carry the smaller down
+                const bool gt = ck > kk[i];
+                const uint32_t tk = gt ? kk[i] : ck, te = gt ? ee[i] : ce;
+                kk[i] = gt ? ck : kk[i];
+                ee[i] = gt ? ce : ee[i];
+                ck = tk;
+                ce = te;
+            }
+        }
+        for (int j = 0; j < k; ++j) {
+            const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, kk[0]);
+            const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, kk[0] == kmax ? ee[0] : 0xFFFFFFFFu);
+            if (lane == j) mine = emin;
+            if (ee[0] == emin) {
+#pragma unroll
+                for (int i = 0; i < 7; ++i) { kk[i] = kk[i + 1]; ee[i] = ee[i + 1]; }
+                kk[7] = 0u;
+                ee[7] = 0xFFFFFFFFu;
+            }
+        }
+    } else {
+        uint32_t taken = 0u;
+        uint32_t bk = 0u;
+        uint32_t be = 0xFFFFFFFFu;
+        auto rescan = [&]() {
+            bk = 0u;
+            be = 0xFFFFFFFFu;
+            for (int i = 0, e = lane; e < E; ++i, e += 32) {
+                const uint32_t kk = ((taken >> i) & 1u) ? 0u : logit_key(ld(e));
+                if (kk > bk) { bk = kk; be = (uint32_t)e; }
+            }
+        };
+        rescan();
+        for (int j = 0; j < k; ++j) {
+            const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
+            const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, bk == kmax ? be : 0xFFFFFFFFu);
+            if (lane == j) mine = emin;
+            if ((int)(emin & 31u) == lane) {
+                taken |= 1u << (emin >> 5);
+                rescan();
+            }
+        }
+    }
+    float v = lane < k ? ld((int)mine) : 0.0f;
+    if (v != v) v = __int_as_float(0xFF800000);
+    const float m = __shfl_sync(0xFFFFFFFFu, v, 0);
+    const float ex = lane < k ? expf(v - m) : 0.0f;
+    const float den = warp_sum(ex);
+    gate = ex / den;
+}
+
+// Top-k + gates of every token of a larger block, one warp per token over the whole
+// grid, into the workspace (idx / gate).
+__device__ __noinline__ void topk_tokens(const PersistParams& p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int t = blockIdx.x * nw + warp; t < p.T; t += gridDim.x * nw) {
+        uint32_t mine;
+        float gate;
+        topk_warp<true>(p.rb.logits + (size_t)t * p.E, p.E, p.k, lane, mine, gate);
+        if (lane < p.k) {
+            p.rb.idx[t * p.k + lane] = (int)mine;
+            p.rb.gate[t * p.k + lane] = gate;
+        }
+    }
+}
+
 // Routing of a small verify block (T*k <= 64, T*E <= 8192) by every CTA into its own
 // shared memory: the layer's logits, top-k + gates, and the grouping as a routing
 // table for the expert phase and the combine.  Every CTA computes the same values.
@@ -466,73 +550,13 @@ __device__ __noinline__ void route_small(const PersistParams& p, int l, int* scr
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     sub(1);
-    // top-k + gates, one warp per token: lane l owns experts l, l + 32, ...; each
-    // round takes the largest key (redux max), the lowest expert among equal keys
-    // (redux min), and the winning lane moves to its next candidate.  For k <= 8
-    // every lane keeps its own 8 best (key desc, expert asc) sorted in registers;
-    // for larger k the winning lane rescans its experts.
     for (int t = warp; t < T; t += nw) {
-        const float* row = lg + (size_t)t * E;
-        uint32_t mine = 0u;
-        if (k <= 8) {
-            uint32_t kk[8], ee[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) { kk[i] = 0u; ee[i] = 0xFFFFFFFFu; }
-#pragma unroll 4
-            for (int e = lane; e < E; e += 32) {
-                uint32_t ck = logit_key(row[e]), ce = (uint32_t)e;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {   // keep the larger here, carry the smaller down
-                    const bool gt = ck > kk[i];
-                    const uint32_t tk = gt ? kk[i] : ck, te = gt ? ee[i] : ce;
-                    kk[i] = gt ? ck : kk[i];
-                    ee[i] = gt ? ce : ee[i];
-                    ck = tk;
-                    ce = te;
-                }
-            }
-            for (int j = 0; j < k; ++j) {
-                const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, kk[0]);
-                const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, kk[0] == kmax ? ee[0] : 0xFFFFFFFFu);
-                if (lane == j) mine = emin;
-                if (ee[0] == emin) {
-#pragma unroll
-                    for (int i = 0; i < 7; ++i) { kk[i] = kk[i + 1]; ee[i] = ee[i + 1]; }
-                    kk[7] = 0u;
-                    ee[7] = 0xFFFFFFFFu;
-                }
-            }
-        } else {
-            uint32_t taken = 0u;
-            uint32_t bk = 0u;
-            uint32_t be = 0xFFFFFFFFu;
-            auto rescan = [&]() {
-                bk = 0u;
-                be = 0xFFFFFFFFu;
-                for (int i = 0, e = lane; e < E; ++i, e += 32) {
-                    const uint32_t kk = ((taken >> i) & 1u) ? 0u : logit_key(row[e]);
-                    if (kk > bk) { bk = kk; be = (uint32_t)e; }
-                }
-            };
-            rescan();
-            for (int j = 0; j < k; ++j) {
-                const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
-                const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, bk == kmax ? be : 0xFFFFFFFFu);
-                if (lane == j) mine = emin;
-                if ((int)(emin & 31u) == lane) {
-                    taken |= 1u << (emin >> 5);
-                    rescan();
-                }
-            }
-        }
-        float v = lane < k ? row[mine] : 0.0f;
-        if (v != v) v = __int_as_float(0xFF800000);
-        const float m = __shfl_sync(0xFFFFFFFFu, v, 0);
-        const float ex = lane < k ? expf(v - m) : 0.0f;
-        const float den = warp_sum(ex);
+        uint32_t mine;
+        float gate;
+        topk_warp<false>(lg + (size_t)t * E, E, k, lane, mine, gate);
         if (lane < k) {
             rt->idx[t * k + lane] = (int)mine;
-            rt->gate[t * k + lane] = ex / den;
+            rt->gate[t * k + lane] = gate;
         }
     }
     __syncthreads();
@@ -751,9 +775,10 @@ __device__ __noinline__ void stack_init_unit(const PersistParams& p, int u, floa
 }
 
 
-// Routing of one layer by one block: logits from the slice partials (fixed order),
-// top-k + gates, grouping (counts, offsets, perm, active list) and the work list.
-// scratch: shared memory of at least (2 * E + 1 + 32 * E + 64) ints.
+// Grouping of a larger block by one CTA (after topk_tokens): counts, offsets, perm,
+// the routed-expert list and each routed expert's first chunk, published in the
+// workspace for the work-list builders (build_items_slice).
+// scratch: shared memory of at least (2 * E + 1 + 32 * E + 64 + 3 * E + T * k) ints.
 __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLayer& ly, int l, int* scratch) {
     const int T = p.T, E = p.E, k = p.k, H = p.H;
     const RouteBufs& rb = p.rb;
@@ -763,48 +788,7 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
         if (l == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[40 + i] = globaltimer_ns();
     };
     sub(0);
-    // (the logits were completed by the router units)
-    // ---- top-k + gates, one warp per token (logits of lane l: experts l, l+32, ...)
-    for (int t = warp; t < T; t += nw) {
-        const float* lrow = rb.logits + (size_t)t * E;
-        float lv[kMaxExperts / 32];
-#pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
-            const int e = lane + 32 * i;
-            float v = e < E ? __ldcg(lrow + e) : __int_as_float(0xFF800000);
-            if (v != v) v = __int_as_float(0xFF800000);
-            lv[i] = v;
-        }
-        float prev_v = __int_as_float(0x7F800000);
-        int prev_e = -1;
-        float my_sel = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            float bv = __int_as_float(0xFF800000);
-            int be = 0x7FFFFFFF;
-#pragma unroll
-            for (int i = 0; i < kMaxExperts / 32; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && route_before(prev_v, prev_e, lv[i], e) && route_before(lv[i], e, bv, be)) {
-                    bv = lv[i];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-                if (route_before(ov, oe, bv, be)) { bv = ov; be = oe; }
-            }
-            prev_v = bv;
-            prev_e = be;
-            if (lane == j) my_sel = bv;
-            if (lane == 0) rb.idx[t * k + j] = be;
-        }
-        const float m = __shfl_sync(0xFFFFFFFFu, my_sel, 0);
-        const float ex = lane < k ? expf(my_sel - m) : 0.0f;
-        const float den = warp_sum(ex);
-        if (lane < k) rb.gate[t * k + lane] = ex / den;
-    }
+    // (top-k and gates were written by topk_tokens)
     sub(1);
     int* cnt = scratch;                  // [E]
     int* flag = scratch + E;             // [E + 1]
@@ -869,62 +853,23 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
         __syncthreads();
     }
     sub(3);
-    // ---- work list: chunks of <= 8 pairs per routed expert.  The grouping is
-    // staged in shared memory first (the item records read it many times).
+    // ---- first chunk of each routed expert (chunks of <= 8 pairs) and the item counts
     const int n_active = misc[0];
     const int rbu = p.I / kTmaRows, rbd = H / kDownRows;
-    int* chunk0 = flag;                 // [n_active]: first chunk index of each routed expert
-    int* s_act = wcnt;                  // [n_active] expert ids
-    int* s_beg = wcnt + E;              // [n_active] first perm position
-    int* s_cnt = wcnt + 2 * E;          // [n_active] pairs
-    int* s_perm = wcnt + 3 * E;         // [T * k] pair id of each perm position
-    for (int a = threadIdx.x; a < n_active; a += blockDim.x) {
-        const int e = __ldcg(rb.active + 1 + a);
-        s_act[a] = e;
-        s_beg[a] = __ldcg(rb.offsets + e);
-        s_cnt[a] = __ldcg(rb.counts + e);
-    }
-    for (int i = threadIdx.x; i < T * k; i += blockDim.x) s_perm[i] = __ldcg(rb.perm + i);
+    int* chunk0 = flag;                 // [n_active + 1]
+    for (int a = threadIdx.x; a < n_active; a += blockDim.x)
+        chunk0[a] = (__ldcg(rb.counts + __ldcg(rb.active + 1 + a)) + kTmaTok - 1) / kTmaTok;
     __syncthreads();
     if (warp == 0) {
-        for (int a = lane; a < n_active; a += 32) {
-            chunk0[a] = (s_cnt[a] + kTmaTok - 1) / kTmaTok;
-        }
-        __syncwarp();
         const int total_chunks = warp_excl_scan(chunk0, n_active);
         if (lane == 0) {
-            misc[1] = total_chunks;
+            chunk0[n_active] = total_chunks;
             wl.n_items[0] = total_chunks * (rbu + rbd);
             wl.n_items[1] = total_chunks * rbu;
         }
     }
     __syncthreads();
-    const int total_chunks = misc[1];
-    const int n_gu = total_chunks * rbu;
-    for (int i = threadIdx.x; i < total_chunks * (rbu + rbd); i += blockDim.x) {
-        const bool down = i >= n_gu;
-        const int j = down ? i - n_gu : i;
-        const int nrb = down ? rbd : rbu;
-        int lo = 0, hi = n_active - 1;   // the routed expert whose items contain j
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (chunk0[mid] * nrb <= j) lo = mid; else hi = mid - 1;
-        }
-        const int nch = (s_cnt[lo] + kTmaTok - 1) / kTmaTok;
-        const int rr = j - chunk0[lo] * nrb, rbi = rr / nch, tc = rr % nch;   // row block major, chunk minor
-        const int chunk = chunk0[lo] + tc;
-        ItemRec r;
-        r.code = item_code(down ? kItemDown : kItemGateUp, rbi, tc, lo);
-        r.e = s_act[lo];
-        r.beg = s_beg[lo] + tc * kTmaTok;
-        r.ntok = min(kTmaTok, s_cnt[lo] - tc * kTmaTok);
-#pragma unroll
-        for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? s_perm[r.beg + q] : s_perm[r.beg + q] / k) : 0;
-        r.chunk = chunk;
-        r.pad[0] = nch;
-        r.pad[1] = r.pad[2] = 0;
-        wl.items[i] = r;
-    }
+    for (int a = threadIdx.x; a <= n_active; a += blockDim.x) wl.chunk0[a] = chunk0[a];
     sub(4);
     // ---- optional copies of the routing
     const int lg = p.layer_base + l;
@@ -934,6 +879,112 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
     if (p.dbg.counts) for (int i = threadIdx.x; i < E; i += blockDim.x) p.dbg.counts[(size_t)lg * E + i] = rb.counts[i];
     if (p.dbg.offsets)
         for (int i = threadIdx.x; i <= E; i += blockDim.x) p.dbg.offsets[(size_t)lg * (E + 1) + i] = rb.offsets[i];
+}
+
+// This CTA's share of the work list of a larger block (all CTAs, after the grouping is
+// published): items in the order of table_item (per routed expert, row block major,
+// chunk minor; gate/up items first).  scratch: 4 * (n_active + 1) ints of shared memory.
+__device__ __noinline__ void build_items_slice(const PersistParams& p, int* scratch) {
+    const RouteBufs& rb = p.rb;
+    const WorkList& wl = p.wl;
+    const int k = p.k;
+    const int n_active = __ldcg(rb.active);
+    int* s_c0 = scratch;                  // [n_active + 1]
+    int* s_act = s_c0 + n_active + 1;     // [n_active]
+    int* s_beg = s_act + n_active;
+    int* s_cnt = s_beg + n_active;
+    for (int a = threadIdx.x; a <= n_active; a += blockDim.x) {
+        s_c0[a] = __ldcg(wl.chunk0 + a);
+        if (a < n_active) {
+            const int e = __ldcg(rb.active + 1 + a);
+            s_act[a] = e;
+            s_beg[a] = __ldcg(rb.offsets + e);
+            s_cnt[a] = __ldcg(rb.counts + e);
+        }
+    }
+    __syncthreads();
+    const int rbu = p.I / kTmaRows, rbd = p.H / kDownRows;
+    const int total_chunks = s_c0[n_active];
+    const int n_gu = total_chunks * rbu, total = total_chunks * (rbu + rbd);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const bool down = i >= n_gu;
+        const int j = down ? i - n_gu : i;
+        const int nrb = down ? rbd : rbu;
+        int lo = 0, hi = n_active - 1;   // the routed expert whose items contain j
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_c0[mid] * nrb <= j) lo = mid; else hi = mid - 1;
+        }
+        const int nch = (s_cnt[lo] + kTmaTok - 1) / kTmaTok;
+        const int rr = j - s_c0[lo] * nrb, rbi = rr / nch, tc = rr % nch;   // row block major, chunk minor
+        ItemRec r;
+        r.code = item_code(down ? kItemDown : kItemGateUp, rbi, tc, lo);
+        r.e = s_act[lo];
+        r.beg = s_beg[lo] + tc * kTmaTok;
+        r.ntok = min(kTmaTok, s_cnt[lo] - tc * kTmaTok);
+        int pq[kTmaTok];
+#pragma unroll
+        for (int q = 0; q < kTmaTok; ++q) pq[q] = q < r.ntok ? __ldcg(rb.perm + r.beg + q) : 0;
+#pragma unroll
+        for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? pq[q] : pq[q] / k) : 0;
+        r.chunk = s_c0[lo] + tc;
+        r.pad[0] = nch;
+        r.pad[1] = r.pad[2] = 0;
+        wl.items[i] = r;
+    }
+}
+
+// y = sum_j g[t, j] * partial[t*k + j] (slot order; slots outside the shard skipped) for
+// a layer without a residual stack, over every thread of the grid, 4 columns per step.
+// dry: one step per thread of this CTA and nothing stored (brings the code into the caches).
+__device__ __noinline__ void combine_elems(const PersistParams& p, int l, const RouteTable* rt, bool dry = false) {
+    const int H4 = p.H / 4, k = p.k;
+    const int n = p.T * H4;
+    const bool store = !dry && l == p.L - 1 && p.write_y;
+    const int i0 = dry ? (int)threadIdx.x : blockIdx.x * blockDim.x + threadIdx.x;
+    const int step = dry ? n : gridDim.x * blockDim.x;
+    for (int i = i0; i < n; i += step) {
+        const int t = i / H4, c4 = i % H4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = 0; j0 < k; j0 += 8) {   // 8 slots' loads in flight, summed in slot order
+            float g[8];
+            float4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int j = j0 + q;
+                g[q] = 0.0f;
+                v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < k) {
+                    const int e = rt ? rt->idx[t * k + j] : __ldcg(p.rb.idx + t * k + j);
+                    if (e >= p.e_begin && e < p.e_end) {
+                        g[q] = rt ? rt->gate[t * k + j] : __ldcg(p.rb.gate + t * k + j);
+                        v[q] = __ldcg(reinterpret_cast<const float4*>(p.ta.partial + (size_t)(t * k + j) * p.H) + c4);
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (j0 + q < k && g[q] != 0.0f) {
+                    acc.x = fmaf(g[q], v[q].x, acc.x);
+                    acc.y = fmaf(g[q], v[q].y, acc.y);
+                    acc.z = fmaf(g[q], v[q].z, acc.z);
+                    acc.w = fmaf(g[q], v[q].w, acc.w);
+                }
+            }
+        }
+        if (store) {
+            const size_t o = (size_t)t * p.H + (size_t)c4 * 4;
+            if (p.y_bf16) {
+                __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 u;
+                u.x = *reinterpret_cast<uint32_t*>(&a);
+                u.y = *reinterpret_cast<uint32_t*>(&b);
+                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.y) + o) = u;
+            } else {
+                *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + o) = acc;
+            }
+        }
+    }
 }
 
 // The expert phase of one layer, compiled as its own function (its register
@@ -1009,7 +1060,8 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
             // code (results discarded; shared memory only) or, on every other such CTA, the
             // combine code (nothing stored), so that code is in L2 when the whole grid needs it
             if (((blockIdx.x - units) & 1) == 0 || l + 1 < p.L) route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
-            else combine_unit(p, blockIdx.x % cunits, l, red, nullptr, true);
+            else if (p.norm) combine_unit(p, blockIdx.x % cunits, l, red, nullptr, true);
+            else combine_elems(p, l, nullptr, true);
         }
         const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
         if (!grid_sync(p.bar, epoch, deadline, abort, status, withhold)) return;
@@ -1017,27 +1069,35 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         if (small) {
             route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
             stamp(3 + 4 * l);
-        } else if (blockIdx.x == 0) {
-            route_phase(p, ly, l, reinterpret_cast<int*>(xs));
-            __syncthreads();
-            stamp(3 + 4 * l);
-            if (threadIdx.x == 0) {
-                __threadfence();
-                atomicExch(p.route_flag, l + 1);
-            }
         } else {
-            int failed = 0;
-            if (threadIdx.x == 0) {
-                uint32_t spins = 0;
-                while (ld_acquire_gpu(p.route_flag) < l + 1) {
-                    if ((++spins & 63u) == 0 && (globaltimer_ns() > deadline || aborted(abort))) {
-                        failed = 1;
-                        if (atomicExch(abort, 1) == 0) raise_status(status, MOE_ERR_TIMEOUT, -2);
-                        break;
+            // larger blocks: top-k on every warp of the grid; grouping by CTA 0 while the
+            // others wait on a release flag; the work list built by every CTA
+            topk_tokens(p);
+            if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
+            if (blockIdx.x == 0) {
+                route_phase(p, ly, l, reinterpret_cast<int*>(xs));
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    atomicExch(p.route_flag, l + 1);
+                }
+            } else {
+                int failed = 0;
+                if (threadIdx.x == 0) {
+                    uint32_t spins = 0;
+                    while (ld_acquire_gpu(p.route_flag) < l + 1) {
+                        if ((++spins & 63u) == 0 && (globaltimer_ns() > deadline || aborted(abort))) {
+                            failed = 1;
+                            if (atomicExch(abort, 1) == 0) raise_status(status, MOE_ERR_TIMEOUT, -2);
+                            break;
+                        }
                     }
                 }
+                if (__syncthreads_or(failed)) return;
             }
-            if (__syncthreads_or(failed)) return;
+            build_items_slice(p, reinterpret_cast<int*>(xs));
+            if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
+            stamp(3 + 4 * l);
         }
         // the slots were written through the generic proxy; TMA writes them next
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1063,7 +1123,10 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         if (small && blockIdx.x == 0) publish_small(p, l, sm.rt);
         if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
         stamp(4 + 4 * l);
-        for (int u = blockIdx.x; u < cunits; u += gridDim.x) combine_unit(p, u, l, red, small ? sm.rt : nullptr);
+        if (p.norm)
+            for (int u = blockIdx.x; u < cunits; u += gridDim.x) combine_unit(p, u, l, red, small ? sm.rt : nullptr);
+        else
+            combine_elems(p, l, small ? sm.rt : nullptr);
         stamp(5 + 4 * l);
         if (l + 1 < p.L && !grid_sync(p.bar, epoch, deadline, abort, status)) return;
     }

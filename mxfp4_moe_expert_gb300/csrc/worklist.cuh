@@ -58,6 +58,7 @@ struct WorkList {
     int* queue;        // next item to claim (zero at the start of the phase)
     int* done;         // [chunks] gate/up items finished per chunk (zero at the start)
     int* abort;        // set when any wait times out
+    int* chunk0;       // [n_active + 1] first chunk of each routed expert, then the total (larger blocks)
 };
 
 // Item idx of the phase, from the routing table (rbu / rbd: row blocks of gate/up and down).
