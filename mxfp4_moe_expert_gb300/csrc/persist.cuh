@@ -172,26 +172,47 @@ __device__ __forceinline__ float inv_rms(const PersistParams& p, int t) {
     return 1.0f / sqrtf(tot / (float)p.H + p.eps);
 }
 
+// The block is routed by every CTA in its own shared memory (route_small) rather than
+// through the workspace (topk_tokens / route_phase / build_items_slice).
+__device__ __forceinline__ bool route_is_small(const PersistParams& p) {
+    return p.T * p.k <= kRtMaxPairs && p.T * p.E <= 8192;
+}
+
+// Router units process G groups of 8 tokens per pass: G = 1 for a single 8-token block
+// (the 16 warps split K); larger blocks G = 2 (1024-column slices) or 4 (narrower).
+__device__ __forceinline__ int router_groups(const PersistParams& p) {
+    return p.T > kPRouteTok ? (p.rslice >= 1024 ? 2 : 4) : 1;
+}
+// Shared-memory layout of a router unit (slot area): the staged input terms
+// [24 G rows][stride] at 0, the weight rows [32][stride] at router_wbase, then the
+// inverse RMS of the pass's tokens (32 floats).  stride = rslice * 2 + 16 bytes (rows
+// padded by 16 bytes: conflict-free ldmatrix).  The warps' sums [16][32][24] floats
+// (48 KB) reuse offset 0 after the MMAs.
+__device__ __forceinline__ uint32_t router_stride(const PersistParams& p) { return (uint32_t)p.rslice * 2 + 16; }
+__device__ __forceinline__ uint32_t router_wbase(const PersistParams& p) {
+    const uint32_t a = max(24u * router_groups(p) * router_stride(p), 16u * 768u * 4u);
+    return (a + 1023u) & ~1023u;
+}
+
 // Router-weight copies: the weight rows of one router unit (up to 32 experts x
-// rslice columns, bf16) land in shared memory (kRouterW bytes into the slot area,
-// rows padded by 16 bytes) through bulk copies completing on sm.rw, one row per lane
-// of the issuing warp.  State in shared memory (rstate): [0] copies issued (mbarrier
-// phases), [1] phases waited for, [2] / [3] unit / layer whose copies were issued
-// ahead of time (-1: none).
-constexpr int kRouterW = 65536;
+// rslice columns, bf16) land in shared memory (router_wbase into the slot area, rows
+// padded) through bulk copies completing on sm.rw, one row per lane of the issuing
+// warp.  State in shared memory (rstate): [0] copies issued (mbarrier phases), [1]
+// phases waited for, [2] / [3] unit / layer whose copies were issued ahead of time
+// (-1: none).
 __device__ __forceinline__ void router_issue(const PersistParams& p, const PersistLayer& ly, int u,
                                              const TcSmem& sm, int* rstate, int lane) {   // whole warp
     const int n_sl = p.H / p.rslice;
     const int eg = u / n_sl, sl = u % n_sl;
     const int ne = min(kPRouteExperts, p.E - eg * kPRouteExperts);
-    const uint32_t row = (uint32_t)p.rslice * 2, stride = row + 16;
+    const uint32_t row = (uint32_t)p.rslice * 2, stride = router_stride(p);
     if (lane == 0) {
         fence_proxy_async_shared();   // earlier generic accesses of the slot area come first
         mbar_arrive_expect_tx(sm.rw, row * ne);
     }
     __syncwarp();
     if (lane < ne)
-        bulk_load_stream(sm.slots + kRouterW + lane * stride,
+        bulk_load_stream(sm.slots + router_wbase(p) + lane * stride,
                          ly.router_w + (size_t)(eg * kPRouteExperts + lane) * p.H + sl * p.rslice, row, sm.rw,
                          l2_evict_first_policy());
     if (lane == 0) rstate[0] += 1;
@@ -211,30 +232,33 @@ __device__ __forceinline__ void split_bf16x3(float x, uint16_t& hi, uint16_t& mi
 }
 
 // Router unit u = (expert group g of 32, column slice s of p.rslice columns): partial
-// logits of the group over the slice for every token, 8 tokens at a time, on the
-// tensor cores: D [32 experts x 24] = W [32 x K] . X^T where the 24 columns of X are
-// the bf16 terms hi / mid / lo of the 8 tokens' inputs (fp32 accumulation; the
-// three terms carry the fp32 input to within 2^-24).  Warp w multiplies the K range
-// [w K/16, (w+1) K/16); the warps' results are summed in a fixed order.  The
-// weight rows come into shared memory by bulk copies (issued ahead of time where
-// possible); the slice of the layer input (x, or RMSNorm of the residual for a
-// stack) is staged as its three terms.  The unit that finishes a group last (a
-// counter per group) sums the group's slice partials in slice order and writes its
-// logits (+ bias): the result does not depend on which unit comes last.  Returns
-// false (every thread) when the weight copies time out.
+// logits of the group over the slice for every token, 8 G tokens per pass, on the
+// tensor cores: per 8-token group D [32 experts x 24] = W [32 x K] . X^T where the 24
+// columns of X are the bf16 terms hi / mid / lo of the 8 tokens' inputs (fp32
+// accumulation; the three terms carry the fp32 input to within 2^-24).  The 16 / G
+// warps of a group split K; their results are summed in a fixed order.  The weight
+// rows come into shared memory by bulk copies (issued ahead of time where possible);
+// the slice of the layer input (x, or RMSNorm of the residual for a stack) is staged
+// as its three terms.  The unit that finishes a group last (a counter per group) sums
+// the group's slice partials in slice order and writes its logits (+ bias): the result
+// does not depend on which unit comes last.  Returns false (every thread) when the
+// weight copies time out.
 __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLayer& ly, int l, int u,
                                          const TcSmem& sm, int* rstate, unsigned long long deadline) {
     const int H = p.H, E = p.E, T = p.T;
     const int n_sl = H / p.rslice;
     const int eg = u / n_sl, sl = u % n_sl;
     const int c0 = sl * p.rslice;
-    const int ncols = p.rslice;                  // 256, 512 or 1024
+    const int ncols = p.rslice;                          // 256, 512 or 1024
+    const int G = router_groups(p), TP = kPRouteTok * G;  // token groups / tokens per pass
+    const int wpg = 16 / G;                              // warps per token group (split K)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = warp / wpg, kp = warp % wpg;          // this warp's token group and K part
     const int ne = min(kPRouteExperts, E - eg * kPRouteExperts);
-    const uint32_t stride = (uint32_t)ncols * 2 + 16;   // bytes per staged row (x terms and weights)
-    uint8_t* xt = sm.slots;                              // [24][stride]: row 8 q + t = term q of token t
+    const uint32_t stride = router_stride(p), wbase = router_wbase(p);
+    uint8_t* xt = sm.slots;                              // [24 G][stride]: row 24 g + 8 q + t = term q of token t of group g
     float* red = reinterpret_cast<float*>(sm.slots);     // [16 warps][32 experts][24] after the MMAs
-    float* sinv = sm.red + 32;                           // [8]
+    float* sinv = reinterpret_cast<float*>(sm.slots + wbase + 32 * stride);   // [TP]
     int* flag = rstate + 4;
     auto rs = [&](int i) {   // router timestamps of CTA 0's first unit (profiling)
         if (u == 0 && l == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[48 + i] = globaltimer_ns();
@@ -251,27 +275,28 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
     }
     __syncthreads();
     const uint32_t parity = (uint32_t)(rstate[0] - 1) & 1u;
-    const uint32_t xs_a = smem_u32(xt), ws_a = smem_u32(sm.slots + kRouterW);
+    const uint32_t xs_a = smem_u32(xt), ws_a = smem_u32(sm.slots + wbase);
     bool have_w = false;
-    for (int t0 = 0; t0 < T; t0 += kPRouteTok) {
-        const int nt = min(kPRouteTok, T - t0);
-        if (t0 > 0) __syncthreads();   // the previous group's sums have been read
+    for (int t0 = 0; t0 < T; t0 += TP) {
+        const int nt = min(TP, T - t0);
+        if (t0 > 0) __syncthreads();   // the previous pass's sums have been read
         if (t0 == 0) rs(1);
-        if (p.norm && warp < nt) {
-            const float v = inv_rms(p, t0 + warp);
-            if (lane == 0) sinv[warp] = v;
-        }
+        if (p.norm)
+            for (int t = warp; t < nt; t += 16) {
+                const float v = inv_rms(p, t0 + t);
+                if (lane == 0) sinv[t] = v;
+            }
         __syncthreads();
-        // stage the three bf16 terms of the 8 tokens' inputs (tokens >= nt: zero)
+        // stage the three bf16 terms of the pass's inputs (tokens >= nt: zero)
         const int n4 = ncols / 4;
-        for (int i0 = threadIdx.x; i0 < kPRouteTok * n4; i0 += 4 * blockDim.x) {
+        for (int i0 = threadIdx.x; i0 < TP * n4; i0 += 4 * blockDim.x) {
             float4 v[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {   // loads first (in flight together), then the stores
                 const int i = i0 + j * blockDim.x;
                 const int t = i / n4, c = (i % n4) * 4;
                 v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i < kPRouteTok * n4 && t < nt) {
+                if (i < TP * n4 && t < nt) {
                     const size_t o = (size_t)(t0 + t) * H + c0 + c;
                     if (p.norm) {
                         const float4 r = __ldcg(reinterpret_cast<const float4*>(p.resid + o));
@@ -288,14 +313,14 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int i = i0 + j * blockDim.x;
-                if (i >= kPRouteTok * n4) continue;
+                if (i >= TP * n4) continue;
                 const int t = i / n4, c = (i % n4) * 4;
                 uint16_t h[4], m[4], lo[4];
                 split_bf16x3(v[j].x, h[0], m[0], lo[0]);
                 split_bf16x3(v[j].y, h[1], m[1], lo[1]);
                 split_bf16x3(v[j].z, h[2], m[2], lo[2]);
                 split_bf16x3(v[j].w, h[3], m[3], lo[3]);
-                uint8_t* base = xt + (size_t)t * stride + c * 2;
+                uint8_t* base = xt + (size_t)(24 * (t >> 3) + (t & 7)) * stride + c * 2;
                 *reinterpret_cast<uint2*>(base) =
                     make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
                 *reinterpret_cast<uint2*>(base + 8 * stride) =
@@ -316,7 +341,7 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
             __syncthreads();
         }
         if (t0 == 0) rs(2);
-        // this warp's K range: ncols / 16 columns = 1, 2 or 4 steps of 16
+        // this warp's K part: ncols / wpg columns in steps of 16, against its group's 24 rows
         float d[2][3][4];
 #pragma unroll
         for (int a = 0; a < 2; ++a)
@@ -324,19 +349,20 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
             for (int b = 0; b < 3; ++b)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) d[a][b][q] = 0.0f;
-        const int kw = ncols / 16;
+        const int kw = ncols / wpg;
+        const uint32_t xg = xs_a + (uint32_t)(24 * gw) * stride;
         for (int ks = 0; ks < kw; ks += 16) {
-            const int k0 = warp * kw + ks;
+            const int k0 = kp * kw + ks;
             uint32_t af[2][4];
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
                 ldmatrix_x4(ws_a + (uint32_t)(mt * 16 + (lane & 15)) * stride + (uint32_t)(k0 + (lane >> 4) * 8) * 2,
                             af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
             uint32_t b0, b1, b2, b3, b4, b5;
-            ldmatrix_x4(xs_a + (uint32_t)((lane >> 4) * 8 + (lane & 7)) * stride +
+            ldmatrix_x4(xg + (uint32_t)((lane >> 4) * 8 + (lane & 7)) * stride +
                             (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2,
                         b0, b1, b2, b3);
-            ldmatrix_x2(xs_a + (uint32_t)(16 + (lane & 7)) * stride + (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2, b4,
+            ldmatrix_x2(xg + (uint32_t)(16 + (lane & 7)) * stride + (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2, b4,
                         b5);
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
@@ -358,19 +384,21 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
                 r[(e + 8) * 24 + n + 1] = d[mt][nb][3];
             }
         __syncthreads();
-        if (threadIdx.x < kPRouteExperts * kPRouteTok) {   // (expert, token): warps in order, then the terms
-            const int e = threadIdx.x >> 3, t = threadIdx.x & 7;
+        for (int i = threadIdx.x; i < kPRouteExperts * TP; i += blockDim.x) {   // (expert, token): K parts in order, then the terms
+            const int e = i / TP, t = i % TP, g = t >> 3, t8 = t & 7;
             float sh = 0.0f, sm_ = 0.0f, slo = 0.0f;
-            for (int w = 0; w < 16; ++w) {
-                const float* r = red + w * 768 + e * 24;
-                sh += r[t];
-                sm_ += r[8 + t];
-                slo += r[16 + t];
+            for (int w = 0; w < wpg; ++w) {
+                const float* r = red + (g * wpg + w) * 768 + e * 24;
+                sh += r[t8];
+                sm_ += r[8 + t8];
+                slo += r[16 + t8];
             }
             if (t < nt && e < ne) p.rpart[((size_t)sl * T + t0 + t) * E + eg * kPRouteExperts + e] = sh + (sm_ + slo);
         }
         if (t0 == 0) rs(3);
     }
+    rs(4);
+    if (!route_is_small(p)) return true;   // larger blocks: the grid sums the partials (logits_reduce)
     // the last unit of the group turns the slice partials into logits
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -397,8 +425,26 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
             p.rb.logits[(size_t)t * E + e] = z + (ly.router_b ? __ldg(ly.router_b + e) : 0.0f);
         }
     }
-    rs(4);
     return true;
+}
+
+// Logits of a larger block from the router slice partials (slices in order) + bias,
+// over every thread of the grid.
+__device__ __noinline__ void logits_reduce(const PersistParams& p, const PersistLayer& ly) {
+    const int TE = p.T * p.E, n_sl = p.H / p.rslice;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < TE; i += gridDim.x * blockDim.x) {
+        const float* src = p.rpart + i;
+        float z = 0.0f;
+        for (int s0 = 0; s0 < n_sl; s0 += 8) {   // 8 loads in flight, summed in slice order
+            float a[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) a[q] = s0 + q < n_sl ? __ldcg(src + (size_t)(s0 + q) * TE) : 0.0f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (s0 + q < n_sl) z += a[q];
+        }
+        p.rb.logits[i] = z + (ly.router_b ? __ldg(ly.router_b + i % p.E) : 0.0f);
+    }
 }
 
 // The expert operand of the layer input: task i = (token t, MX block kb) splits the
@@ -1019,7 +1065,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     int* rstate = reinterpret_cast<int*>(sm.red + 40);     // router-weight copy state (router_issue)
     const int units = ((p.E + kPRouteExperts - 1) / kPRouteExperts) * (p.H / p.rslice);
     const int cunits = p.T * (p.H / kCombineChunk);
-    const bool small = p.T * p.k <= kRtMaxPairs && p.T * p.E <= 8192;
+    const bool small = route_is_small(p);
     auto stamp = [&](int i) {
         if (blockIdx.x == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[i] = globaltimer_ns();
     };
@@ -1072,6 +1118,8 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         } else {
             // larger blocks: top-k on every warp of the grid; grouping by CTA 0 while the
             // others wait on a release flag; the work list built by every CTA
+            logits_reduce(p, ly);
+            if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
             topk_tokens(p);
             if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
             if (blockIdx.x == 0) {
