@@ -178,7 +178,7 @@ def run_gpu(args):
     inputs, layers = device_layers(wl, device=dev)
     flags = pkg.MOE_FLAG_NORM if wl.norm else 0
     persistent = args.path == "persistent" and moe_tma(wl)
-    if args.path == "multi":
+    if args.path in ("multi", "graph"):
         flags |= pkg.MOE_FLAG_MULTI_KERNEL
     moe = pkg.MoeLayers(hidden=wl.H, inter=wl.I, num_experts=wl.E, top_k=wl.k, max_tokens=wl.T, layers=layers,
                         flags=flags, rms_eps=wl.rms_eps)
@@ -197,6 +197,20 @@ def run_gpu(args):
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     clean = torch.ones(64 << 20, dtype=torch.float32, device=dev) if args.flush == "clean" else None
+    graph = None
+    if args.path == "graph":
+        # the one-launch-per-phase forward captured once and replayed: the launch gaps of
+        # the per-operator model without the persistent kernel (SURVEY next-step 2)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                moe.forward(x, y, wsp, side.cuda_stream)
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            moe.forward(x, y, wsp, side.cuda_stream)
+        torch.cuda.synchronize()
 
     def flush_l2(i):
         # "write": a 256 MiB write (L2 is 129 MB) leaves L2 full of dirty lines of the
@@ -207,8 +221,14 @@ def run_gpu(args):
         flush.fill_(i & 0xFF)
         if clean is not None:
             clean.sum()
+    def step(dbg_i=None):
+        if graph is not None:
+            graph.replay()
+        else:
+            moe.forward(x, y, wsp, st, dbg_i)
+
     for _ in range(max(args.warmup, 3)):
-        moe.forward(x, y, wsp, st)
+        step()
     torch.cuda.synchronize()
     L = wl.layers
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -217,7 +237,7 @@ def run_gpu(args):
         for e in evs:
             e.record(stream)
     # per-kernel events force the one-launch-per-phase path: only used there
-    kdbg = [None if persistent else moe.expert_timing(evs) for evs in kev]
+    kdbg = [None if (persistent or graph is not None) else moe.expert_timing(evs) for evs in kev]
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -231,7 +251,7 @@ def run_gpu(args):
     for i in range(args.steps):
         flush_l2(i)
         ev[i][0].record(stream)
-        moe.forward(x, y, wsp, st, kdbg[i])
+        step(kdbg[i])
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
@@ -241,7 +261,7 @@ def run_gpu(args):
     if sampler:
         sampler.__exit__()
     per = [a.elapsed_time(b) * 1e3 for a, b in ev]   # us per forward
-    if persistent:   # the whole forward is one kernel (plus two tiny memsets)
+    if persistent or graph is not None:   # the whole forward is one kernel / one graph
         kern = [v / L for v in per]
     else:
         kern = [sum(evs[2 * l].elapsed_time(evs[2 * l + 1]) for l in range(L)) * 1e3 / L for evs in kev]
@@ -284,10 +304,13 @@ def run_gpu(args):
     gbs = alg_bytes / (us * 1e-6) / 1e9
     # algorithmic bytes of the timed kernel per layer: the persistent kernel moves all
     # of the layer's bytes; the separate expert kernel the routed experts' nibbles and scales
-    kern_bytes = alg_bytes / wl.layers if persistent else sum(n_active) * wl.expert_bytes / wl.layers
+    kern_bytes = alg_bytes / wl.layers if (persistent or graph is not None) else \
+        sum(n_active) * wl.expert_bytes / wl.layers
     kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
     if persistent:
         launches_per_step = -(-wl.layers // 8)
+    elif graph is not None:
+        launches_per_step = (1 if wl.norm else 0) + 6 * wl.layers   # replayed inside one graph
     elif moe_tma(wl):
         launches_per_step = (1 if wl.norm else 0) + 6 * wl.layers
     else:
@@ -299,7 +322,8 @@ def run_gpu(args):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (MXFP4 weights)",
         "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "layers": wl.layers, "path": "persistent" if persistent else args.path, "routed_experts": n_active, "algorithmic_bytes": alg_bytes,
+                   "layers": wl.layers, "path": "persistent" if persistent else args.path,
+                   "routed_experts": n_active, "algorithmic_bytes": alg_bytes,
                    "l2": FLUSH_DESC[args.flush],
                    "parallelism": f"replicas{ws}"},
         "hbm_gbs": round(gbs, 1),
@@ -307,7 +331,9 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(kern_gbs / peak, 4),
                      "traffic": measured_traffic(wl.name) if persistent else None, "peak_kind": peak_kind,
-                     "kernel": "persistent forward kernel" if persistent else "expert FFN kernel",
+                     "kernel": "persistent forward kernel" if persistent else
+                               "whole forward (CUDA graph of the per-phase launches)" if graph is not None else
+                               "expert FFN kernel",
                      "kernel_us_per_layer": round(kern_us, 2),
                      "kernel_bytes_per_layer": int(kern_bytes)},
         "forward_hbm_frac": round(gbs / peak, 4),
@@ -353,6 +379,65 @@ def measured_traffic(workload):
     if not e or e.get("source_sha256") != kernel_sources_sha256():
         return None
     return int(e["dram_read_bytes"] + e["dram_write_bytes"])
+
+
+def run_sweep(args):
+    """Multi-stream sweep (SURVEY next-step 3): the 384-expert layer over verify blocks of
+    8 x {1, 4, 16, 32, 64} tokens (streams of 8 positions), persistent forward, clean L2
+    before each step.  Prints one JSON line with a row per block size."""
+    import torch
+
+    import mxfp4_moe_expert_gb300 as pkg
+    from mxfp4_moe_expert_gb300.synth import WORKLOADS, make_inputs
+    from mxfp4_moe_expert_gb300.workload import device_layers, touched_bytes
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if not os.path.exists(pkg.LIB_PATH):
+        from mxfp4_moe_expert_gb300 import build
+        build.build()
+    base = WORKLOADS["large"]
+    sizes = [8, 32, 128, 256, 512]
+    _, layers = device_layers(base, device=dev)
+    moe = pkg.MoeLayers(hidden=base.H, inter=base.I, num_experts=base.E, top_k=base.k, max_tokens=max(sizes),
+                        layers=layers)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st = stream.cuda_stream
+    peak, peak_kind = _peaks()
+    rows = []
+    for T in sizes:
+        wl = base.scaled(T=T, name=f"large_T{T}")
+        x = make_inputs(wl).x.to(dev)
+        y = torch.empty((T, base.H), dtype=torch.float32, device=dev)
+        wsp = moe.new_workspace(T, dev)
+        bufs, dbg = moe.debug_buffers(T, dev)
+        moe.forward(x, y, wsp, st, dbg, check=True)
+        counts = bufs["expert_counts"].cpu()
+        alg = touched_bytes(wl, [counts[0]])
+        chunks = int(((counts[0] + 7) // 8).sum())
+        for _ in range(max(args.warmup, 3)):
+            moe.forward(x, y, wsp, st)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            clean.sum()
+            ev[i][0].record(stream)
+            moe.forward(x, y, wsp, st)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert pkg.moe_mxfp4_check(moe.handle, wsp.data_ptr(), st) == 0
+        us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
+        rows.append({"tokens": T, "streams": T // 8, "us_per_forward": round(us, 2),
+                     "us_per_stream": round(us / (T // 8), 2), "routed_experts": int((counts[0] > 0).sum()),
+                     "chunks": chunks, "algorithmic_bytes": alg, "hbm_gbs": round(alg / (us * 1e-6) / 1e9, 1),
+                     "frac_of_peak": round(alg / (us * 1e-6) / 1e9 / peak, 4)})
+        del wsp, bufs
+    print(json.dumps({"metric": "multi_stream_sweep", "unit": "us", "config": {"workload": "large", "H": base.H,
+                      "I": base.I, "E": base.E, "k": base.k, "path": "persistent",
+                      "l2": FLUSH_DESC["clean"]}, "peak_gbs": peak, "peak_kind": peak_kind,
+                      "steps": args.steps, "rows": rows}))
 
 
 def moe_tma(wl):
@@ -404,13 +489,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush", default="clean", choices=["write", "clean", "none"],
                     help="L2 state before each timed step (see FLUSH_DESC)")
-    ap.add_argument("--path", default="persistent", choices=["persistent", "multi"],
-                    help="one cooperative launch per forward, or one launch per phase")
+    ap.add_argument("--path", default="persistent", choices=["persistent", "multi", "graph"],
+                    help="one cooperative launch per forward, one launch per phase, or those launches "
+                         "captured in a CUDA graph")
+    ap.add_argument("--sweep", action="store_true", help="multi-stream sweep of the 384-expert layer")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_gpu(args)
 
