@@ -357,11 +357,16 @@ FLUSH_DESC = {
 }
 
 
+# the sources the persistent forward kernel is compiled from
+KERNEL_SOURCES = ("common.cuh", "expert_tc.cuh", "moe_mxfp4.cu", "persist.cuh", "ptx.cuh", "route.cuh",
+                  "worklist.cuh")
+
+
 def kernel_sources_sha256():
-    """Hash of the library's kernel sources (the same recipe as profiles/dram_traffic.json)."""
+    """Hash of the persistent kernel's sources (the same recipe as profiles/dram_traffic.json)."""
     import hashlib
     csrc = os.path.join(ROOT, "mxfp4_moe_expert_gb300", "csrc")
-    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)) + [os.path.join(ROOT, "include", "moe_mxfp4.h")]
+    files = [os.path.join(csrc, f) for f in KERNEL_SOURCES]
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())

@@ -207,6 +207,27 @@ int moe_mxfp4_forward_static(moe_mxfp4_handle* h, const void* x_dev, int32_t num
 int moe_mxfp4_quantize(const float* w_dev, int64_t rows, int64_t cols, uint8_t* q_dev, uint8_t* s_dev,
                        void* stream);
 
+/* Acceptance of speculative verify blocks ("MiMo 把 1T 模型推到每秒千 token", DFlash
+ * section: one target forward scores the drafted positions of a block; the longest
+ * prefix the target agrees with is kept and the rest discarded).  Block position i of
+ * stream s holds input token tokens[s, i] (position 0: the last committed token,
+ * positions 1..B-1: drafted tokens), and the target's logits at position i predict
+ * the token of position i + 1.  The call computes, per stream:
+ *   target[s, i]   = argmax_v logits[s, i, v]   (lowest index among equal maxima; NaN
+ *                    ranks as -inf)
+ *   a              = the largest m <= B-1 with tokens[s, i] == target[s, i-1], i = 1..m
+ *   accepted[s]    = a + 1   (tokens this verify yields: the a accepted drafts and the
+ *                    target's own next token; the pages' "acceptance length")
+ *   next_token[s]  = target[s, a]
+ * logits_dev: fp32 [S, B, V]; tokens_dev: int32 [S, B]; target_dev: int32 [S, B]
+ * (output, also the working array); accepted_dev, next_token_dev: int32 [S] (outputs;
+ * next_token_dev may be NULL).  Device pointers, caller-owned; asynchronous on stream.
+ * MOE_ERR_INVALID_ARG for S < 0, B < 1, V < 1, S*B or V above 2^31 - 1, or a NULL
+ * required pointer; S = 0 is a no-op. */
+int moe_mxfp4_accept(const float* logits_dev, const int32_t* tokens_dev, int32_t num_streams, int32_t block,
+                     int64_t vocab, int32_t* target_dev, int32_t* accepted_dev, int32_t* next_token_dev,
+                     void* stream);
+
 #ifdef __cplusplus
 }
 #endif

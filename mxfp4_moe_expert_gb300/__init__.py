@@ -39,6 +39,7 @@ EXPORTED = (
     "moe_mxfp4_status_string",
     "moe_mxfp4_quantize",
     "moe_mxfp4_forward_static",
+    "moe_mxfp4_accept",
 )
 
 MOE_MXFP4_STATIC_WORKSPACE_BYTES = 16 << 20
@@ -119,6 +120,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_mxfp4_quantize.restype = ctypes.c_int
     lib.moe_mxfp4_forward_static.argtypes = [P, P, ctypes.c_int32, P, P]
     lib.moe_mxfp4_forward_static.restype = ctypes.c_int
+    lib.moe_mxfp4_accept.argtypes = [P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, P, P, P, P]
+    lib.moe_mxfp4_accept.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -186,6 +189,26 @@ def moe_mxfp4_forward_static(handle, x_ptr, num_tokens, y_ptr, stream_ptr) -> in
 
 
 # ----------------------------------------------------------------------------- torch convenience
+
+
+def moe_mxfp4_accept(logits_ptr, tokens_ptr, num_streams, block, vocab, target_ptr, accepted_ptr,
+                     next_token_ptr, stream_ptr) -> int:
+    return load_library().moe_mxfp4_accept(logits_ptr, tokens_ptr, num_streams, block, vocab, target_ptr,
+                                           accepted_ptr, next_token_ptr, stream_ptr)
+
+
+def accept(logits, tokens, stream=None):
+    """logits: fp32 CUDA [S, B, V]; tokens: int32 CUDA [S, B].  Returns (target [S, B],
+    accepted [S], next_token [S]) as int32 CUDA tensors (see moe_mxfp4_accept)."""
+    import torch
+    S, B, V = logits.shape
+    target = torch.empty((S, B), dtype=torch.int32, device=logits.device)
+    acc = torch.empty((S,), dtype=torch.int32, device=logits.device)
+    nxt = torch.empty((S,), dtype=torch.int32, device=logits.device)
+    st = stream if stream is not None else torch.cuda.current_stream(logits.device).cuda_stream
+    _check(moe_mxfp4_accept(logits.data_ptr(), tokens.data_ptr(), S, B, V, target.data_ptr(), acc.data_ptr(),
+                            nxt.data_ptr(), st), "moe_mxfp4_accept")
+    return target, acc, nxt
 
 
 def quantize(w, q=None, s=None, stream=None):

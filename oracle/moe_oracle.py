@@ -282,3 +282,25 @@ def topk_margin(logits_row: np.ndarray, k: int) -> float:
     """Smallest gap between adjacent logits among the top-(k+1) of one token."""
     top = np.sort(np.asarray(logits_row, np.float64))[::-1][: min(k + 1, logits_row.size)]
     return float(np.min(top[:-1] - top[1:])) if top.size > 1 else math.inf
+
+
+def accept_block(logits: np.ndarray, tokens: np.ndarray) -> dict:
+    """Acceptance of verify blocks ("MiMo 把 1T 模型推到每秒千 token", DFlash section: the
+    target scores all drafted positions in one forward and the longest agreeing prefix
+    is kept).  logits [S, B, V] (position i predicts the token of position i + 1);
+    tokens [S, B] (position 0 the last committed token, 1..B-1 the drafts).  Per
+    stream: target = greedy token per position (first maximum; NaN as -inf); a = number
+    of leading drafts equal to the target's prediction for their position; accepted =
+    a + 1 tokens yielded; next_token = target[a]."""
+    lg = np.where(np.isnan(logits), -np.inf, logits)
+    target = np.argmax(lg, axis=2).astype(np.int32)   # numpy returns the first maximum
+    S, B = tokens.shape
+    accepted = np.zeros(S, dtype=np.int32)
+    nxt = np.zeros(S, dtype=np.int32)
+    for s in range(S):
+        a = 0
+        while a + 1 < B and tokens[s, a + 1] == target[s, a]:
+            a += 1
+        accepted[s] = a + 1
+        nxt[s] = target[s, a]
+    return dict(target=target, accepted=accepted, next_token=nxt)

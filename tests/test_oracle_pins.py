@@ -364,3 +364,42 @@ def test_bandwidth_bound_reproduces_page_numbers():
 def test_verify_tokens_per_s():
     # one verify forward per 6.30 accepted tokens: 1 ms per verify -> 6300 tokens/s
     assert O.verify_tokens_per_s(1e-3) == pytest.approx(6300.0)
+
+
+# ----------------------------------------------------------------------------- verify acceptance
+
+
+def _one_hot_logits(targets, V, base=0.0):
+    """Logits whose greedy token at each position is the given one (value 1 vs base)."""
+    S, B = targets.shape
+    lg = np.full((S, B, V), base)
+    for s in range(S):
+        for i in range(B):
+            lg[s, i, targets[s, i]] = 1.0
+    return lg
+
+
+def test_accept_block_hand_cases():
+    # position i's logits predict the token of position i + 1 (DFlash verify, page 3)
+    targets = np.array([[2, 3, 1, 4],     # drafts 2, 3 agree, draft 0 at position 3 does not
+                        [1, 1, 2, 0],     # every draft agrees: 3 accepted + the target's token
+                        [4, 0, 0, 0]])    # the first draft disagrees
+    tokens = np.array([[9, 2, 3, 0],
+                       [7, 1, 1, 2],
+                       [5, 3, 0, 0]])
+    r = O.accept_block(_one_hot_logits(targets, 5), tokens)
+    assert r["target"].tolist() == targets.tolist()
+    assert r["accepted"].tolist() == [3, 4, 1]       # tokens yielded per verify
+    assert r["next_token"].tolist() == [1, 0, 4]     # the target's token after the accepted drafts
+
+
+def test_accept_block_ties_nan_and_block_of_one():
+    lg = np.zeros((1, 3, 6))
+    lg[0, 0, [1, 4]] = 2.0               # tie: the lower token wins
+    lg[0, 1, :] = [0.5, np.nan, 0.1, 0.7, -1.0, 0.7]   # NaN never wins; tie 3 / 5 -> 3
+    lg[0, 2, 2] = 1.0
+    r = O.accept_block(lg, np.array([[0, 1, 3]]))
+    assert r["target"].tolist() == [[1, 3, 2]]
+    assert r["accepted"].tolist() == [3] and r["next_token"].tolist() == [2]
+    one = O.accept_block(np.zeros((2, 1, 4)), np.zeros((2, 1), dtype=np.int64))
+    assert one["accepted"].tolist() == [1, 1] and one["next_token"].tolist() == [0, 0]
