@@ -82,6 +82,8 @@ constexpr int kItemRing = 8;
 //   xb4: [T][H/256][8 term rows][128 B] packed E2M1, 128-byte swizzle (row phase = term)
 //   xsf: [T][H/256][8 term rows][8 blocks]
 //   hb4: [chunk][I/256][64 rows (8p + j)][128 B] swizzled; hsf: [chunk][I/256][64 rows][8 blocks]
+//   xc4 / xcs (larger blocks): the layer input gathered per chunk in the layout of hb4 / hsf
+//   ([chunk][H/256][64 rows][128 B] / [..][8 blocks]), so a gate/up stage needs one copy
 __host__ __device__ constexpr size_t xb4_bytes(int T, int H) { return (size_t)T * (H / 2) * kTcTerms; }
 __host__ __device__ constexpr size_t xsf_bytes(int T, int H) { return (size_t)T * (H / 32) * kTcTerms; }
 __host__ __device__ constexpr size_t hb4_chunk_bytes(int I) { return (size_t)(I / 2) * kTcRowsA; }
@@ -103,6 +105,8 @@ struct TcArgs {
     int H, I, T, layer;
     const uint8_t* xb4;
     const uint8_t* xsf;
+    const uint8_t* xc4;       // per-chunk gathered input operand, or NULL (per-token copies)
+    const uint8_t* xcs;
     uint8_t* hb4;
     uint8_t* hsf;
     float* partial;           // [pairs (t*k + j), H]
@@ -363,6 +367,9 @@ __device__ __forceinline__ void tc_prefetch_stage(const TcItemGeom& g, int st) {
     }
 }
 
+// kGathered: the gate/up items' activation operand comes per chunk (xc4 / xcs, one copy
+// per stage and one per scale group) instead of per token and pair.
+template <bool kGathered>
 __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, const TcSmem& s_in,
                                         TcRoleState& rs_in, unsigned long long deadline) {
     // arguments and counters in registers (the caller's copies live in local memory)
@@ -454,7 +461,8 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                     break;
                 }
                 uint8_t* sdst = s.scales + se * kTcScaleEntry;
-                const uint32_t sfa_bytes = gu ? (uint32_t)ntok * spb * 64 : (uint32_t)spb * 512;
+                const bool per_tok = gu && !kGathered;
+                const uint32_t sfa_bytes = per_tok ? (uint32_t)ntok * spb * 64 : (uint32_t)spb * 512;
                 mbar_arrive_expect_tx(&s.sfull[se], 2u * (uint32_t)sw * kTmaRows + sfa_bytes);
                 if (cur.pad[0] > 1) {
                     tma_load_2d(sdst, ms0, st * 8, r0, &s.sfull[se]);
@@ -463,7 +471,10 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                     tma_load_2d_stream(sdst, ms0, st * 8, r0, &s.sfull[se], pol);
                     tma_load_2d_stream(sdst + kScaleBox1, ms1, st * 8, r1, &s.sfull[se], pol);
                 }
-                if (gu) {   // per pair: the group's stages of its token (contiguous in xsf)
+                if (gu && kGathered) {   // the chunk's gathered scales of the group's stages
+                    bulk_load(sdst + kScaleSfa, a.xcs + ((size_t)cur.chunk * (H / kTcKS) + st) * 512,
+                              (uint32_t)spb * 512, &s.sfull[se]);
+                } else if (gu) {   // per pair: the group's stages of its token (contiguous in xsf)
                     for (int p = 0; p < ntok; ++p)
                         bulk_load(sdst + kScaleSfa + p * spb * 64,
                                   a.xsf + ((size_t)cur.tok[p] * (H / kTcKS) + st) * 64, (uint32_t)spb * 64,
@@ -478,7 +489,7 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
             if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
             s.meta[slot] = TcSlotMeta{kind, st, nk, (int)rs.sc - 1, (st % spb) * 8, sw, st % spb == spb - 1 ? 1 : 0, spb};
             mbar_arrive(&s.claim[slot]);   // the scale-factor warps may prepare this slot now
-            const uint32_t abytes = gu ? (uint32_t)ntok * 1024 : 8192u;
+            const uint32_t abytes = (gu && !kGathered) ? (uint32_t)ntok * 1024 : 8192u;
             mbar_arrive_expect_tx(&s.full[slot], 2 * 16384 + abytes);
             tc_trace(a, 0, rs.it);
             ++rs.it;   // this slot now has copies in flight
@@ -498,7 +509,9 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                     for (; pf_next <= ps - nk && pf_next < gn.nk; ++pf_next) tc_prefetch_stage(gn, pf_next);
                 }
             }
-            if (gu) {
+            if (gu && kGathered) {
+                bulk_load(dst + kSlotA, a.xc4 + ((size_t)cur.chunk * (H / kTcKS) + st) * 8192, 8192, &s.full[slot]);
+            } else if (gu) {
                 for (int p = 0; p < ntok; ++p) {
                     const size_t ts = (size_t)cur.tok[p] * (H / kTcKS) + st;
                     bulk_load(dst + kSlotA + p * 1024, a.xb4 + ts * 1024, 1024, &s.full[slot]);
@@ -597,6 +610,9 @@ __device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint
 // A slot is prepared as soon as the producer has claimed it (its previous MMAs are
 // done): the scales come from the scale ring, not from the slot's own copies, so
 // the work overlaps the stage's weight copies.
+// kGathered: as for tc_produce (the activation scales of gate/up stages are laid out per
+// stage, like the down items', instead of per pair).
+template <bool kGathered>
 __device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, uint32_t tmem, TcRoleState& rs_in, int w,
                                    int lane, unsigned long long deadline) {
     const TcArgs a = a_in;
@@ -638,8 +654,9 @@ __device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, uint3
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int row = 32 * c + lane;
-                    const int off = m.kind == kItemGateUp ? (row >> 3) * m.pad * 64 + sg * 64 + (row & 7) * 8
-                                                          : sg * 512 + row * 8;
+                    const int off = (!kGathered && m.kind == kItemGateUp)
+                                        ? (row >> 3) * m.pad * 64 + sg * 64 + (row & 7) * 8
+                                        : sg * 512 + row * 8;
                     v[c] = *reinterpret_cast<const uint2*>(ent + kScaleSfa + off);
                 }
                 b0 = 0;
@@ -821,15 +838,16 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
 }
 
 // One expert phase, dispatched by warp role; every thread of the block calls it.
+template <bool kGathered>
 __device__ __forceinline__ void tc_phase(const TcMaps& maps, const TcArgs& a, const TcSmem& s, uint32_t tmem,
                                          TcRoleState& rs, unsigned long long deadline) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == kTcWarpProducer) {
-        if (lane == 0) tc_produce(maps, a, s, rs, deadline);
+        if (lane == 0) tc_produce<kGathered>(maps, a, s, rs, deadline);
     } else if (warp == kTcWarpMma) {
         if (lane == 0) tc_mma(a, s, tmem, rs, deadline);
     } else if (tc_is_sf_warp(warp)) {
-        tc_sf(a, s, tmem, rs, (warp == 6) ? 0 : (warp == 7) ? 1 : 2, lane, deadline);
+        tc_sf<kGathered>(a, s, tmem, rs, (warp == 6) ? 0 : (warp == 7) ? 1 : 2, lane, deadline);
     } else if (tc_is_epi_warp(warp)) {
         tc_epilogue(a, s, tmem, rs, warp, lane, deadline);
     }
@@ -882,7 +900,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) expert_tc_kernel(const __grid_c
         prefetch_tensormap(&maps.down_s);
     }
     TcRoleState rs{0u, 0u, 0u, 0u};
-    tc_phase(maps, args, s, tmem, rs, deadline);
+    tc_phase<false>(maps, args, s, tmem, rs, deadline);
     tc_teardown(s, tmem, args.timeout_ns);
 }
 

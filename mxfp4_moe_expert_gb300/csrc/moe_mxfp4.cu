@@ -38,7 +38,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // Byte offsets of the workspace sections for T tokens.
 struct WsLayout {
     size_t status, xstage, ystage, act, resid, logits, idx, gate, counts, offsets, perm, active, hbuf, partial;
-    size_t xb4, xsf, ss, tickets, hb4, hsf, items, sync, rpart, chunk0, total;
+    size_t xb4, xsf, ss, tickets, hb4, hsf, items, sync, rpart, chunk0, xc4, xcs, total;
 };
 
 // Upper bound of the chunks of one layer: every routed expert contributes
@@ -89,6 +89,10 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     L.sync = take((8 + chunks) * 4);   // n_items[2], queue, abort, ..., done[chunks]
     L.rpart = take((size_t)(H / 256 + 1) * T * E * 4);   // router partials per column slice (>= 256 columns)
     L.chunk0 = take((E + 1) * 4);
+    // larger blocks (routed through the workspace): the input operand gathered per chunk
+    const bool gathered = !((size_t)T * k <= 64 && (size_t)T * E <= 8192);
+    L.xc4 = take(gathered ? chunks * (H / 256) * 8192 : 0);
+    L.xcs = take(gathered ? chunks * (H / 256) * 512 : 0);
     L.total = o;
     return L;
 }
@@ -328,6 +332,10 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     p.ta.items = p.wl.items;
     p.ta.n_items = p.wl.n_items;
     p.wl.abort = reinterpret_cast<int*>(ws + L.status + 24);   // cleared with the status words
+    if (!((size_t)T * k <= 64 && (size_t)T * E <= 8192)) {   // larger blocks: gathered input operand
+        p.ta.xc4 = reinterpret_cast<uint8_t*>(ws + L.xc4);
+        p.ta.xcs = reinterpret_cast<uint8_t*>(ws + L.xcs);
+    }
     p.ta.abort = p.wl.abort;
     if (c.flags & MOE_FLAG_TRACE) p.ta.trace = reinterpret_cast<unsigned long long*>(ws + L.status + 4096);
     const int chunks = (int)max_chunks(c, T);
@@ -373,7 +381,9 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
                         cudaMemsetAsync(ws + L.tickets, 0, tickets_bytes(c, T), st) != cudaSuccess))
             return MOE_ERR_CUDA;
         void* kargs[] = {&p};
-        if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(moe::persist_kernel), dim3(h->persist_grid),
+        const void* kern = p.ta.xc4 ? reinterpret_cast<const void*>(moe::persist_kernel<true>)
+                                    : reinterpret_cast<const void*>(moe::persist_kernel<false>);
+        if (cudaLaunchCooperativeKernel(kern, dim3(h->persist_grid),
                                         dim3(moe::kTcThreads), kargs, moe::kTcSmemBytes, st) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
@@ -444,12 +454,15 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
                                            (int)(std::min<size_t>((size_t)c.max_tokens * c.top_k, 512u * moe::kTmaTok) *
                                                  sizeof(int))) != cudaSuccess)
             h->tma = false;
-        if (h->tma && cudaFuncSetAttribute(moe::persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (h->tma &&
+            cudaFuncSetAttribute(moe::persist_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 moe::kTcSmemBytes) == cudaSuccess &&
+            cudaFuncSetAttribute(moe::persist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            moe::kTcSmemBytes) == cudaSuccess) {
             int per_sm = 0;
             int coop = 0;
             cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-            if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe::persist_kernel, moe::kTcThreads,
+            if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe::persist_kernel<false>, moe::kTcThreads,
                                                                       moe::kTcSmemBytes) == cudaSuccess &&
                 per_sm >= 1)
                 h->persist_grid = prop.multiProcessorCount;

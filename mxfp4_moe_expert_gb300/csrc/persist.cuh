@@ -980,6 +980,40 @@ __device__ __noinline__ void build_items_slice(const PersistParams& p, int* scra
     }
 }
 
+// The layer input's expert operand gathered per chunk (larger blocks, every CTA, after
+// the grouping is published): unit = (chunk, 256-wide stage), one warp per unit; pair
+// slot p of the chunk gets its token's 8 term rows (1 KB) and their scales (64 B).
+// scratch: the routing arrays staged by build_items_slice.
+__device__ __noinline__ void gather_chunk_operand(const PersistParams& p, const int* scratch) {
+    const int n_active = __ldcg(p.rb.active);
+    const int* s_c0 = scratch;
+    const int* s_beg = scratch + n_active + 1 + n_active;
+    const int* s_cnt = s_beg + n_active;
+    const int nst = p.H / kTcKS, total_chunks = s_c0[n_active];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int u = blockIdx.x * nw + warp; u < total_chunks * nst; u += gridDim.x * nw) {
+        const int c = u / nst, st = u % nst;
+        int lo = 0, hi = n_active - 1;   // the routed expert of chunk c
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_c0[mid] <= c) lo = mid; else hi = mid - 1;
+        }
+        const int tc = c - s_c0[lo], beg = s_beg[lo] + tc * kTmaTok, ntok = min(kTmaTok, s_cnt[lo] - tc * kTmaTok);
+        uint8_t* dst = const_cast<uint8_t*>(p.ta.xc4) + ((size_t)c * nst + st) * 8192;   // workspace memory
+        uint8_t* dsf = const_cast<uint8_t*>(p.ta.xcs) + ((size_t)c * nst + st) * 512;
+        for (int q = 0; q < ntok; ++q) {
+            const int t = __ldcg(p.rb.perm + beg + q) / p.k;
+            const int4* src = reinterpret_cast<const int4*>(p.xb4 + ((size_t)t * nst + st) * 1024);
+            int4* d = reinterpret_cast<int4*>(dst + q * 1024);
+            d[lane] = __ldcg(src + lane);
+            d[lane + 32] = __ldcg(src + lane + 32);
+            if (lane < 4)
+                reinterpret_cast<int4*>(dsf + q * 64)[lane] =
+                    __ldcg(reinterpret_cast<const int4*>(p.xsf + ((size_t)t * nst + st) * 64) + lane);
+        }
+    }
+}
+
 // y = sum_j g[t, j] * partial[t*k + j] (slot order; slots outside the shard skipped) for
 // a layer without a residual stack, over every thread of the grid, 4 columns per step.
 // dry: one step per thread of this CTA and nothing stored (brings the code into the caches).
@@ -1035,6 +1069,7 @@ __device__ __noinline__ void combine_elems(const PersistParams& p, int l, const 
 
 // The expert phase of one layer, compiled as its own function (its register
 // allocation does not carry the rest of the persistent kernel's live state).
+template <bool kGathered>
 __device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMaps* maps, uint8_t* smem_raw,
                                                   uint32_t tmem, TcRoleState* rs, unsigned long long deadline) {
     const TcSmem s = tc_smem(smem_raw);
@@ -1048,11 +1083,14 @@ __device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMap
         prefetch_tensormap(&maps->down_s);
     }
     TcRoleState r = *rs;
-    tc_phase(*maps, args, s, tmem, r, deadline);
+    tc_phase<kGathered>(*maps, args, s, tmem, r, deadline);
     *rs = r;
 }
 
 // All layers of one launch; returns early (in every thread of the block) on a timeout / abort.
+// kLarge: the block is routed through the workspace (route_is_small(p) is false), with
+// the input operand gathered per chunk; the host launches the matching instantiation.
+template <bool kLarge>
 __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* smem_raw, uint32_t tmem,
                                             unsigned long long deadline) {
     const TcSmem sm = tc_smem(smem_raw);
@@ -1065,7 +1103,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     int* rstate = reinterpret_cast<int*>(sm.red + 40);     // router-weight copy state (router_issue)
     const int units = ((p.E + kPRouteExperts - 1) / kPRouteExperts) * (p.H / p.rslice);
     const int cunits = p.T * (p.H / kCombineChunk);
-    const bool small = route_is_small(p);
+    constexpr bool small = !kLarge;
     auto stamp = [&](int i) {
         if (blockIdx.x == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[i] = globaltimer_ns();
     };
@@ -1144,6 +1182,8 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
                 if (__syncthreads_or(failed)) return;
             }
             build_items_slice(p, reinterpret_cast<int*>(xs));
+            gather_chunk_operand(p, reinterpret_cast<const int*>(xs));
+            fence_proxy_async_global();   // read next by the expert phase's bulk copies
             if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
             stamp(3 + 4 * l);
         }
@@ -1156,7 +1196,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         ta.done = p.dones + (size_t)l * p.chunk_stride;
         ta.rt = small ? sm.rt : nullptr;
         if (l != 0 || p.layer_base != 0) ta.trace = nullptr;
-        persist_expert_phase(ta, &ly.maps, smem_raw, tmem, &rs, deadline);
+        persist_expert_phase<kLarge>(ta, &ly.maps, smem_raw, tmem, &rs, deadline);
         if (l + 1 < p.L && blockIdx.x < units) {   // the next layer's first router unit, ahead of time
             fence_proxy_async_shared();
             __syncthreads();
@@ -1180,12 +1220,13 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     }
 }
 
+template <bool kLarge>
 __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_constant__ PersistParams p) {
     extern __shared__ uint8_t smem_raw[];
     const TcSmem sm = tc_smem(smem_raw);
     const uint32_t tmem = tc_setup(sm);
     const unsigned long long deadline = globaltimer_ns() + p.ta.timeout_ns;
-    persist_layers(p, smem_raw, tmem, deadline);
+    persist_layers<kLarge>(p, smem_raw, tmem, deadline);
     __syncthreads();
     if (threadIdx.x == 0 && p.tstamp && blockIdx.x < 256)   // when each CTA finished (profiling)
         p.tstamp[56 + blockIdx.x] = globaltimer_ns();
