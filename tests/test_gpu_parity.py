@@ -130,6 +130,8 @@ def test_layer_parity_full_oracle(wl):
 @pytest.mark.parametrize("wl", [
     Workload("stack_small", T=6, H=512, I=256, E=12, k=3, layers=4, norm=True, seed=0x5EED0104),
     Workload("stack_tma", T=7, H=1024, I=512, E=12, k=3, layers=3, norm=True, seed=0x5EED0115),
+    # 96 pairs: routed through the workspace, input operand gathered per chunk, residual stack
+    Workload("stack_tma_large_block", T=24, H=1024, I=512, E=12, k=4, layers=2, norm=True, seed=0x5EED0117),
 ], ids=lambda w: w.name)
 def test_stack_parity_small(wl):
     inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
