@@ -22,6 +22,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -48,10 +49,10 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, path: str = ""):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(), f"clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -200,7 +201,7 @@ def run_gpu(args):
     graph = None
     if args.path == "graph":
         # the one-launch-per-phase forward captured once and replayed: the launch gaps of
-        # the per-operator model without the persistent kernel (SURVEY next-step 2)
+        # the per-operator model without the persistent kernel
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         with torch.cuda.stream(side):
@@ -242,7 +243,7 @@ def run_gpu(args):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(local, args.clocks_csv) if rank == 0 else None
     if sampler:
         sampler.__enter__()
         time.sleep(0.1)
@@ -276,9 +277,16 @@ def run_gpu(args):
         ts = wsp[64:64 + 8 * nst].cpu().view(torch.int64).tolist()
         names = ["staging"] + [f"l{l}_{n}" for l in range(min(L, 8)) for n in ("router", "route", "experts", "combine")]
         phases = {n: round((ts[i + 1] - ts[i]) / 1e3, 2) for i, n in enumerate(names)}
-        sub = wsp[64 + 8 * 40:64 + 8 * 52].cpu().view(torch.int64).tolist()   # routing / router sub-steps, layer 0
-        phases["l0_route_steps"] = [round((sub[i + 1] - sub[i]) / 1e3, 2) for i in range(4)]
-        phases["l0_router_unit0"] = [round((sub[8 + i + 1] - sub[8 + i]) / 1e3, 2) for i in range(3)]
+        sub = wsp[64 + 8 * 34:64 + 8 * 55].cpu().view(torch.int64).tolist()   # routing / router sub-steps, layer 0
+        phases["l0_route_steps"] = [round((sub[6 + i + 1] - sub[6 + i]) / 1e3, 2) for i in range(4)]
+        phases["l0_router_unit0"] = [round((sub[14 + i + 1] - sub[14 + i]) / 1e3, 2) for i in range(4)]
+        # CTA 0: its router units, the operand split, the wait at the barrier
+        phases["l0_router_cta0"] = [round((sub[19] - ts[1]) / 1e3, 2), round((sub[20] - sub[19]) / 1e3, 2),
+                                    round((ts[2] - sub[20]) / 1e3, 2)]
+        if wl.T * wl.k > 64 or wl.T * wl.E > 8192:   # routed through the workspace: logits sum, top-k,
+            # grouping (CTA 0), work list, operand gather (from the router phase's end)
+            marks = [ts[2]] + sub[0:5]
+            phases["l0_large_route_steps"] = [round((marks[i + 1] - marks[i]) / 1e3, 2) for i in range(5)]
     if ws > 1:
         t = torch.tensor([us], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -337,6 +345,7 @@ def run_gpu(args):
                      "kernel_us_per_layer": round(kern_us, 2),
                      "kernel_bytes_per_layer": int(kern_bytes)},
         "forward_hbm_frac": round(gbs / peak, 4),
+        "dist_us_per_layer": _percentiles([v / wl.layers for v in per]),
         "phases_us": phases,
         "e2e": {"value": round(e2e_us / wl.layers, 2), "unit": "us", "h2d_bytes_per_step": wl.T * wl.H * 2,
                 "d2h_bytes_per_step": wl.T * wl.H * 4},
@@ -386,8 +395,15 @@ def measured_traffic(workload):
     return int(e["dram_read_bytes"] + e["dram_write_bytes"])
 
 
+def _percentiles(v):
+    """Median, 10th and 90th percentile (nearest rank) of the per-step times."""
+    q = sorted(v)
+    pick = lambda f: q[min(len(q) - 1, max(0, int(round(f * (len(q) - 1)))))]
+    return {"median": round(statistics.median(q), 2), "p10": round(pick(0.1), 2), "p90": round(pick(0.9), 2)}
+
+
 def run_sweep(args):
-    """Multi-stream sweep (SURVEY next-step 3): the 384-expert layer over verify blocks of
+    """Multi-stream sweep: the 384-expert layer over verify blocks of
     8 x {1, 4, 16, 32, 64} tokens (streams of 8 positions), persistent forward, clean L2
     before each step.  Prints one JSON line with a row per block size."""
     import torch
@@ -492,6 +508,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-experts", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default="", help="keep the nvidia-smi clock samples of the timed region here")
     ap.add_argument("--flush", default="clean", choices=["write", "clean", "none"],
                     help="L2 state before each timed step (see FLUSH_DESC)")
     ap.add_argument("--path", default="persistent", choices=["persistent", "multi", "graph"],

@@ -139,9 +139,13 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
                      moe_mxfp4_handle** out);
 
 /* Bytes of device workspace a forward over num_tokens tokens needs.  The first 512
- * bytes hold the status words; in a persistent forward, bytes 64..335 receive CTA 0's
- * %globaltimer (uint64 ns) at the end of each phase (start, input staging, and per
- * layer l: router 2+4l, routing 3+4l, experts 4+4l, combine 5+4l), for profiling, and
+ * bytes hold the status words; in a persistent forward, bytes 64..511 receive CTA 0's
+ * %globaltimer (uint64 ns) at the end of each phase (entry i at 64 + 8 i: start,
+ * input staging, and per layer l < 8: router 2+4l, routing 3+4l, experts 4+4l, combine
+ * 5+4l; for the first layer also the routing sub-steps at 34..38 (blocks routed through
+ * the workspace) or 40..44, the steps of router unit 0 at 48..52 (unit 1 when the block
+ * has several token blocks), the end of CTA 0's router units at 53 and of its operand
+ * split at 54), for profiling, and
  * bytes 512..2559 receive each CTA's %globaltimer when it finished (CTA i at 512 + 8 i).
  * With MOE_FLAG_TRACE, bytes 4096..16383 receive the first layer's expert-phase
  * timestamps of CTA 0 as 6 arrays of 256 uint64 (ns, ring stage or item i < 256):
@@ -159,8 +163,12 @@ int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens
 
 /* The same forward on HOST buffers: copies x_host (bf16 [T, H]) into the
  * workspace, runs the forward, copies y back to y_host (fp32 or bf16 [T, H])
- * and synchronises the stream.  Pinned host memory makes the copies
- * asynchronous.  Returns the device status (as moe_mxfp4_check). */
+ * and synchronises the stream once (the status words are copied behind y on the
+ * same stream into a 64-byte pinned buffer that the handle allocates on first use
+ * and frees in moe_mxfp4_destroy).  Pinned host memory makes the copies of x and y
+ * asynchronous.  Calls on one handle from several threads are serialised from the
+ * status copy on.  Returns the device status (as moe_mxfp4_check), or MOE_ERR_CUDA
+ * when a copy, the pinned allocation or the synchronisation fails. */
 int moe_mxfp4_forward_host(moe_mxfp4_handle* h, const void* x_host, int32_t num_tokens, void* y_host,
                            void* workspace_dev, size_t workspace_bytes, void* stream);
 
@@ -168,7 +176,8 @@ int moe_mxfp4_forward_host(moe_mxfp4_handle* h, const void* x_host, int32_t num_
  * forward that used this workspace (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_BAD_SCALE). */
 int moe_mxfp4_check(moe_mxfp4_handle* h, const void* workspace_dev, void* stream);
 
-/* Frees the handle (host memory only).  NULL is ignored. */
+/* Frees the handle (its host memory, including the pinned status buffer of
+ * moe_mxfp4_forward_host).  NULL is ignored. */
 void moe_mxfp4_destroy(moe_mxfp4_handle* h);
 
 /* Static description of a status code. */

@@ -258,15 +258,25 @@ __device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, 
 // zero (or below 2^-120) gives zero codes and scale byte 0.  Returns the codes (term
 // j in bits 4j..4j+3) and, in sb0 / sb1, the scale bytes of terms 0-3 / 4-7 (term j
 // in byte j % 4, the same in every lane).
+// kRedux: the block max by one redux.sync (faster where many independent splits are in
+// flight; the shuffle tree is faster inside the expert epilogue).  Both give the same max.
+template <bool kRedux = false>
 __device__ __forceinline__ uint32_t split_e2m1_terms(float v, uint32_t& sb0, uint32_t& sb1) {
     uint32_t codes = 0;
     sb0 = sb1 = 0;
     float r = v;
 #pragma unroll
     for (int j = 0; j < kTcTerms; ++j) {
-        float m = fabsf(r);
+        // max |r| over the block, NaNs ignored (as fmaxf does); the bits of non-negative
+        // floats order like unsigned integers, which lets redux.sync take the max
+        float m;
+        if (kRedux) {
+            m = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, r != r ? 0u : __float_as_uint(fabsf(r))));
+        } else {
+            m = fabsf(r);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        }
         const uint32_t eb = __float_as_uint(m) >> 23;   // biased exponent of max|r| (m >= 0)
         if (eb >= 8u && eb < 255u) {
             // X = 2^(e-2) with e = eb - 127 puts max|r| / X in [4, 8); halve the ratio when it exceeds 6

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -26,6 +27,9 @@ struct moe_mxfp4_handle {
     int device = 0;
     int sm_count = 0;
     int e_begin = 0, e_end = 0;
+    std::mutex host_mu;                // serialises moe_mxfp4_forward_host on this handle
+    int* status_host = nullptr;        // pinned copy of the status words for moe_mxfp4_forward_host
+    ~moe_mxfp4_handle() { if (status_host) cudaFreeHost(status_host); }
 };
 
 namespace {
@@ -332,7 +336,8 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     p.ta.items = p.wl.items;
     p.ta.n_items = p.wl.n_items;
     p.wl.abort = reinterpret_cast<int*>(ws + L.status + 24);   // cleared with the status words
-    if (!((size_t)T * k <= 64 && (size_t)T * E <= 8192)) {   // larger blocks: gathered input operand
+    const bool small_block = (size_t)T * k <= 64 && (size_t)T * E <= 8192;   // routed in shared memory
+    if (!small_block) {   // larger blocks: gathered input operand
         p.ta.xc4 = reinterpret_cast<uint8_t*>(ws + L.xc4);
         p.ta.xcs = reinterpret_cast<uint8_t*>(ws + L.xcs);
     }
@@ -343,12 +348,34 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     p.queues = reinterpret_cast<int*>(ws + L.tickets);
     p.dones = p.queues + moe::kMaxPersistLayers;
     p.rcnt = p.dones + (size_t)moe::kMaxPersistLayers * chunks;
-    // router unit width: the widest slice that still gives every other SM a unit
+    // router units.  Blocks routed in shared memory: one token block, and the widest slice
+    // that still gives every other SM a unit.  Larger blocks: the slice width and token
+    // block with the fewest passes on the busiest CTA (ceil(units / grid) rounds of
+    // ceil(rtok / tokens per pass) passes); ties go to the wider slice, then to fewer units.
+    const int egroups = (E + moe::kPRouteExperts - 1) / moe::kPRouteExperts;
     p.rslice = 256;
+    p.rtok = T;
     for (int w = 1024; w >= 512; w /= 2) {
-        if (H % w == 0 && ((E + moe::kPRouteExperts - 1) / moe::kPRouteExperts) * (H / w) >= h->persist_grid / 2) {
+        if (H % w == 0 && egroups * (H / w) >= h->persist_grid / 2) {
             p.rslice = w;
             break;
+        }
+    }
+    if (!small_block) {
+        long best = -1, best_units = 0;
+        for (int w = 1024; w >= 256; w /= 2) {
+            if (H % w) continue;
+            const int tp = moe::kPRouteTok * (w >= 1024 ? 2 : 4);   // tokens per pass (router_groups)
+            for (int rt = tp; rt < T + tp; rt += tp) {
+                const long units = (long)egroups * (H / w) * ((T + rt - 1) / rt);
+                const long cost = ((units + h->persist_grid - 1) / h->persist_grid) * ((rt + tp - 1) / tp);
+                if (best < 0 || cost < best || (cost == best && w == p.rslice && units < best_units)) {
+                    best = cost;
+                    best_units = units;
+                    p.rslice = w;
+                    p.rtok = rt;
+                }
+            }
         }
     }
     p.bar = reinterpret_cast<unsigned*>(ws + L.status + 16);
@@ -525,7 +552,17 @@ int moe_mxfp4_forward_host(moe_mxfp4_handle* h, const void* x_host, int32_t num_
                                     stream, nullptr);
     if (r != MOE_OK) return r;
     if (cudaMemcpyAsync(y_host, ws + L.ystage, yb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
-    return moe_mxfp4_check(h, workspace_dev, stream);
+    // the status words ride on the stream behind y, so one synchronisation covers both
+    std::lock_guard<std::mutex> lock(h->host_mu);
+    if (!h->status_host && cudaHostAlloc(reinterpret_cast<void**>(&h->status_host), 64, cudaHostAllocPortable) !=
+                               cudaSuccess) {
+        h->status_host = nullptr;
+        return MOE_ERR_CUDA;
+    }
+    if (cudaMemcpyAsync(h->status_host, workspace_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    return h->status_host[0];
 }
 
 int moe_mxfp4_check(moe_mxfp4_handle* h, const void* workspace_dev, void* stream) {
@@ -546,7 +583,6 @@ void moe_mxfp4_destroy(moe_mxfp4_handle* h) { delete h; }
 // workspace lives in this file-scope array, one per GPU that loads the library.
 // Host code must not use the array's name as a pointer (on the host it only
 // stands for the symbol); its device address is looked up once per device.
-#include <mutex>
 
 namespace {
 static __device__ __align__(256) unsigned char g_static_workspace[MOE_MXFP4_STATIC_WORKSPACE_BYTES];

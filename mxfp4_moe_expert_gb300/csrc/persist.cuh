@@ -69,6 +69,7 @@ struct PersistParams {
     float* ss;         // [T, H / 256] sums of squares of the residual per column block
     float* rpart;      // [H / rslice, T, E] router slice partials
     int rslice;        // columns per router unit (256, 512 or 1024; divides H)
+    int rtok;          // tokens per router unit (T for blocks routed in shared memory; else a multiple of 8 G)
     int* rcnt;         // [kMaxPersistLayers, 32] finished router units per expert group (zeroed per launch)
     unsigned long long* tstamp;   // CTA 0's %globaltimer at phase ends (or NULL)
     TcArgs ta;         // expert phase: operands, partial, status, timeout (per-layer fields set per layer)
@@ -189,6 +190,27 @@ __device__ __forceinline__ int router_groups(const PersistParams& p) {
 // padded by 16 bytes: conflict-free ldmatrix).  The warps' sums [16][32][24] floats
 // (48 KB) reuse offset 0 after the MMAs.
 __device__ __forceinline__ uint32_t router_stride(const PersistParams& p) { return (uint32_t)p.rslice * 2 + 16; }
+// Router units: (weight slice r = (expert group eg of 32, column slice sl), token block tb),
+// u = r * token blocks + tb with r = eg * slices + sl: the token blocks of one weight
+// slice are adjacent.
+__device__ __forceinline__ int router_egroups(const PersistParams& p) { return (p.E + kPRouteExperts - 1) / kPRouteExperts; }
+__device__ __forceinline__ int router_tblocks(const PersistParams& p) { return (p.T + p.rtok - 1) / p.rtok; }
+__device__ __forceinline__ int router_units(const PersistParams& p) {
+    return router_egroups(p) * (p.H / p.rslice) * router_tblocks(p);
+}
+// This CTA's router units, first / end / step: blocks routed in shared memory take units
+// b, b + grid, ... (one token block each); larger blocks (kContiguous) a contiguous range,
+// so that consecutive units of a CTA mostly share their weight slice (kept in shared memory).
+template <bool kContiguous>
+__device__ __forceinline__ int router_first(int units) {
+    return kContiguous ? (int)((long long)units * blockIdx.x / gridDim.x) : (int)blockIdx.x;
+}
+template <bool kContiguous>
+__device__ __forceinline__ int router_end(int units) {
+    return kContiguous ? (int)((long long)units * (blockIdx.x + 1) / gridDim.x) : units;
+}
+template <bool kContiguous>
+__device__ __forceinline__ int router_step() { return kContiguous ? 1 : (int)gridDim.x; }
 __device__ __forceinline__ uint32_t router_wbase(const PersistParams& p) {
     const uint32_t a = max(24u * router_groups(p) * router_stride(p), 16u * 768u * 4u);
     return (a + 1023u) & ~1023u;
@@ -203,7 +225,8 @@ __device__ __forceinline__ uint32_t router_wbase(const PersistParams& p) {
 __device__ __forceinline__ void router_issue(const PersistParams& p, const PersistLayer& ly, int u,
                                              const TcSmem& sm, int* rstate, int lane) {   // whole warp
     const int n_sl = p.H / p.rslice;
-    const int eg = u / n_sl, sl = u % n_sl;
+    const int r = u / router_tblocks(p);   // the token block does not change the weights
+    const int eg = r / n_sl, sl = r % n_sl;
     const int ne = min(kPRouteExperts, p.E - eg * kPRouteExperts);
     const uint32_t row = (uint32_t)p.rslice * 2, stride = router_stride(p);
     if (lane == 0) {
@@ -231,8 +254,9 @@ __device__ __forceinline__ void split_bf16x3(float x, uint16_t& hi, uint16_t& mi
     lo = __bfloat16_as_ushort(l);
 }
 
-// Router unit u = (expert group g of 32, column slice s of p.rslice columns): partial
-// logits of the group over the slice for every token, 8 G tokens per pass, on the
+// Router unit u = (token block of p.rtok tokens, expert group g of 32, column slice s of
+// p.rslice columns): partial logits of the group over the slice for the block's tokens,
+// 8 G tokens per pass, on the
 // tensor cores: per 8-token group D [32 experts x 24] = W [32 x K] . X^T where the 24
 // columns of X are the bf16 terms hi / mid / lo of the 8 tokens' inputs (fp32
 // accumulation; the three terms carry the fp32 input to within 2^-24).  The 16 / G
@@ -247,7 +271,9 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
                                          const TcSmem& sm, int* rstate, unsigned long long deadline) {
     const int H = p.H, E = p.E, T = p.T;
     const int n_sl = H / p.rslice;
-    const int eg = u / n_sl, sl = u % n_sl;
+    const int n_tb = router_tblocks(p);
+    const int r = u / n_tb, eg = r / n_sl, sl = r % n_sl;
+    const int tbeg = (u % n_tb) * p.rtok, tend = min(T, tbeg + p.rtok);   // this unit's tokens
     const int c0 = sl * p.rslice;
     const int ncols = p.rslice;                          // 256, 512 or 1024
     const int G = router_groups(p), TP = kPRouteTok * G;  // token groups / tokens per pass
@@ -260,27 +286,32 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
     float* red = reinterpret_cast<float*>(sm.slots);     // [16 warps][32 experts][24] after the MMAs
     float* sinv = reinterpret_cast<float*>(sm.slots + wbase + 32 * stride);   // [TP]
     int* flag = rstate + 4;
-    auto rs = [&](int i) {   // router timestamps of CTA 0's first unit (profiling)
-        if (u == 0 && l == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[48 + i] = globaltimer_ns();
+    auto rs = [&](int i) {   // router timestamps of unit 0, or 1 with token blocks (CTA 0's second unit; profiling)
+        if (u == (n_tb > 1 ? 1 : 0) && l == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[48 + i] = globaltimer_ns();
     };
     rs(0);
     fence_proxy_async_shared();
     __syncthreads();   // earlier users of the slot area are done
     if (warp == 0) {
         const bool pre = rstate[2] == u && rstate[3] == l;
+        // the previous unit's weights are this unit's (same slice and layer, all landed)
+        const bool resident = !pre && rstate[5] == r && rstate[6] == l && rstate[0] == rstate[1];
         __syncwarp();
-        if (!pre) router_issue(p, ly, u, sm, rstate, lane);
+        if (!pre && !resident) router_issue(p, ly, u, sm, rstate, lane);
         __syncwarp();
-        if (lane == 0) rstate[2] = rstate[3] = -1;
+        if (lane == 0) {
+            rstate[2] = rstate[3] = -1;
+            rstate[7] = resident;
+        }
     }
     __syncthreads();
     const uint32_t parity = (uint32_t)(rstate[0] - 1) & 1u;
     const uint32_t xs_a = smem_u32(xt), ws_a = smem_u32(sm.slots + wbase);
-    bool have_w = false;
-    for (int t0 = 0; t0 < T; t0 += TP) {
-        const int nt = min(TP, T - t0);
-        if (t0 > 0) __syncthreads();   // the previous pass's sums have been read
-        if (t0 == 0) rs(1);
+    bool have_w = rstate[7] != 0;
+    for (int t0 = tbeg; t0 < tend; t0 += TP) {
+        const int nt = min(TP, tend - t0);
+        if (t0 > tbeg) __syncthreads();   // the previous pass's sums have been read
+        if (t0 == tbeg) rs(1);
         if (p.norm)
             for (int t = warp; t < nt; t += 16) {
                 const float v = inv_rms(p, t0 + t);
@@ -289,10 +320,11 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
         __syncthreads();
         // stage the three bf16 terms of the pass's inputs (tokens >= nt: zero)
         const int n4 = ncols / 4;
-        for (int i0 = threadIdx.x; i0 < TP * n4; i0 += 4 * blockDim.x) {
-            float4 v[4];
+        constexpr int kLd = 4;   // items per thread per round (loads in flight together)
+        for (int i0 = threadIdx.x; i0 < TP * n4; i0 += kLd * blockDim.x) {
+            float4 v[kLd];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {   // loads first (in flight together), then the stores
+            for (int j = 0; j < kLd; ++j) {   // loads first (in flight together), then the stores
                 const int i = i0 + j * blockDim.x;
                 const int t = i / n4, c = (i % n4) * 4;
                 v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -311,7 +343,7 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kLd; ++j) {
                 const int i = i0 + j * blockDim.x;
                 if (i >= TP * n4) continue;
                 const int t = i / n4, c = (i % n4) * 4;
@@ -335,12 +367,16 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
                 if (threadIdx.x == 0 && atomicExch(p.wl.abort, 1) == 0) raise_status(p.ta.status, MOE_ERR_TIMEOUT, -3);
                 return false;
             }
-            if (threadIdx.x == 0) rstate[1] = rstate[0];
+            if (threadIdx.x == 0) {
+                rstate[1] = rstate[0];
+                rstate[5] = r;   // weight slice now in shared memory
+                rstate[6] = l;
+            }
             have_w = true;
         } else {
             __syncthreads();
         }
-        if (t0 == 0) rs(2);
+        if (t0 == tbeg) rs(2);
         // this warp's K part: ncols / wpg columns in steps of 16, against its group's 24 rows
         float d[2][3][4];
 #pragma unroll
@@ -395,7 +431,7 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
             }
             if (t < nt && e < ne) p.rpart[((size_t)sl * T + t0 + t) * E + eg * kPRouteExperts + e] = sh + (sm_ + slo);
         }
-        if (t0 == 0) rs(3);
+        if (t0 == tbeg) rs(3);
     }
     rs(4);
     if (!route_is_small(p)) return true;   // larger blocks: the grid sums the partials (logits_reduce)
@@ -455,19 +491,44 @@ __device__ __noinline__ void operand_tasks(const PersistParams& p, const Persist
     const int H = p.H, nb = H / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const int gw = (gridDim.x - 1 - blockIdx.x) * nw + warp;
-    for (int i = gw; i < p.T * nb; i += gridDim.x * nw) {
-        const int t = i / nb, kb = i % nb;
-        const size_t o = (size_t)t * H + kb * 32 + lane;
-        float v;
-        if (p.norm) {
-            const float iv = inv_rms(p, t);
-            v = __ldcg(p.resid + o) * iv * __bfloat162float(ly.norm_w[kb * 32 + lane]);
-        } else {
-            v = __bfloat162float(p.x[o]);
+    const int n = p.T * nb, step = gridDim.x * nw;
+    if (n <= step) {   // at most one task per warp (small blocks): the short code path
+        if (gw < n) {
+            const int t = gw / nb, kb = gw % nb;
+            const size_t o = (size_t)t * H + kb * 32 + lane;
+            const float v = p.norm ? __ldcg(p.resid + o) * inv_rms(p, t) * __bfloat162float(ly.norm_w[kb * 32 + lane])
+                                   : __bfloat162float(p.x[o]);
+            uint32_t sb0, sb1;
+            const uint32_t codes = split_e2m1_terms(v, sb0, sb1);
+            store_act_terms(p.xb4, p.xsf, H, t, kb, lane, codes, sb0, sb1);
         }
-        uint32_t sb0, sb1;
-        const uint32_t codes = split_e2m1_terms(v, sb0, sb1);
-        store_act_terms(p.xb4, p.xsf, H, t, kb, lane, codes, sb0, sb1);
+        fence_proxy_async_global();
+        return;
+    }
+    constexpr int kB = 4;   // tasks in flight per warp: their loads and shuffle chains overlap
+    for (int i0 = gw; i0 < n; i0 += kB * step) {
+        float v[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int i = i0 + j * step, t = i / nb, kb = i % nb;
+            v[j] = 0.0f;
+            if (i >= n) continue;
+            const size_t o = (size_t)t * H + kb * 32 + lane;
+            if (p.norm) {
+                const float iv = inv_rms(p, t);
+                v[j] = __ldcg(p.resid + o) * iv * __bfloat162float(ly.norm_w[kb * 32 + lane]);
+            } else {
+                v[j] = __bfloat162float(p.x[o]);
+            }
+        }
+        uint32_t codes[kB], sb0[kB], sb1[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) codes[j] = split_e2m1_terms<true>(v[j], sb0[j], sb1[j]);
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int i = i0 + j * step;
+            if (i < n) store_act_terms(p.xb4, p.xsf, H, i / nb, i % nb, lane, codes[j], sb0[j], sb1[j]);
+        }
     }
     fence_proxy_async_global();   // read next by the expert phase's bulk copies
 }
@@ -871,33 +932,47 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
         }
     }
     __syncthreads();
-    // ---- perm: pairs in id order inside each expert (rounds of blockDim pairs)
-    for (int base = 0; base < npairs; base += blockDim.x) {
-        const int s = base + threadIdx.x;
+    // ---- perm: pairs in id order inside each expert.  Warp w owns the contiguous segment
+    // [w seg, (w + 1) seg) of the pair ids: its per-expert counts, one scan over the warps
+    // in warp order (on top of the expert offsets), then each warp places its pairs in order.
+    const int seg = (npairs + nw - 1) / nw;
+    const int s_lo = min(npairs, warp * seg), s_hi = min(npairs, s_lo + seg);
+    auto pair_expert = [&](int s) {
         int e = -1;
-        if (s < npairs) {
+        if (s < s_hi) {
             e = rb.idx[s];
             if (e < p.e_begin || e >= p.e_end) e = -1;
         }
-        for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wcnt[i] = 0;
-        __syncthreads();
+        return e;
+    };
+    for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    for (int b = s_lo; b < s_hi; b += 32) {
+        const int e = pair_expert(b + lane);
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+        if (e >= 0 && (peers & ((1u << lane) - 1u)) == 0) wcnt[warp * E + e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+        int run = cnt[x];
+        for (int w = 0; w < nw; ++w) {
+            const int c = wcnt[w * E + x];
+            wcnt[w * E + x] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (int b = s_lo; b < s_hi; b += 32) {
+        const int s = b + lane, e = pair_expert(s);
         const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
         const int lane_rank = __popc(peers & ((1u << lane) - 1u));
-        if (e >= 0 && lane_rank == 0) wcnt[warp * E + e] = __popc(peers);
-        __syncthreads();
-        for (int x = threadIdx.x; x < E; x += blockDim.x) {
-            int run = cnt[x];
-            for (int w = 0; w < nw; ++w) {
-                const int c = wcnt[w * E + x];
-                wcnt[w * E + x] = run;
-                run += c;
-            }
-            cnt[x] = run;
-        }
-        __syncthreads();
         if (e >= 0) rb.perm[wcnt[warp * E + e] + lane_rank] = s;
-        __syncthreads();
+        __syncwarp();
+        if (e >= 0 && lane_rank == 0) wcnt[warp * E + e] += __popc(peers);
+        __syncwarp();
     }
+    __syncthreads();
     sub(3);
     // ---- first chunk of each routed expert (chunks of <= 8 pairs) and the item counts
     const int n_active = misc[0];
@@ -980,17 +1055,22 @@ __device__ __noinline__ void build_items_slice(const PersistParams& p, int* scra
     }
 }
 
+constexpr uint32_t kGatherBufBase = 17408, kGatherBufBytes = 9216;   // per-warp staging buffers (slot area)
+static_assert(kGatherBufBase + 16 * kGatherBufBytes <= (uint32_t)kTcStages * kTcSlotBytes, "gather buffers in the slot area");
+static_assert(4 * (kMaxExperts + 1) * sizeof(int) <= kGatherBufBase, "routing arrays below the gather buffers");
 // The layer input's expert operand gathered per chunk (larger blocks, every CTA, after
 // the grouping is published): unit = (chunk, 256-wide stage), one warp per unit; pair
 // slot p of the chunk gets its token's 8 term rows (1 KB) and their scales (64 B).
 // scratch: the routing arrays staged by build_items_slice.
-__device__ __noinline__ void gather_chunk_operand(const PersistParams& p, const int* scratch) {
+__device__ __noinline__ void gather_chunk_operand(const PersistParams& p, const int* scratch, uint8_t* slots) {
     const int n_active = __ldcg(p.rb.active);
     const int* s_c0 = scratch;
     const int* s_beg = scratch + n_active + 1 + n_active;
     const int* s_cnt = s_beg + n_active;
     const int nst = p.H / kTcKS, total_chunks = s_c0[n_active];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    // this warp's staging buffer: 8 KB of rows + 512 B of scales, past the routing arrays
+    const uint32_t buf = smem_u32(slots) + kGatherBufBase + (uint32_t)warp * kGatherBufBytes;
     for (int u = blockIdx.x * nw + warp; u < total_chunks * nst; u += gridDim.x * nw) {
         const int c = u / nst, st = u % nst;
         int lo = 0, hi = n_active - 1;   // the routed expert of chunk c
@@ -1001,16 +1081,21 @@ __device__ __noinline__ void gather_chunk_operand(const PersistParams& p, const 
         const int tc = c - s_c0[lo], beg = s_beg[lo] + tc * kTmaTok, ntok = min(kTmaTok, s_cnt[lo] - tc * kTmaTok);
         uint8_t* dst = const_cast<uint8_t*>(p.ta.xc4) + ((size_t)c * nst + st) * 8192;   // workspace memory
         uint8_t* dsf = const_cast<uint8_t*>(p.ta.xcs) + ((size_t)c * nst + st) * 512;
+        // the chunk's tokens (lane q: pair q), then every pair's rows and scales into this
+        // warp's shared-memory buffer (all copies in flight at once), then out in one run
+        const int tq = lane < ntok ? __ldcg(p.rb.perm + beg + lane) / p.k : 0;
         for (int q = 0; q < ntok; ++q) {
-            const int t = __ldcg(p.rb.perm + beg + q) / p.k;
-            const int4* src = reinterpret_cast<const int4*>(p.xb4 + ((size_t)t * nst + st) * 1024);
-            int4* d = reinterpret_cast<int4*>(dst + q * 1024);
-            d[lane] = __ldcg(src + lane);
-            d[lane + 32] = __ldcg(src + lane + 32);
-            if (lane < 4)
-                reinterpret_cast<int4*>(dsf + q * 64)[lane] =
-                    __ldcg(reinterpret_cast<const int4*>(p.xsf + ((size_t)t * nst + st) * 64) + lane);
+            const int t = __shfl_sync(0xFFFFFFFFu, tq, q);
+            const uint8_t* src = p.xb4 + ((size_t)t * nst + st) * 1024;
+            cp_async_16(buf + q * 1024 + lane * 16, src + lane * 16);
+            cp_async_16(buf + q * 1024 + 512 + lane * 16, src + 512 + lane * 16);
+            if (lane < 4) cp_async_16(buf + 8192 + q * 64 + lane * 16, p.xsf + ((size_t)t * nst + st) * 64 + lane * 16);
         }
+        cp_async_wait_all();
+        __syncwarp();
+        for (int i = lane; i < ntok * 64; i += 32) reinterpret_cast<int4*>(dst)[i] = ld_shared_v4(buf + i * 16);
+        if (lane < ntok * 4) reinterpret_cast<int4*>(dsf)[lane] = ld_shared_v4(buf + 8192 + lane * 16);
+        __syncwarp();   // the buffer is read before the next unit's copies land
     }
 }
 
@@ -1101,7 +1186,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     unsigned epoch = 0;
     TcRoleState rs{0u, 0u, 0u, 0u};
     int* rstate = reinterpret_cast<int*>(sm.red + 40);     // router-weight copy state (router_issue)
-    const int units = ((p.E + kPRouteExperts - 1) / kPRouteExperts) * (p.H / p.rslice);
+    const int units = router_units(p);
     const int cunits = p.T * (p.H / kCombineChunk);
     constexpr bool small = !kLarge;
     auto stamp = [&](int i) {
@@ -1113,17 +1198,19 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         if (lane == 0) {
             rstate[0] = rstate[1] = 0;
             rstate[2] = rstate[3] = -1;
+            rstate[5] = rstate[6] = -1;   // no weight slice resident
         }
         __syncwarp();
-        if (blockIdx.x < units) {
-            router_issue(p, p.layer[0], blockIdx.x, sm, rstate, lane);
+        if (router_first<kLarge>(units) < router_end<kLarge>(units)) {
+            router_issue(p, p.layer[0], router_first<kLarge>(units), sm, rstate, lane);
             if (lane == 0) {
-                rstate[2] = blockIdx.x;
+                rstate[2] = router_first<kLarge>(units);
                 rstate[3] = 0;
             }
-            if (!p.norm) {
-                const int c0 = (blockIdx.x % (p.H / p.rslice)) * p.rslice;
-                for (int t = lane; t < min(p.T, 64); t += 32)
+            if (!p.norm) {   // the first unit's input rows into L2
+                const int n_tb = router_tblocks(p), u0 = router_first<kLarge>(units);
+                const int c0 = ((u0 / n_tb) % (p.H / p.rslice)) * p.rslice, tb0 = (u0 % n_tb) * p.rtok;
+                for (int t = tb0 + lane; t < min(p.T, tb0 + min(p.rtok, 64)); t += 32)
                     prefetch_l2(p.x + (size_t)t * p.H + c0, (uint32_t)p.rslice * 2);
             }
         }
@@ -1136,9 +1223,12 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
 
     for (int l = 0; l < p.L; ++l) {
         const PersistLayer& ly = p.layer[l];
-        for (int u = blockIdx.x; u < units; u += gridDim.x)
+        for (int u = router_first<kLarge>(units); u < router_end<kLarge>(units); u += router_step<kLarge>())
             if (!router_unit(p, ly, l, u, sm, rstate, deadline)) return;
+        if (threadIdx.x == 0) rstate[5] = -1;   // the slot area is reused from here on
+        if (l == 0) stamp(53);
         operand_tasks(p, ly);
+        if (l == 0) stamp(54);
         if (small && blockIdx.x >= units) {
             // a CTA without a router unit would only wait at the barrier: it runs the routing
             // code (results discarded; shared memory only) or, on every other such CTA, the
@@ -1156,10 +1246,15 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         } else {
             // larger blocks: top-k on every warp of the grid; grouping by CTA 0 while the
             // others wait on a release flag; the work list built by every CTA
+            auto lstamp = [&](int i) {   // routing sub-steps of the first layer (CTA 0, profiling)
+                if (l == 0) stamp(34 + i);
+            };
             logits_reduce(p, ly);
             if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
+            lstamp(0);
             topk_tokens(p);
             if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
+            lstamp(1);
             if (blockIdx.x == 0) {
                 route_phase(p, ly, l, reinterpret_cast<int*>(xs));
                 __syncthreads();
@@ -1181,9 +1276,12 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
                 }
                 if (__syncthreads_or(failed)) return;
             }
+            lstamp(2);
             build_items_slice(p, reinterpret_cast<int*>(xs));
-            gather_chunk_operand(p, reinterpret_cast<const int*>(xs));
+            lstamp(3);
+            gather_chunk_operand(p, reinterpret_cast<const int*>(xs), sm.slots);
             fence_proxy_async_global();   // read next by the expert phase's bulk copies
+            lstamp(4);
             if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
             stamp(3 + 4 * l);
         }
@@ -1197,13 +1295,14 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         ta.rt = small ? sm.rt : nullptr;
         if (l != 0 || p.layer_base != 0) ta.trace = nullptr;
         persist_expert_phase<kLarge>(ta, &ly.maps, smem_raw, tmem, &rs, deadline);
-        if (l + 1 < p.L && blockIdx.x < units) {   // the next layer's first router unit, ahead of time
+        // the next layer's first router unit, ahead of time
+        if (l + 1 < p.L && router_first<kLarge>(units) < router_end<kLarge>(units)) {
             fence_proxy_async_shared();
             __syncthreads();
             if (threadIdx.x < 32) {
-                router_issue(p, p.layer[l + 1], blockIdx.x, sm, rstate, threadIdx.x);
+                router_issue(p, p.layer[l + 1], router_first<kLarge>(units), sm, rstate, threadIdx.x);
                 if (threadIdx.x == 0) {
-                    rstate[2] = blockIdx.x;
+                    rstate[2] = router_first<kLarge>(units);
                     rstate[3] = l + 1;
                 }
             }
