@@ -365,7 +365,7 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
         long best = -1, best_units = 0;
         for (int w = 1024; w >= 256; w /= 2) {
             if (H % w) continue;
-            const int tp = moe::kPRouteTok * (w >= 1024 ? 2 : 4);   // tokens per pass (router_groups)
+            const int tp = moe::kPRouteTok * (p.norm ? 2 : 4) * (w >= 1024 ? 1 : 2);   // tokens per pass (router_groups)
             for (int rt = tp; rt < T + tp; rt += tp) {
                 const long units = (long)egroups * (H / w) * ((T + rt - 1) / rt);
                 const long cost = ((units + h->persist_grid - 1) / h->persist_grid) * ((rt + tp - 1) / tp);

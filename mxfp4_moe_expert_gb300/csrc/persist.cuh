@@ -179,16 +179,21 @@ __device__ __forceinline__ bool route_is_small(const PersistParams& p) {
     return p.T * p.k <= kRtMaxPairs && p.T * p.E <= 8192;
 }
 
+// bf16 terms per input value of the router: the RMSNorm output of a stack is fp32 (three
+// terms hi + mid + lo carry it to 2^-24); the plain input x is bf16 already (one term).
+__device__ __forceinline__ int router_terms(const PersistParams& p) { return p.norm ? 3 : 1; }
 // Router units process G groups of 8 tokens per pass: G = 1 for a single 8-token block
-// (the 16 warps split K); larger blocks G = 2 (1024-column slices) or 4 (narrower).
+// (the 16 warps split K); larger blocks G = 2 / 4 (three terms; 1024-column slices /
+// narrower) or 4 / 8 (one term).
 __device__ __forceinline__ int router_groups(const PersistParams& p) {
-    return p.T > kPRouteTok ? (p.rslice >= 1024 ? 2 : 4) : 1;
+    if (p.T <= kPRouteTok) return 1;
+    return (p.norm ? 2 : 4) * (p.rslice >= 1024 ? 1 : 2);
 }
 // Shared-memory layout of a router unit (slot area): the staged input terms
-// [24 G rows][stride] at 0, the weight rows [32][stride] at router_wbase, then the
-// inverse RMS of the pass's tokens (32 floats).  stride = rslice * 2 + 16 bytes (rows
-// padded by 16 bytes: conflict-free ldmatrix).  The warps' sums [16][32][24] floats
-// (48 KB) reuse offset 0 after the MMAs.
+// [8 NT G rows][stride] at 0 (NT = router_terms), the weight rows [32][stride] at
+// router_wbase, then the inverse RMS of the pass's tokens (TP floats).  stride = rslice *
+// 2 + 16 bytes (rows padded by 16 bytes: conflict-free ldmatrix).  The warps' sums
+// [16][32][24] floats (48 KB) reuse offset 0 after the MMAs.
 __device__ __forceinline__ uint32_t router_stride(const PersistParams& p) { return (uint32_t)p.rslice * 2 + 16; }
 // Router units: (weight slice r = (expert group eg of 32, column slice sl), token block tb),
 // u = r * token blocks + tb with r = eg * slices + sl: the token blocks of one weight
@@ -212,7 +217,7 @@ __device__ __forceinline__ int router_end(int units) {
 template <bool kContiguous>
 __device__ __forceinline__ int router_step() { return kContiguous ? 1 : (int)gridDim.x; }
 __device__ __forceinline__ uint32_t router_wbase(const PersistParams& p) {
-    const uint32_t a = max(24u * router_groups(p) * router_stride(p), 16u * 768u * 4u);
+    const uint32_t a = max(8u * router_terms(p) * router_groups(p) * router_stride(p), 16u * 768u * 4u);
     return (a + 1023u) & ~1023u;
 }
 
@@ -256,19 +261,21 @@ __device__ __forceinline__ void split_bf16x3(float x, uint16_t& hi, uint16_t& mi
 
 // Router unit u = (token block of p.rtok tokens, expert group g of 32, column slice s of
 // p.rslice columns): partial logits of the group over the slice for the block's tokens,
-// 8 G tokens per pass, on the
-// tensor cores: per 8-token group D [32 experts x 24] = W [32 x K] . X^T where the 24
-// columns of X are the bf16 terms hi / mid / lo of the 8 tokens' inputs (fp32
-// accumulation; the three terms carry the fp32 input to within 2^-24).  The 16 / G
-// warps of a group split K; their results are summed in a fixed order.  The weight
-// rows come into shared memory by bulk copies (issued ahead of time where possible);
-// the slice of the layer input (x, or RMSNorm of the residual for a stack) is staged
-// as its three terms.  The unit that finishes a group last (a counter per group) sums
-// the group's slice partials in slice order and writes its logits (+ bias): the result
-// does not depend on which unit comes last.  Returns false (every thread) when the
-// weight copies time out.
+// 8 G tokens per pass, on the tensor cores: per 8-token group D [32 experts x 8 NT] =
+// W [32 x K] . X^T where the 8 NT columns of X are the NT bf16 terms of the 8 tokens'
+// inputs (fp32 accumulation; every bf16 x bf16 product is exact).  NT = 3 for the
+// RMSNorm output of a stack (hi / mid / lo carry the fp32 value to within 2^-24), staged
+// through registers; NT = 1 for the bf16 input x, copied into shared memory as it is
+// (cp.async, no register round trip).  The 16 / G warps of a group split K; their
+// results are summed in a fixed order, the terms last (hi + (mid + lo)).  The weight rows
+// come into shared memory by bulk copies (issued ahead of time where possible).  The
+// unit that finishes a group last (a counter per group) sums the group's slice partials
+// in slice order and writes its logits (+ bias): the result does not depend on which
+// unit comes last.  Returns false (every thread) when the weight copies time out.
+template <int NT>
 __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLayer& ly, int l, int u,
                                          const TcSmem& sm, int* rstate, unsigned long long deadline) {
+    static_assert(NT == 1 || NT == 3, "router input terms");
     const int H = p.H, E = p.E, T = p.T;
     const int n_sl = H / p.rslice;
     const int n_tb = router_tblocks(p);
@@ -282,9 +289,9 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
     const int gw = warp / wpg, kp = warp % wpg;          // this warp's token group and K part
     const int ne = min(kPRouteExperts, E - eg * kPRouteExperts);
     const uint32_t stride = router_stride(p), wbase = router_wbase(p);
-    uint8_t* xt = sm.slots;                              // [24 G][stride]: row 24 g + 8 q + t = term q of token t of group g
+    uint8_t* xt = sm.slots;                              // [8 NT G][stride]: row 8 (NT g + q) + t = term q of token t of group g
     float* red = reinterpret_cast<float*>(sm.slots);     // [16 warps][32 experts][24] after the MMAs
-    float* sinv = reinterpret_cast<float*>(sm.slots + wbase + 32 * stride);   // [TP]
+    float* sinv = reinterpret_cast<float*>(sm.slots + wbase + 32 * stride);   // [TP] (three terms)
     int* flag = rstate + 4;
     auto rs = [&](int i) {   // router timestamps of unit 0, or 1 with token blocks (CTA 0's second unit; profiling)
         if (u == (n_tb > 1 ? 1 : 0) && l == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[48 + i] = globaltimer_ns();
@@ -312,53 +319,58 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
         const int nt = min(TP, tend - t0);
         if (t0 > tbeg) __syncthreads();   // the previous pass's sums have been read
         if (t0 == tbeg) rs(1);
-        if (p.norm)
+        if constexpr (NT == 1) {
+            // the pass's rows of x as they are (rows >= nt keep stale data: their output
+            // columns are not stored)
+            const int n16 = ncols / 8;   // 16-byte pieces per row
+            for (int i = threadIdx.x; i < nt * n16; i += blockDim.x) {
+                const int t = i / n16, c = (i % n16) * 8;
+                cp_async_16(xs_a + (uint32_t)t * stride + (uint32_t)c * 2, p.x + (size_t)(t0 + t) * H + c0 + c);
+            }
+            cp_async_wait_all();
+        } else {
             for (int t = warp; t < nt; t += 16) {
                 const float v = inv_rms(p, t0 + t);
                 if (lane == 0) sinv[t] = v;
             }
-        __syncthreads();
-        // stage the three bf16 terms of the pass's inputs (tokens >= nt: zero)
-        const int n4 = ncols / 4;
-        constexpr int kLd = 4;   // items per thread per round (loads in flight together)
-        for (int i0 = threadIdx.x; i0 < TP * n4; i0 += kLd * blockDim.x) {
-            float4 v[kLd];
+            __syncthreads();
+            // stage the three bf16 terms of the pass's inputs (tokens >= nt: zero)
+            const int n4 = ncols / 4;
+            constexpr int kLd = 4;   // items per thread per round (loads in flight together)
+            for (int i0 = threadIdx.x; i0 < TP * n4; i0 += kLd * blockDim.x) {
+                float4 v[kLd];
 #pragma unroll
-            for (int j = 0; j < kLd; ++j) {   // loads first (in flight together), then the stores
-                const int i = i0 + j * blockDim.x;
-                const int t = i / n4, c = (i % n4) * 4;
-                v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i < TP * n4 && t < nt) {
-                    const size_t o = (size_t)(t0 + t) * H + c0 + c;
-                    if (p.norm) {
+                for (int j = 0; j < kLd; ++j) {   // loads first (in flight together), then the stores
+                    const int i = i0 + j * blockDim.x;
+                    const int t = i / n4, c = (i % n4) * 4;
+                    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (i < TP * n4 && t < nt) {
+                        const size_t o = (size_t)(t0 + t) * H + c0 + c;
                         const float4 r = __ldcg(reinterpret_cast<const float4*>(p.resid + o));
                         const uint2 wv = __ldg(reinterpret_cast<const uint2*>(ly.norm_w + c0 + c));
                         const float iv = sinv[t];
                         v[j] = make_float4(r.x * iv * bf16_lo(wv.x), r.y * iv * bf16_hi(wv.x),
                                            r.z * iv * bf16_lo(wv.y), r.w * iv * bf16_hi(wv.y));
-                    } else {
-                        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(p.x + o));
-                        v[j] = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
                     }
                 }
-            }
 #pragma unroll
-            for (int j = 0; j < kLd; ++j) {
-                const int i = i0 + j * blockDim.x;
-                if (i >= TP * n4) continue;
-                const int t = i / n4, c = (i % n4) * 4;
-                uint16_t h[4], m[4], lo[4];
-                split_bf16x3(v[j].x, h[0], m[0], lo[0]);
-                split_bf16x3(v[j].y, h[1], m[1], lo[1]);
-                split_bf16x3(v[j].z, h[2], m[2], lo[2]);
-                split_bf16x3(v[j].w, h[3], m[3], lo[3]);
-                uint8_t* base = xt + (size_t)(24 * (t >> 3) + (t & 7)) * stride + c * 2;
-                *reinterpret_cast<uint2*>(base) =
-                    make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
-                *reinterpret_cast<uint2*>(base + 8 * stride) =
-                    make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
-                *reinterpret_cast<uint2*>(base + 16 * stride) =
-                    make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+                for (int j = 0; j < kLd; ++j) {
+                    const int i = i0 + j * blockDim.x;
+                    if (i >= TP * n4) continue;
+                    const int t = i / n4, c = (i % n4) * 4;
+                    uint16_t h[4], m[4], lo[4];
+                    split_bf16x3(v[j].x, h[0], m[0], lo[0]);
+                    split_bf16x3(v[j].y, h[1], m[1], lo[1]);
+                    split_bf16x3(v[j].z, h[2], m[2], lo[2]);
+                    split_bf16x3(v[j].w, h[3], m[3], lo[3]);
+                    uint8_t* base = xt + (size_t)(8 * NT * (t >> 3) + (t & 7)) * stride + c * 2;
+                    *reinterpret_cast<uint2*>(base) =
+                        make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+                    *reinterpret_cast<uint2*>(base + 8 * stride) =
+                        make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
+                    *reinterpret_cast<uint2*>(base + 16 * stride) =
+                        make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+                }
             }
         }
         if (!have_w) {   // the weight rows have landed (bounded wait)
@@ -377,16 +389,16 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
             __syncthreads();
         }
         if (t0 == tbeg) rs(2);
-        // this warp's K part: ncols / wpg columns in steps of 16, against its group's 24 rows
-        float d[2][3][4];
+        // this warp's K part: ncols / wpg columns in steps of 16, against its group's 8 NT rows
+        float d[2][NT][4];
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
-            for (int b = 0; b < 3; ++b)
+            for (int b = 0; b < NT; ++b)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) d[a][b][q] = 0.0f;
         const int kw = ncols / wpg;
-        const uint32_t xg = xs_a + (uint32_t)(24 * gw) * stride;
+        const uint32_t xg = xs_a + (uint32_t)(8 * NT * gw) * stride;
         for (int ks = 0; ks < kw; ks += 16) {
             const int k0 = kp * kw + ks;
             uint32_t af[2][4];
@@ -394,24 +406,24 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
             for (int mt = 0; mt < 2; ++mt)
                 ldmatrix_x4(ws_a + (uint32_t)(mt * 16 + (lane & 15)) * stride + (uint32_t)(k0 + (lane >> 4) * 8) * 2,
                             af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
-            uint32_t b0, b1, b2, b3, b4, b5;
-            ldmatrix_x4(xg + (uint32_t)((lane >> 4) * 8 + (lane & 7)) * stride +
-                            (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2,
-                        b0, b1, b2, b3);
-            ldmatrix_x2(xg + (uint32_t)(16 + (lane & 7)) * stride + (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2, b4,
-                        b5);
+            uint32_t b[NT][2];
+            if constexpr (NT == 3)   // terms hi and mid (rows 0..15), then lo below
+                ldmatrix_x4(xg + (uint32_t)((lane >> 4) * 8 + (lane & 7)) * stride +
+                                (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2,
+                            b[0][0], b[0][1], b[1][0], b[1][1]);
+            ldmatrix_x2(xg + (uint32_t)(8 * (NT - 1) + (lane & 7)) * stride + (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2,
+                        b[NT - 1][0], b[NT - 1][1]);
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                mma_bf16_16816(d[mt][0], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b0, b1);
-                mma_bf16_16816(d[mt][1], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b2, b3);
-                mma_bf16_16816(d[mt][2], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b4, b5);
-            }
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int nb = 0; nb < NT; ++nb)
+                    mma_bf16_16816(d[mt][nb], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b[nb][0], b[nb][1]);
         }
         __syncthreads();   // every warp's reads of the x terms are done: red overwrites them
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int nb = 0; nb < 3; ++nb) {
+            for (int nb = 0; nb < NT; ++nb) {
                 const int e = mt * 16 + (lane >> 2), n = nb * 8 + 2 * (lane & 3);
                 float* r = red + warp * 768;
                 r[e * 24 + n] = d[mt][nb][0];
@@ -426,8 +438,10 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
             for (int w = 0; w < wpg; ++w) {
                 const float* r = red + (g * wpg + w) * 768 + e * 24;
                 sh += r[t8];
-                sm_ += r[8 + t8];
-                slo += r[16 + t8];
+                if (NT == 3) {
+                    sm_ += r[8 + t8];
+                    slo += r[16 + t8];
+                }
             }
             if (t < nt && e < ne) p.rpart[((size_t)sl * T + t0 + t) * E + eg * kPRouteExperts + e] = sh + (sm_ + slo);
         }
@@ -1224,7 +1238,9 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     for (int l = 0; l < p.L; ++l) {
         const PersistLayer& ly = p.layer[l];
         for (int u = router_first<kLarge>(units); u < router_end<kLarge>(units); u += router_step<kLarge>())
-            if (!router_unit(p, ly, l, u, sm, rstate, deadline)) return;
+            if (!(p.norm ? router_unit<3>(p, ly, l, u, sm, rstate, deadline)
+                         : router_unit<1>(p, ly, l, u, sm, rstate, deadline)))
+                return;
         if (threadIdx.x == 0) rstate[5] = -1;   // the slot area is reused from here on
         if (l == 0) stamp(53);
         operand_tasks(p, ly);
