@@ -221,29 +221,28 @@ __device__ __forceinline__ uint32_t router_wbase(const PersistParams& p) {
     return (a + 1023u) & ~1023u;
 }
 
-// Router-weight copies: the weight rows of one router unit (up to 32 experts x
-// rslice columns, bf16) land in shared memory (router_wbase into the slot area, rows
-// padded) through bulk copies completing on sm.rw, one row per lane of the issuing
-// warp.  State in shared memory (rstate): [0] copies issued (mbarrier phases), [1]
-// phases waited for, [2] / [3] unit / layer whose copies were issued ahead of time
-// (-1: none).
-__device__ __forceinline__ void router_issue(const PersistParams& p, const PersistLayer& ly, int u,
-                                             const TcSmem& sm, int* rstate, int lane) {   // whole warp
+// Router-weight copies: the weight rows of one router unit (up to 32 experts x rslice
+// columns, bf16) into shared memory (router_wbase into the slot area, rows padded), as
+// 16-byte cp.async copies spread over every thread of the CTA (L2 evict-first): all in
+// flight at once, without a copy-engine request per row.  They have landed once every
+// thread has passed cp.async.wait_all and the block has synchronised.  State in shared
+// memory (rstate): [2] / [3] unit / layer whose copies were issued ahead of time (-1:
+// none), [5] / [6] weight slice / layer in shared memory (-1: none), [8] router_unit's
+// decision to fetch.
+__device__ __forceinline__ void router_fetch(const PersistParams& p, const PersistLayer& ly, int u,
+                                             const TcSmem& sm) {   // whole CTA
     const int n_sl = p.H / p.rslice;
     const int r = u / router_tblocks(p);   // the token block does not change the weights
     const int eg = r / n_sl, sl = r % n_sl;
     const int ne = min(kPRouteExperts, p.E - eg * kPRouteExperts);
-    const uint32_t row = (uint32_t)p.rslice * 2, stride = router_stride(p);
-    if (lane == 0) {
-        fence_proxy_async_shared();   // earlier generic accesses of the slot area come first
-        mbar_arrive_expect_tx(sm.rw, row * ne);
+    const int n16 = p.rslice / 8;          // 16-byte pieces per row
+    const uint32_t stride = router_stride(p), dst = smem_u32(sm.slots + router_wbase(p));
+    const uint64_t pol = l2_evict_first_policy();
+    const __nv_bfloat16* src = ly.router_w + (size_t)eg * kPRouteExperts * p.H + (size_t)sl * p.rslice;
+    for (int i = threadIdx.x; i < ne * n16; i += blockDim.x) {
+        const int row = i / n16, c = (i % n16) * 8;
+        cp_async_16_hint(dst + (uint32_t)row * stride + (uint32_t)c * 2, src + (size_t)row * p.H + c, pol);
     }
-    __syncwarp();
-    if (lane < ne)
-        bulk_load_stream(sm.slots + router_wbase(p) + lane * stride,
-                         ly.router_w + (size_t)(eg * kPRouteExperts + lane) * p.H + sl * p.rslice, row, sm.rw,
-                         l2_evict_first_policy());
-    if (lane == 0) rstate[0] += 1;
 }
 
 // x = hi + mid + lo with each term a bf16 (round to nearest): the remainder is below
@@ -271,10 +270,10 @@ __device__ __forceinline__ void split_bf16x3(float x, uint16_t& hi, uint16_t& mi
 // come into shared memory by bulk copies (issued ahead of time where possible).  The
 // unit that finishes a group last (a counter per group) sums the group's slice partials
 // in slice order and writes its logits (+ bias): the result does not depend on which
-// unit comes last.  Returns false (every thread) when the weight copies time out.
+// unit comes last.
 template <int NT>
-__device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLayer& ly, int l, int u,
-                                         const TcSmem& sm, int* rstate, unsigned long long deadline) {
+__device__ __noinline__ void router_unit(const PersistParams& p, const PersistLayer& ly, int l, int u,
+                                         const TcSmem& sm, int* rstate) {
     static_assert(NT == 1 || NT == 3, "router input terms");
     const int H = p.H, E = p.E, T = p.T;
     const int n_sl = H / p.rslice;
@@ -299,22 +298,16 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
     rs(0);
     fence_proxy_async_shared();
     __syncthreads();   // earlier users of the slot area are done
-    if (warp == 0) {
+    if (threadIdx.x == 0) {
         const bool pre = rstate[2] == u && rstate[3] == l;
-        // the previous unit's weights are this unit's (same slice and layer, all landed)
-        const bool resident = !pre && rstate[5] == r && rstate[6] == l && rstate[0] == rstate[1];
-        __syncwarp();
-        if (!pre && !resident) router_issue(p, ly, u, sm, rstate, lane);
-        __syncwarp();
-        if (lane == 0) {
-            rstate[2] = rstate[3] = -1;
-            rstate[7] = resident;
-        }
+        // the previous unit's weights are this unit's (same slice and layer; they landed in that unit)
+        const bool resident = !pre && rstate[5] == r && rstate[6] == l;
+        rstate[2] = rstate[3] = -1;
+        rstate[8] = !pre && !resident;
     }
     __syncthreads();
-    const uint32_t parity = (uint32_t)(rstate[0] - 1) & 1u;
+    if (rstate[8]) router_fetch(p, ly, u, sm);
     const uint32_t xs_a = smem_u32(xt), ws_a = smem_u32(sm.slots + wbase);
-    bool have_w = rstate[7] != 0;
     for (int t0 = tbeg; t0 < tend; t0 += TP) {
         const int nt = min(TP, tend - t0);
         if (t0 > tbeg) __syncthreads();   // the previous pass's sums have been read
@@ -327,7 +320,6 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
                 const int t = i / n16, c = (i % n16) * 8;
                 cp_async_16(xs_a + (uint32_t)t * stride + (uint32_t)c * 2, p.x + (size_t)(t0 + t) * H + c0 + c);
             }
-            cp_async_wait_all();
         } else {
             for (int t = warp; t < nt; t += 16) {
                 const float v = inv_rms(p, t0 + t);
@@ -373,20 +365,11 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
                 }
             }
         }
-        if (!have_w) {   // the weight rows have landed (bounded wait)
-            const int ok = wait_phase(sm.rw, parity, deadline, p.wl.abort) ? 1 : 0;
-            if (__syncthreads_and(ok) == 0) {
-                if (threadIdx.x == 0 && atomicExch(p.wl.abort, 1) == 0) raise_status(p.ta.status, MOE_ERR_TIMEOUT, -3);
-                return false;
-            }
-            if (threadIdx.x == 0) {
-                rstate[1] = rstate[0];
-                rstate[5] = r;   // weight slice now in shared memory
-                rstate[6] = l;
-            }
-            have_w = true;
-        } else {
-            __syncthreads();
+        cp_async_wait_all();   // this thread's weight and input copies have landed
+        __syncthreads();
+        if (t0 == tbeg && threadIdx.x == 0) {
+            rstate[5] = r;   // weight slice now in shared memory
+            rstate[6] = l;
         }
         if (t0 == tbeg) rs(2);
         // this warp's K part: ncols / wpg columns in steps of 16, against its group's 8 NT rows
@@ -448,7 +431,7 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
         if (t0 == tbeg) rs(3);
     }
     rs(4);
-    if (!route_is_small(p)) return true;   // larger blocks: the grid sums the partials (logits_reduce)
+    if (!route_is_small(p)) return;   // larger blocks: the grid sums the partials (logits_reduce)
     // the last unit of the group turns the slice partials into logits
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -475,7 +458,6 @@ __device__ __noinline__ bool router_unit(const PersistParams& p, const PersistLa
             p.rb.logits[(size_t)t * E + e] = z + (ly.router_b ? __ldg(ly.router_b + e) : 0.0f);
         }
     }
-    return true;
 }
 
 // Logits of a larger block from the router slice partials (slices in order) + bias,
@@ -1199,7 +1181,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     float* xs = reinterpret_cast<float*>(sm.slots);        // routing scratch
     unsigned epoch = 0;
     TcRoleState rs{0u, 0u, 0u, 0u};
-    int* rstate = reinterpret_cast<int*>(sm.red + 40);     // router-weight copy state (router_issue)
+    int* rstate = reinterpret_cast<int*>(sm.red + 40);     // router-weight copy state (router_fetch)
     const int units = router_units(p);
     const int cunits = p.T * (p.H / kCombineChunk);
     constexpr bool small = !kLarge;
@@ -1207,26 +1189,23 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         if (blockIdx.x == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[i] = globaltimer_ns();
     };
     stamp(0);
-    if (threadIdx.x < 32) {   // warp 0: this CTA's first router unit, weights into shared memory, x into L2
-        const int lane = threadIdx.x;
-        if (lane == 0) {
-            rstate[0] = rstate[1] = 0;
-            rstate[2] = rstate[3] = -1;
-            rstate[5] = rstate[6] = -1;   // no weight slice resident
+    // this CTA's first router unit: weights into shared memory, x into L2
+    if (threadIdx.x == 0) {
+        rstate[2] = rstate[3] = -1;
+        rstate[5] = rstate[6] = -1;   // no weight slice resident
+    }
+    if (router_first<kLarge>(units) < router_end<kLarge>(units)) {
+        router_fetch(p, p.layer[0], router_first<kLarge>(units), sm);
+        if (threadIdx.x == 0) {
+            rstate[2] = router_first<kLarge>(units);
+            rstate[3] = 0;
         }
-        __syncwarp();
-        if (router_first<kLarge>(units) < router_end<kLarge>(units)) {
-            router_issue(p, p.layer[0], router_first<kLarge>(units), sm, rstate, lane);
-            if (lane == 0) {
-                rstate[2] = router_first<kLarge>(units);
-                rstate[3] = 0;
-            }
-            if (!p.norm) {   // the first unit's input rows into L2
-                const int n_tb = router_tblocks(p), u0 = router_first<kLarge>(units);
-                const int c0 = ((u0 / n_tb) % (p.H / p.rslice)) * p.rslice, tb0 = (u0 % n_tb) * p.rtok;
-                for (int t = tb0 + lane; t < min(p.T, tb0 + min(p.rtok, 64)); t += 32)
-                    prefetch_l2(p.x + (size_t)t * p.H + c0, (uint32_t)p.rslice * 2);
-            }
+        if (!p.norm && threadIdx.x < 32) {   // the first unit's input rows into L2
+            const int lane = threadIdx.x;
+            const int n_tb = router_tblocks(p), u0 = router_first<kLarge>(units);
+            const int c0 = ((u0 / n_tb) % (p.H / p.rslice)) * p.rslice, tb0 = (u0 % n_tb) * p.rtok;
+            for (int t = tb0 + lane; t < min(p.T, tb0 + min(p.rtok, 64)); t += 32)
+                prefetch_l2(p.x + (size_t)t * p.H + c0, (uint32_t)p.rslice * 2);
         }
     }
     if (p.norm && p.init_from_x) {
@@ -1238,9 +1217,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     for (int l = 0; l < p.L; ++l) {
         const PersistLayer& ly = p.layer[l];
         for (int u = router_first<kLarge>(units); u < router_end<kLarge>(units); u += router_step<kLarge>())
-            if (!(p.norm ? router_unit<3>(p, ly, l, u, sm, rstate, deadline)
-                         : router_unit<1>(p, ly, l, u, sm, rstate, deadline)))
-                return;
+            p.norm ? router_unit<3>(p, ly, l, u, sm, rstate) : router_unit<1>(p, ly, l, u, sm, rstate);
         if (threadIdx.x == 0) rstate[5] = -1;   // the slot area is reused from here on
         if (l == 0) stamp(53);
         operand_tasks(p, ly);
@@ -1315,12 +1292,10 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         if (l + 1 < p.L && router_first<kLarge>(units) < router_end<kLarge>(units)) {
             fence_proxy_async_shared();
             __syncthreads();
-            if (threadIdx.x < 32) {
-                router_issue(p, p.layer[l + 1], router_first<kLarge>(units), sm, rstate, threadIdx.x);
-                if (threadIdx.x == 0) {
-                    rstate[2] = router_first<kLarge>(units);
-                    rstate[3] = l + 1;
-                }
+            router_fetch(p, p.layer[l + 1], router_first<kLarge>(units), sm);
+            if (threadIdx.x == 0) {
+                rstate[2] = router_first<kLarge>(units);
+                rstate[3] = l + 1;
             }
         }
         if (small && blockIdx.x == 0) publish_small(p, l, sm.rt);
@@ -1345,10 +1320,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_con
     __syncthreads();
     if (threadIdx.x == 0 && p.tstamp && blockIdx.x < 256)   // when each CTA finished (profiling)
         p.tstamp[56 + blockIdx.x] = globaltimer_ns();
-    if (threadIdx.x == 0) {   // router-weight copies still in flight (a run cut short) land before exit
-        const int* rstate = reinterpret_cast<const int*>(sm.red + 40);
-        if (rstate[0] > rstate[1]) drain_phase(sm.rw, (uint32_t)(rstate[0] - 1) & 1u, globaltimer_ns() + p.ta.timeout_ns);
-    }
+    cp_async_wait_all();   // router-weight copies still in flight (a run cut short) land before exit
     tc_teardown(sm, tmem, p.ta.timeout_ns);
 }
 

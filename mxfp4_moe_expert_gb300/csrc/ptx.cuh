@@ -279,6 +279,11 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 __device__ __forceinline__ void cp_async_16(uint32_t saddr, const void* gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gsrc) : "memory");
 }
+// The same with an L2 cache policy (createpolicy) for the source lines.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t saddr, const void* gsrc, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(saddr), "l"(gsrc), "l"(policy)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ int4 ld_shared_v4(uint32_t saddr) {
     int4 v;
