@@ -148,7 +148,6 @@ struct TcSmem {
     uint8_t* scales;    // [kTcScaleRing][2 boxes][kTcScaleEntry / 2]
     uint64_t *full, *empty, *accf, *acce, *ringf, *ringe, *sfull, *sempty, *epib, *drain;
     uint64_t *claim, *sfc, *drain2;   // slot claimed by the producer; scale factors in tensor memory; SF drain
-    uint64_t* rw;       // router-weight copies of the persistent kernel
     uint32_t* tmem_slot;
     TcSlotMeta* meta;
     TcItemInfo* ring;
@@ -173,7 +172,6 @@ __device__ __forceinline__ TcSmem tc_smem(uint8_t* smem_raw) {
     s.sempty = b; b += kTcScaleRing;
     s.epib = b; b += 1;
     s.drain = b; b += 1;
-    s.rw = b; b += 1;
     s.claim = b; b += kTcStages;
     s.sfc = b; b += kTcStages;
     s.drain2 = b; b += 1;
@@ -184,7 +182,7 @@ __device__ __forceinline__ TcSmem tc_smem(uint8_t* smem_raw) {
     s.red = reinterpret_cast<float*>(aux + 640 + kItemRing * sizeof(TcItemInfo) + sizeof(RouteTable));
     return s;
 }
-static_assert(8 * (4 * kTcStages + 2 + 2 * kItemRing + 2 * kTcScaleRing + 4) <= 384, "barriers");
+static_assert(8 * (4 * kTcStages + 2 + 2 * kItemRing + 2 * kTcScaleRing + 3) <= 384, "barriers");
 static_assert(400 + kTcStages * sizeof(TcSlotMeta) <= 640, "slot metadata");
 static_assert(640 + kItemRing * sizeof(TcItemInfo) + sizeof(RouteTable) + 64 * sizeof(float) <= kTcAuxBytes, "aux");
 
@@ -206,7 +204,6 @@ __device__ __forceinline__ void tc_smem_init(const TcSmem& s) {
     }
     mbar_init(s.epib, kTcEpiWarps);
     mbar_init(s.drain, 1);
-    mbar_init(s.rw, 1);
     for (int i = 0; i < kTcStages; ++i) {
         mbar_init(&s.claim[i], 1);
         mbar_init(&s.sfc[i], kTcSfWarps);

@@ -267,7 +267,7 @@ __device__ __forceinline__ void split_bf16x3(float x, uint16_t& hi, uint16_t& mi
 // through registers; NT = 1 for the bf16 input x, copied into shared memory as it is
 // (cp.async, no register round trip).  The 16 / G warps of a group split K; their
 // results are summed in a fixed order, the terms last (hi + (mid + lo)).  The weight rows
-// come into shared memory by bulk copies (issued ahead of time where possible).  The
+// come into shared memory by router_fetch (issued ahead of time where possible).  The
 // unit that finishes a group last (a counter per group) sums the group's slice partials
 // in slice order and writes its logits (+ bias): the result does not depend on which
 // unit comes last.
@@ -1098,10 +1098,20 @@ __device__ __noinline__ void gather_chunk_operand(const PersistParams& p, const 
 // y = sum_j g[t, j] * partial[t*k + j] (slot order; slots outside the shard skipped) for
 // a layer without a residual stack, over every thread of the grid, 4 columns per step.
 // dry: one step per thread of this CTA and nothing stored (brings the code into the caches).
-__device__ __noinline__ void combine_elems(const PersistParams& p, int l, const RouteTable* rt, bool dry = false) {
+// Blocks routed through the workspace first copy every pair's (expert, gate) into shared
+// memory (scratch, up to 4096 pairs), so a step waits for its partials only.
+__device__ __noinline__ void combine_elems(const PersistParams& p, int l, const RouteTable* rt, uint8_t* scratch,
+                                           bool dry = false) {
     const int H4 = p.H / 4, k = p.k;
     const int n = p.T * H4;
     const bool store = !dry && l == p.L - 1 && p.write_y;
+    int2* tab = nullptr;   // [T * k] (expert, gate bits)
+    if (!rt && !dry && p.T * k <= 4096) {
+        tab = reinterpret_cast<int2*>(scratch);
+        for (int i = threadIdx.x; i < p.T * k; i += blockDim.x)
+            tab[i] = make_int2(__ldcg(p.rb.idx + i), __float_as_int(__ldcg(p.rb.gate + i)));
+        __syncthreads();
+    }
     const int i0 = dry ? (int)threadIdx.x : blockIdx.x * blockDim.x + threadIdx.x;
     const int step = dry ? n : gridDim.x * blockDim.x;
     for (int i = i0; i < n; i += step) {
@@ -1116,9 +1126,11 @@ __device__ __noinline__ void combine_elems(const PersistParams& p, int l, const 
                 g[q] = 0.0f;
                 v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (j < k) {
-                    const int e = rt ? rt->idx[t * k + j] : __ldcg(p.rb.idx + t * k + j);
+                    const int e = rt ? rt->idx[t * k + j] : tab ? tab[t * k + j].x : __ldcg(p.rb.idx + t * k + j);
                     if (e >= p.e_begin && e < p.e_end) {
-                        g[q] = rt ? rt->gate[t * k + j] : __ldcg(p.rb.gate + t * k + j);
+                        g[q] = rt    ? rt->gate[t * k + j]
+                               : tab ? __int_as_float(tab[t * k + j].y)
+                                     : __ldcg(p.rb.gate + t * k + j);
                         v[q] = __ldcg(reinterpret_cast<const float4*>(p.ta.partial + (size_t)(t * k + j) * p.H) + c4);
                     }
                 }
@@ -1228,7 +1240,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
             // combine code (nothing stored), so that code is in L2 when the whole grid needs it
             if (((blockIdx.x - units) & 1) == 0 || l + 1 < p.L) route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
             else if (p.norm) combine_unit(p, blockIdx.x % cunits, l, red, nullptr, true);
-            else combine_elems(p, l, nullptr, true);
+            else combine_elems(p, l, nullptr, sm.slots, true);
         }
         const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
         if (!grid_sync(p.bar, epoch, deadline, abort, status, withhold)) return;
@@ -1304,7 +1316,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         if (p.norm)
             for (int u = blockIdx.x; u < cunits; u += gridDim.x) combine_unit(p, u, l, red, small ? sm.rt : nullptr);
         else
-            combine_elems(p, l, small ? sm.rt : nullptr);
+            combine_elems(p, l, small ? sm.rt : nullptr, sm.slots);
         stamp(5 + 4 * l);
         if (l + 1 < p.L && !grid_sync(p.bar, epoch, deadline, abort, status)) return;
     }
