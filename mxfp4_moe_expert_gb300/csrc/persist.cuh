@@ -4,21 +4,24 @@
 // guide "关键实现细节" item 3: per-launch gaps of 5-10 us and 10-30% operator-boundary
 // overhead at high token rates).  One CTA per SM, the expert kernel's block
 // shape (16 warps) and tensor-memory allocation.  Per layer:
-//   [router]           all CTAs, (32 experts x 256..1024 columns) units: partial
-//                      logits, completed per expert group by the group's last unit;
-//                      every warp of the grid: the layer input as the experts'
-//                      operand (8 E2M1 terms per MX block)
+//   [router]           all CTAs, units of (32 experts x 256..1024 columns x a token
+//                      block): partial logits, completed per expert group by the
+//                      group's last unit (small blocks) or by the whole grid (larger
+//                      blocks); every warp of the grid: the layer input as the
+//                      experts' operand (8 E2M1 terms per MX block)
 //   -- grid barrier --
 //   [route]            small blocks (T*k <= 64): every CTA takes the top-k and groups
 //                      the pairs in its own shared memory (identical results
 //                      everywhere; CTA 0 publishes them after its expert phase);
-//                      larger blocks: CTA 0 builds a global work list while the
-//                      other CTAs wait on a release flag
+//                      larger blocks: top-k on every warp, the grouping by CTA 0 while
+//                      the other CTAs wait on a release flag, then every CTA builds its
+//                      share of the work list and gathers the operand per chunk
 //   [experts]          the work-queue expert phase of expert_tc.cuh
 //   -- grid barrier --
-//   [combine]          all CTAs, (token, 1024 columns) units: gate-weighted sum of
-//                      the pair outputs, residual add, sums of squares for the next
-//                      layer's RMSNorm
+//   [combine]          all CTAs: gate-weighted sum of the pair outputs (grid-stride
+//                      over (token, 4 columns)); with a stack, (token, 256 columns)
+//                      units that also add the residual and keep the sums of squares
+//                      for the next layer's RMSNorm
 //   -- grid barrier --  (before the next layer's router)
 // Every wait is bounded by the forward's deadline; a timeout sets the status
 // word and the abort flag, and every CTA leaves at its next wait.
