@@ -60,3 +60,22 @@ def test_traffic_record_names_a_summary_and_a_source_hash(name):
     rec = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))[name]
     assert rec["dram_read_bytes"] > 0 and rec["dram_write_bytes"] > 0
     assert len(rec["source_sha256"]) == 64
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON line with
+    the keys the driver reads; run on the small workload so it takes a second."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                        "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "us" and d["higher_is_better"] is False
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["value"] > 0   # at least 3 warm-up steps, whatever asked
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "tiny"
