@@ -55,3 +55,19 @@ def test_status_strings_and_host_side_validation(lib_path):
     assert pkg.moe_mxfp4_quantize(None, 1, 32, None, None, None) == pkg.MOE_ERR_INVALID_ARG
     assert pkg.moe_mxfp4_forward(None, None, 8, None, None, 0, None) == pkg.MOE_ERR_INVALID_ARG
     pkg.moe_mxfp4_destroy(None)
+
+
+def test_every_entry_point_rejects_a_null_handle_or_bad_sizes_without_a_device(lib_path):
+    """Host-side argument checks of the entry points, all before any CUDA call."""
+    pkg.load_library(lib_path)
+    assert pkg.moe_mxfp4_workspace_bytes(None, 8)[0] == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_forward_host(None, None, 8, None, None, 0, None) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_check(None, None, None) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_forward_static(None, None, 8, None, None) == pkg.MOE_ERR_INVALID_ARG
+    # acceptance: sizes are checked first; zero streams is a no-op; null buffers are refused
+    assert pkg.moe_mxfp4_accept(None, None, -1, 8, 100, None, None, None, None) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_accept(None, None, 1, 0, 100, None, None, None, None) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_accept(None, None, 1, 8, 0, None, None, None, None) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_accept(None, None, 1, 8, 1 << 31, None, None, None, None) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_accept(None, None, 0, 8, 100, None, None, None, None) == pkg.MOE_OK
+    assert pkg.moe_mxfp4_accept(None, None, 1, 8, 100, None, None, None, None) == pkg.MOE_ERR_INVALID_ARG
