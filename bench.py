@@ -338,7 +338,7 @@ def run_gpu(args):
         "implied_tokens_per_s": round(ACCEPTANCE_LENGTH / (us * 1e-6), 1),
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(kern_gbs / peak, 4),
-                     "traffic": measured_traffic(wl.name) if persistent else None, "peak_kind": peak_kind,
+                     "traffic": layer_traffic(wl) if persistent else None, "peak_kind": peak_kind,
                      "kernel": "persistent forward kernel" if persistent else
                                "whole forward (CUDA graph of the per-phase launches)" if graph is not None else
                                "expert FFN kernel",
@@ -393,6 +393,14 @@ def measured_traffic(workload):
     if not e or e.get("source_sha256") != kernel_sources_sha256():
         return None
     return int(e["dram_read_bytes"] + e["dram_write_bytes"])
+
+
+def layer_traffic(wl):
+    """The captured DRAM bytes of one launch per layer it runs (a launch runs up to 8
+    layers), on the same per-layer basis as `kernel_bytes_per_layer`; None without a
+    current capture."""
+    t = measured_traffic(wl.name)
+    return None if t is None else int(round(t / min(wl.layers, 8)))
 
 
 def _percentiles(v):

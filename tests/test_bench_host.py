@@ -54,7 +54,7 @@ def test_tma_path_rule():
     assert not b.moe_tma(WORKLOADS["tiny"])   # H = 256: the one-launch-per-phase path
 
 
-@pytest.mark.parametrize("name", ["large", "mid", "batched"])
+@pytest.mark.parametrize("name", ["large", "mid", "batched", "stack"])
 def test_traffic_record_names_a_summary_and_a_source_hash(name):
     import json
     rec = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))[name]
