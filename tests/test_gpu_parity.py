@@ -112,6 +112,9 @@ SMALL = [
     Workload("tma_many_tokens", T=40, H=512, I=512, E=4, k=2, seed=0x5EED0114),
     # 64 pairs over 4 experts: several 8-pair chunks per expert in the shared-memory routing path
     Workload("tma_multi_chunk", T=32, H=512, I=512, E=4, k=2, seed=0x5EED0116),
+    # the largest block of the persistent path: T * k = 4096 pairs (512 chunks), routed through
+    # the workspace, every router token block and the combine's shared-memory pair table full
+    Workload("tma_max_pairs", T=512, H=512, I=512, E=16, k=8, seed=0x5EED0118),
 ]
 
 
