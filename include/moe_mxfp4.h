@@ -26,7 +26,8 @@
  *    library never allocates device memory (the caller provides a workspace
  *    whose size moe_mxfp4_workspace_bytes reports) and never frees caller memory.
  *  - Weights are BORROWED at create time: they must stay allocated and unchanged
- *    until moe_mxfp4_destroy.  No copy or repack is made.
+ *    until moe_mxfp4_destroy.  create makes no copy or repack (moe_mxfp4_pack, below,
+ *    is a separate call the caller makes once, into memory it owns).
  *  - Calls are asynchronous on the given stream (a cudaStream_t passed as void*,
  *    NULL = legacy default stream) unless stated otherwise.  Errors the host can
  *    see are returned at once; errors found on the device (a NaN scale byte, a
@@ -44,6 +45,9 @@
  *    S[r, c/32] multiplies elements c of row r by 2^(S - 127).
  *  - norm_w: bf16 [H] (required with MOE_FLAG_NORM).
  *  Every base pointer must be 16-byte aligned; H and I must be multiples of 128.
+ *  - packed (optional, see moe_mxfp4_pack): the same expert bytes rearranged
+ *    tile-major, so that the expert kernels read every stage of weights as one
+ *    contiguous run of memory.  Requires H and I multiples of 512.
  *
  * What a layer computes (per token t):
  *   logit[e] = sum_h x[t,h] Wr[e,h] + b[e]
@@ -112,6 +116,9 @@ typedef struct {
     const uint8_t* down_q_dev;  /* [E, H, I/2] */
     const uint8_t* down_s_dev;  /* [E, H, I/32] */
     const void* norm_w_dev;     /* bf16 [H] or NULL */
+    const uint8_t* packed_dev;  /* NULL, or this layer's experts in the packed layout (moe_mxfp4_pack,
+                                 * 256-byte aligned): the forward then reads the experts from here only
+                                 * and gate_q_dev .. down_s_dev may be NULL */
 } moe_mxfp4_layer;
 
 /* Optional copies of the routing of every layer, written by a forward when the
@@ -195,7 +202,9 @@ const char* moe_mxfp4_status_string(int status);
  *  - Returns MOE_ERR_WORKSPACE, and runs nothing, when num_tokens needs more workspace
  *    than the static array holds (moe_mxfp4_workspace_bytes tells the need).
  *  - The first call on a device, with that device current, looks up the array's device
- *    address (once per device); make that first call before any stream capture.
+ *    address (once per device); make that first call before any stream capture.  The
+ *    address is kept for the life of the process: after cudaDeviceReset on a device, do
+ *    not call this function again on that device.
  *  - All calls on a device share the one array and leave their contents in it; the
  *    forward re-initialises everything it needs.  Calls whose work overlaps on the GPU
  *    (different streams, or different handles at the same time) race on the array.
@@ -205,6 +214,33 @@ const char* moe_mxfp4_status_string(int status);
 #define MOE_MXFP4_STATIC_WORKSPACE_BYTES (16u << 20)
 int moe_mxfp4_forward_static(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens, void* y_dev,
                              void* stream);
+
+/* Packed expert layout.  The canonical layout above stores each matrix row by row, so
+ * the weights the kernels stream per 256-K stage of a work item (the gate and the up
+ * rows of a 128-row block, or 256 down rows: 32 KB of codes) are 256 runs of 128 bytes
+ * in one or two matrices, and the scales of a few consecutive 32-blocks are a few bytes
+ * per row: each stage costs two or four copy requests through two tensor maps.  The
+ * packed layout holds the same bytes, rearranged once (when the weights are loaded,
+ * like any inference engine's weight preprocessing), so that each stage and each scale
+ * group is one contiguous run read by one copy ("MiMo x TileRT", 万亿参数推理为什么特别难:
+ * decode speed is HBM bandwidth over bytes read, so the bytes must arrive at the full
+ * rate).  Three 256-byte-aligned sections:
+ *   codes:     gate/up tiles [E][I/128][H/256][256 rows: 128 gate, then the same 128 up][128 B],
+ *              then down tiles [E][H/256][I/256][256 rows][128 B]
+ *   scales_gu: [E][I/128][H/256/G_H][256 rows: 128 gate, 128 up][8 G_H B]
+ *   scales_d:  [E][H/256][I/256/G_I][256 rows][8 G_I B]
+ * where rows are in order within a tile, a code row holds the 128 bytes of its matrix
+ * row at K offset 256 st, and G_K (256-K stages per scale group) is the largest of 8, 6,
+ * 4, 2 that divides K/256.  The packed buffer has exactly the bytes of the canonical one
+ * plus section padding.  moe_mxfp4_packed_bytes reports its size for (H, I, E);
+ * moe_mxfp4_pack fills it from a layer's canonical pointers (device memory,
+ * caller-owned; asynchronous on stream; the source must stay unchanged until the copy
+ * has run).  Both return MOE_ERR_UNSUPPORTED when H or I is not a multiple of 512,
+ * MOE_ERR_INVALID_ARG for a bad size or pointer (packed_dev must be 256-byte aligned and
+ * packed_bytes at least the reported size). */
+int moe_mxfp4_packed_bytes(int32_t hidden, int32_t inter, int32_t num_experts, size_t* bytes);
+int moe_mxfp4_pack(int32_t hidden, int32_t inter, int32_t num_experts, const moe_mxfp4_layer* layer,
+                   void* packed_dev, size_t packed_bytes, void* stream);
 
 /* MXFP4 conversion of an fp32 matrix w_dev [rows, cols] (cols a multiple of 32)
  * into nibbles q_dev [rows, cols/2] and E8M0 scales s_dev [rows, cols/32], by the

@@ -40,6 +40,8 @@ EXPORTED = (
     "moe_mxfp4_quantize",
     "moe_mxfp4_forward_static",
     "moe_mxfp4_accept",
+    "moe_mxfp4_packed_bytes",
+    "moe_mxfp4_pack",
 )
 
 MOE_MXFP4_STATIC_WORKSPACE_BYTES = 16 << 20
@@ -73,6 +75,7 @@ class moe_mxfp4_layer(ctypes.Structure):
         ("down_q_dev", ctypes.c_void_p),
         ("down_s_dev", ctypes.c_void_p),
         ("norm_w_dev", ctypes.c_void_p),
+        ("packed_dev", ctypes.c_void_p),
     ]
 
 
@@ -122,6 +125,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_mxfp4_forward_static.restype = ctypes.c_int
     lib.moe_mxfp4_accept.argtypes = [P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, P, P, P, P]
     lib.moe_mxfp4_accept.restype = ctypes.c_int
+    lib.moe_mxfp4_packed_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_mxfp4_packed_bytes.restype = ctypes.c_int
+    lib.moe_mxfp4_pack.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(moe_mxfp4_layer),
+                                   P, ctypes.c_size_t, P]
+    lib.moe_mxfp4_pack.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -188,7 +197,42 @@ def moe_mxfp4_forward_static(handle, x_ptr, num_tokens, y_ptr, stream_ptr) -> in
     return load_library().moe_mxfp4_forward_static(handle, x_ptr, num_tokens, y_ptr, stream_ptr)
 
 
+def moe_mxfp4_packed_bytes(hidden, inter, num_experts) -> tuple[int, int]:
+    n = ctypes.c_size_t()
+    st = load_library().moe_mxfp4_packed_bytes(hidden, inter, num_experts, ctypes.byref(n))
+    return st, n.value
+
+
+def moe_mxfp4_pack(hidden, inter, num_experts, layer: moe_mxfp4_layer, packed_ptr, packed_bytes, stream_ptr) -> int:
+    return load_library().moe_mxfp4_pack(hidden, inter, num_experts, ctypes.byref(layer), packed_ptr, packed_bytes,
+                                         stream_ptr)
+
+
 # ----------------------------------------------------------------------------- torch convenience
+
+
+def _layer_desc(L) -> moe_mxfp4_layer:
+    def p(name):
+        t = L.get(name)
+        return t.data_ptr() if t is not None else None
+    return moe_mxfp4_layer(p("router_w"), p("router_b"), p("gate_q"), p("gate_s"), p("up_q"), p("up_s"),
+                           p("down_q"), p("down_s"), p("norm_w"), p("packed"))
+
+
+def pack(layer: dict, hidden: int, inter: int, num_experts: int, stream=None):
+    """The packed (tile-major) copy of one layer's experts (moe_mxfp4_pack) as a new uint8
+    CUDA tensor; `layer` holds the canonical gate_q .. down_s tensors."""
+    import torch
+    dev = layer["gate_q"].device
+    st_, n = moe_mxfp4_packed_bytes(hidden, inter, num_experts)
+    _check(st_, "moe_mxfp4_packed_bytes")
+    out = torch.empty(n + 256, dtype=torch.uint8, device=dev)
+    off = (-out.data_ptr()) % 256                     # 256-byte aligned view
+    out = out[off:off + n]
+    st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+    canon = {k: v for k, v in layer.items() if k != "packed"}
+    _check(moe_mxfp4_pack(hidden, inter, num_experts, _layer_desc(canon), out.data_ptr(), n, st), "moe_mxfp4_pack")
+    return out
 
 
 def moe_mxfp4_accept(logits_ptr, tokens_ptr, num_streams, block, vocab, target_ptr, accepted_ptr,
@@ -227,7 +271,8 @@ class MoeLayers:
     """Owns a handle over caller-provided device tensors (kept alive here).
 
     layers: list of dicts with router_w (bf16 [E,H]), router_b (fp32 [E] or None),
-    gate_q/gate_s/up_q/up_s/down_q/down_s (uint8) and norm_w (bf16 [H] or None).
+    gate_q/gate_s/up_q/up_s/down_q/down_s (uint8), norm_w (bf16 [H] or None) and
+    optionally packed (the layer's experts in the packed layout, see pack()).
     """
 
     def __init__(self, *, hidden, inter, num_experts, top_k, max_tokens, layers, flags=0, rms_eps=1e-6,
@@ -235,13 +280,7 @@ class MoeLayers:
         self._keep = layers
         self.cfg = moe_mxfp4_config(len(layers), hidden, inter, num_experts, top_k, max_tokens, rms_eps, flags,
                                     expert_begin, expert_end, dense_threshold, timeout_us)
-        descs = []
-        for L in layers:
-            def p(name, L=L):
-                t = L.get(name)
-                return t.data_ptr() if t is not None else None
-            descs.append(moe_mxfp4_layer(p("router_w"), p("router_b"), p("gate_q"), p("gate_s"), p("up_q"),
-                                         p("up_s"), p("down_q"), p("down_s"), p("norm_w")))
+        descs = [_layer_desc(L) for L in layers]
         self.handle = None
         st, h = moe_mxfp4_create(self.cfg, descs)
         _check(st, "moe_mxfp4_create")

@@ -51,6 +51,11 @@ constexpr int kTcThreads = 512;            // 16 warps
 // warp roles: epilogue warps are those of lane quarters 0 and 1 (warp % 4 < 2)
 constexpr int kTcWarpProducer = 2, kTcWarpMma = 3;
 __device__ __forceinline__ bool tc_is_sf_warp(int w) { return w == 6 || w == 7 || w == 10; }
+// activation loaders (warps 11, 14, 15): the gate/up stages' activation rows and scales of
+// blocks whose operand is read per token (not gathered per chunk); loader j serves the
+// ring positions it with it % 3 == j
+__device__ __forceinline__ int tc_loader_index(int w) { return w == 11 ? 0 : w == 14 ? 1 : w == 15 ? 2 : -1; }
+constexpr int kTcLoaders = 3;
 __device__ __forceinline__ bool tc_is_epi_warp(int w) { return (w & 3) < 2; }
 constexpr int kTcEpiWarps = 8;
 constexpr int kTcSfWarps = 3;
@@ -96,9 +101,21 @@ __host__ __device__ constexpr int scale_box_width(int K) {
     return w;
 }
 
+// Tensor maps of one layer's experts.  Canonical layout: codes uint8 [rows, K/2], box
+// {128 B, 128 rows}, 128-byte swizzle (two boxes per stage); scales uint8 [rows, K/32],
+// box {scale_box_width(K) B, 128 rows} (two boxes per scale group).  Packed layout
+// (pack.cuh): gate_q maps the whole code region as rows of 128 B, box {128 B, 256 rows}
+// with 128-byte swizzle (one stage, 32 contiguous KB); gate_s / down_s map the gate/up
+// and the down scale regions as rows of 128 B, box {128 B, 2 scale_box_width(K) rows}
+// (one scale group of 256 weight rows, contiguous); up_q, down_q and up_s are unused.
+// Both layouts put the same bytes in the same places in shared memory, except that a
+// packed scale group holds its second 128 rows right after the first (at +128 sw bytes
+// instead of +kScaleBox1).
 struct TcMaps {
-    CUtensorMap gate_q, up_q, down_q;   // uint8 [rows, K/2], box {128 B, 128 rows}, 128-byte swizzle
-    CUtensorMap gate_s, up_s, down_s;   // uint8 [rows, K/32], box {scale_box_width(K) B, 128 rows}
+    CUtensorMap gate_q, up_q, down_q;
+    CUtensorMap gate_s, up_s, down_s;
+    int packed;
+    int down_row0;   // packed: first 128-byte row of the down tiles in the code region
 };
 
 struct TcArgs {
@@ -136,6 +153,8 @@ struct TcSlotMeta {
     int sc_w;       // box row width (bytes)
     int sc_last;    // last stage reading that pair
     int pad;
+    int s1off;      // byte offset of the second 128 weight rows' scales in the entry
+    int ri;         // item ring entry of the stage's item (its tokens)
 };
 
 struct TcItemInfo {
@@ -189,7 +208,7 @@ static_assert(640 + kItemRing * sizeof(TcItemInfo) + sizeof(RouteTable) + 64 * s
 // One thread initialises the barriers; then the block synchronises.
 __device__ __forceinline__ void tc_smem_init(const TcSmem& s) {
     for (int i = 0; i < kTcStages; ++i) {
-        mbar_init(&s.full[i], 1);
+        mbar_init(&s.full[i], 2);   // the producer (expect_tx) and the stage's activation loader
         mbar_init(&s.empty[i], 1);
     }
     mbar_init(s.accf, 1);
@@ -199,7 +218,7 @@ __device__ __forceinline__ void tc_smem_init(const TcSmem& s) {
         mbar_init(&s.ringe[i], kTcEpiWarps);
     }
     for (int i = 0; i < kTcScaleRing; ++i) {
-        mbar_init(&s.sfull[i], 1);
+        mbar_init(&s.sfull[i], 2);   // the producer (expect_tx) and the group's activation loader
         mbar_init(&s.sempty[i], kTcSfWarps);
     }
     mbar_init(s.epib, kTcEpiWarps);
@@ -329,20 +348,12 @@ struct TcRoleState {
     uint32_t eb;    // epilogue barrier uses
 };
 
-// L2 prefetch distance of the producer, in stages (32 KB of weights each), along the
-// sequence of the items it claims.  Off by default: measured on GB300 with the large
-// layer, every distance from 3 to 16 stages made the expert phase slower (the
-// producer thread spends its time issuing prefetches instead of loads).
-#ifndef MOE_PF_STAGES
-#define MOE_PF_STAGES 0
-#endif
-constexpr int kPfStages = MOE_PF_STAGES;
-
 // Where an item's weights live: the two 128-row code boxes of a stage, their scale
 // boxes, and the number of stages per scale-box pair.
 struct TcItemGeom {
     const CUtensorMap *q0, *q1, *s0, *s1;
-    int r0, r1, nk, spb, sw;
+    int r0, r1, nk, spb, sw, packed;
+    int y0, ys0;   // packed: the item's first code row and first scale row (rows of 128 B)
 };
 __device__ __forceinline__ TcItemGeom tc_item_geom(const TcMaps& maps, const ItemRec& it, int H, int I, int wgu,
                                                    int wd) {
@@ -358,22 +369,18 @@ __device__ __forceinline__ TcItemGeom tc_item_geom(const TcMaps& maps, const Ite
     g.nk = gu ? H / kTcKS : I / kTcKS;
     g.sw = gu ? wgu : wd;
     g.spb = g.sw / 8;
+    g.packed = maps.packed;
+    // packed: item (e, row block rb) owns nk consecutive 32 KB code tiles (256 rows of 128
+    // B each) and nk / spb consecutive scale groups (2 sw rows of 128 B each)
+    const int blk = gu ? it.e * (I / kTmaRows) + rb : it.e * (H / kTcN) + rb;
+    g.y0 = (gu ? 0 : maps.down_row0) + blk * g.nk * 256;
+    g.ys0 = blk * (g.nk / g.spb) * 2 * g.sw;
+    if (g.packed) {
+        g.q0 = g.q1 = &maps.gate_q;
+        g.s0 = g.s1 = gu ? &maps.gate_s : &maps.down_s;
+    }
     return g;
 }
-// Prefetches stage st of an item into L2 (its code boxes, and its scale boxes when a
-// new scale-box pair starts there).
-__device__ __forceinline__ void tc_prefetch_stage(const TcItemGeom& g, int st) {
-    tma_prefetch_2d(g.q0, st * 128, g.r0);
-    tma_prefetch_2d(g.q1, st * 128, g.r1);
-#ifndef MOE_PF_SCALES
-#define MOE_PF_SCALES 1
-#endif
-    if (MOE_PF_SCALES && st % g.spb == 0) {
-        tma_prefetch_2d(g.s0, st * 8, g.r0);
-        tma_prefetch_2d(g.s1, st * 8, g.r1);
-    }
-}
-
 // kGathered: the gate/up items' activation operand comes per chunk (xc4 / xcs, one copy
 // per stage and one per scale group) instead of per token and pair.
 template <bool kGathered>
@@ -391,7 +398,6 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
     int next_idx = atomicAdd(a.queue, 1);
     ItemRec next{};
     if (next_idx < n_items) next = a.rt ? table_item(a.rt, next_idx, rbu, rbd) : load_item(a.items + next_idx);
-    int pf_next = 0;   // leading stages of the next item already prefetched
     const uint64_t pol = l2_evict_first_policy();
     for (;;) {
         const int idx = next_idx;
@@ -422,7 +428,7 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
         if (end) {
             const int slot = rs.it % kTcStages;
             if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
-            s.meta[slot] = TcSlotMeta{-1, 0, 1, 0, 0, 0, 0, 0};
+            s.meta[slot] = TcSlotMeta{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};   // its loader adds the second arrival
             mbar_arrive(&s.claim[slot]);
             mbar_arrive(&s.full[slot]);
             ++rs.it;
@@ -440,10 +446,6 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
         const int r0 = g.r0, r1 = g.r1;
         const int sw = g.sw;                           // scale box width (bytes)
         const int spb = g.spb;                         // stages per scale-box pair
-        const bool has_next = next_idx < n_items;
-        const TcItemGeom gn = tc_item_geom(maps, next, H, I, wgu, wd);
-        for (int q = pf_next; q < min(kPfStages, nk); ++q) tc_prefetch_stage(g, q);   // not yet prefetched
-        pf_next = 0;
         bool h_ready = gu;
         for (int st = 0; st < nk; ++st) {
             if (!h_ready) {
@@ -468,10 +470,14 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                     break;
                 }
                 uint8_t* sdst = s.scales + se * kTcScaleEntry;
-                const bool per_tok = gu && !kGathered;
-                const uint32_t sfa_bytes = per_tok ? (uint32_t)ntok * spb * 64 : (uint32_t)spb * 512;
+                // the activation scales of per-token gate/up stages come from the loaders
+                const uint32_t sfa_bytes = (gu && !kGathered) ? 0u : (uint32_t)spb * 512;
                 mbar_arrive_expect_tx(&s.sfull[se], 2u * (uint32_t)sw * kTmaRows + sfa_bytes);
-                if (cur.pad[0] > 1) {
+                if (g.packed) {   // one contiguous box: both 128-row halves of the group
+                    const int ys = g.ys0 + (st / spb) * 2 * sw;
+                    if (cur.pad[0] > 1) tma_load_2d(sdst, ms0, 0, ys, &s.sfull[se]);
+                    else tma_load_2d_stream(sdst, ms0, 0, ys, &s.sfull[se], pol);
+                } else if (cur.pad[0] > 1) {
                     tma_load_2d(sdst, ms0, st * 8, r0, &s.sfull[se]);
                     tma_load_2d(sdst + kScaleBox1, ms1, st * 8, r1, &s.sfull[se]);
                 } else {
@@ -481,12 +487,7 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                 if (gu && kGathered) {   // the chunk's gathered scales of the group's stages
                     bulk_load(sdst + kScaleSfa, a.xcs + ((size_t)cur.chunk * (H / kTcKS) + st) * 512,
                               (uint32_t)spb * 512, &s.sfull[se]);
-                } else if (gu) {   // per pair: the group's stages of its token (contiguous in xsf)
-                    for (int p = 0; p < ntok; ++p)
-                        bulk_load(sdst + kScaleSfa + p * spb * 64,
-                                  a.xsf + ((size_t)cur.tok[p] * (H / kTcKS) + st) * 64, (uint32_t)spb * 64,
-                                  &s.sfull[se]);
-                } else {
+                } else if (!gu) {
                     bulk_load(sdst + kScaleSfa, a.hsf + ((size_t)cur.chunk * (I / kTcKS) + st) * 512,
                               (uint32_t)spb * 512, &s.sfull[se]);
                 }
@@ -494,36 +495,29 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
             }
             const int slot = rs.it % kTcStages;
             if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
-            s.meta[slot] = TcSlotMeta{kind, st, nk, (int)rs.sc - 1, (st % spb) * 8, sw, st % spb == spb - 1 ? 1 : 0, spb};
+            s.meta[slot] = TcSlotMeta{kind,  st, nk, (int)rs.sc - 1, (st % spb) * 8, sw, st % spb == spb - 1 ? 1 : 0,
+                                      spb,   g.packed ? kTmaRows * sw : kScaleBox1, (int)((rs.n - 1) % kItemRing)};
             mbar_arrive(&s.claim[slot]);   // the scale-factor warps may prepare this slot now
-            const uint32_t abytes = (gu && !kGathered) ? (uint32_t)ntok * 1024 : 8192u;
+            const uint32_t abytes = (gu && !kGathered) ? 0u : 8192u;   // per-token rows: the loaders
             mbar_arrive_expect_tx(&s.full[slot], 2 * 16384 + abytes);
             tc_trace(a, 0, rs.it);
             ++rs.it;   // this slot now has copies in flight
             uint8_t* dst = s.slots + (size_t)slot * kTcSlotBytes;
-            if (cur.pad[0] > 1) {   // rows shared by several chunks: kept in L2 for the other chunks
+            // rows shared by several chunks (pad[0] > 1) keep the normal L2 policy: the other
+            // chunks read them again from L2
+            if (g.packed) {   // one contiguous 32 KB box: the stage's 256 weight rows
+                if (cur.pad[0] > 1) tma_load_2d(dst + kSlotB, mq0, 0, g.y0 + st * 256, &s.full[slot]);
+                else tma_load_2d_stream(dst + kSlotB, mq0, 0, g.y0 + st * 256, &s.full[slot], pol);
+            } else if (cur.pad[0] > 1) {
                 tma_load_2d(dst + kSlotB, mq0, st * 128, r0, &s.full[slot]);
                 tma_load_2d(dst + kSlotB + 16384, mq1, st * 128, r1, &s.full[slot]);
             } else {
                 tma_load_2d_stream(dst + kSlotB, mq0, st * 128, r0, &s.full[slot], pol);
                 tma_load_2d_stream(dst + kSlotB + 16384, mq1, st * 128, r1, &s.full[slot], pol);
             }
-            if (kPfStages > 0) {   // kPfStages ahead into L2: later in this item, else the start of the next one
-                const int ps = st + kPfStages;
-                if (ps < nk) {
-                    tc_prefetch_stage(g, ps);
-                } else if (has_next) {
-                    for (; pf_next <= ps - nk && pf_next < gn.nk; ++pf_next) tc_prefetch_stage(gn, pf_next);
-                }
-            }
             if (gu && kGathered) {
                 bulk_load(dst + kSlotA, a.xc4 + ((size_t)cur.chunk * (H / kTcKS) + st) * 8192, 8192, &s.full[slot]);
-            } else if (gu) {
-                for (int p = 0; p < ntok; ++p) {
-                    const size_t ts = (size_t)cur.tok[p] * (H / kTcKS) + st;
-                    bulk_load(dst + kSlotA + p * 1024, a.xb4 + ts * 1024, 1024, &s.full[slot]);
-                }
-            } else {
+            } else if (!gu) {
                 const size_t cs = (size_t)cur.chunk * (I / kTcKS) + st;
                 bulk_load(dst + kSlotA, a.hb4 + cs * 8192, 8192, &s.full[slot]);
             }
@@ -642,7 +636,7 @@ __device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, uint3
                 uint2 v[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    v[c] = *reinterpret_cast<const uint2*>(ent + w * kScaleBox1 + (32 * c + lane) * m.sc_w + m.sc_off);
+                    v[c] = *reinterpret_cast<const uint2*>(ent + w * m.s1off + (32 * c + lane) * m.sc_w + m.sc_off);
                 uint32_t ff = 0;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -689,6 +683,69 @@ __device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, uint3
         ++rs.it;
         if (m.kind < 0) break;
     }
+    if (failed && lane == 0 && atomicExch(a.abort, 1) == 0) raise_status(a.status, MOE_ERR_TIMEOUT, a.layer * 65536);
+    rs_in = rs;
+    return !failed;
+}
+
+// ---- activation loaders -----------------------------------------------------------
+// The per-token activation operand of a gate/up stage (rows 8p + j of pair p: its
+// token's 8 E2M1 term rows, 1 KB) and, at a scale group's first stage, the group's
+// activation scales (per pair spb x 64 B) are read from global memory with 16-byte
+// cp.async by a whole warp, not by the TMA producer: every CTA reads these few KB of
+// hot L2 lines at about the same time, and as bulk copies they held the producer's
+// queue behind them (about 0.3-0.6 us per 1 KB copy, measured).  The loader of a stage
+// waits for its copies, makes them visible to the tensor cores' proxy and arrives on
+// the stage's full barrier (and the group's scale barrier); for every other stage it
+// arrives at once.  All loaders follow every ring position, so that each one sees the
+// END slot.
+__device__ __noinline__ bool tc_load(const TcArgs& a_in, const TcSmem& s_in, TcRoleState& rs_in, int li, int lane,
+                                     unsigned long long deadline) {
+    const TcArgs a = a_in;
+    const TcSmem s = s_in;
+    TcRoleState rs = rs_in;
+    const int nst = a.H / kTcKS;
+    bool failed = false;
+    for (;;) {
+        const int slot = rs.it % kTcStages;
+        if (!warp_wait_phase(&s.claim[slot], (rs.it / kTcStages) & 1, deadline, a.abort)) { failed = true; break; }
+        const TcSlotMeta m = s.meta[slot];
+        const bool mine = (int)(rs.it % kTcLoaders) == li;
+        ++rs.it;
+        if (!mine) {
+            if (m.kind < 0) break;
+            continue;
+        }
+        const bool first = m.kind >= 0 && m.sc_off == 0;   // the first stage of a scale group
+        if (m.kind == kItemGateUp && !a.xc4) {
+            const TcItemInfo& inf = s.ring[m.ri];
+            const int ntok = inf.ntok;
+            const uint32_t dst = smem_u32(s.slots + (size_t)slot * kTcSlotBytes + kSlotA);
+            for (int p = 0; p < ntok; ++p) {
+                const uint8_t* src = a.xb4 + ((size_t)inf.ids[p] * nst + m.stage) * 1024;
+                cp_async_16(dst + p * 1024 + lane * 16, src + lane * 16);
+                cp_async_16(dst + p * 1024 + 512 + lane * 16, src + 512 + lane * 16);
+            }
+            if (first) {   // the group's activation scales: per pair spb stages x 64 B, contiguous in xsf
+                const uint32_t sdst = smem_u32(s.scales + (m.sc % kTcScaleRing) * kTcScaleEntry + kScaleSfa);
+                const int per = m.pad * 4;   // 16-byte pieces per pair (spb x 64 B)
+                for (int i = lane; i < ntok * per; i += 32) {
+                    const int p = i / per, q = i % per;
+                    cp_async_16(sdst + p * m.pad * 64 + q * 16,
+                                a.xsf + ((size_t)inf.ids[p] * nst + m.stage) * 64 + q * 16);
+                }
+            }
+            cp_async_wait_all();
+            fence_proxy_async_shared();   // read next by the tensor cores (and tcgen05.cp)
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&s.full[slot]);
+            if (first) mbar_arrive(&s.sfull[m.sc % kTcScaleRing]);
+        }
+        if (m.kind < 0) break;
+    }
+    cp_async_wait_all();
     if (failed && lane == 0 && atomicExch(a.abort, 1) == 0) raise_status(a.status, MOE_ERR_TIMEOUT, a.layer * 65536);
     rs_in = rs;
     return !failed;
@@ -855,6 +912,8 @@ __device__ __forceinline__ void tc_phase(const TcMaps& maps, const TcArgs& a, co
         if (lane == 0) tc_mma(a, s, tmem, rs, deadline);
     } else if (tc_is_sf_warp(warp)) {
         tc_sf<kGathered>(a, s, tmem, rs, (warp == 6) ? 0 : (warp == 7) ? 1 : 2, lane, deadline);
+    } else if (tc_loader_index(warp) >= 0) {
+        tc_load(a, s, rs, tc_loader_index(warp), lane, deadline);
     } else if (tc_is_epi_warp(warp)) {
         tc_epilogue(a, s, tmem, rs, warp, lane, deadline);
     }

@@ -15,6 +15,7 @@
 #include "expert_simple.cuh"
 #include "expert_tc.cuh"
 #include "layer_ops.cuh"
+#include "pack.cuh"
 #include "persist.cuh"
 #include "route.cuh"
 
@@ -23,6 +24,7 @@ struct moe_mxfp4_handle {
     std::vector<moe_mxfp4_layer> layers;
     std::vector<moe::TcMaps> maps;    // per layer, when the tensor-core expert path applies
     bool tma = false;
+    bool packed = false;               // some layer's experts are in the packed layout (tensor-core paths only)
     int persist_grid = 0;              // CTAs of the persistent forward (one per SM), 0 = unavailable
     int device = 0;
     int sm_count = 0;
@@ -113,9 +115,13 @@ bool is_device_ptr(const void* p) {
 }
 
 int check_layer(const moe_mxfp4_config& c, const moe_mxfp4_layer& l) {
-    const void* req[] = {l.router_w_dev, l.gate_q_dev, l.gate_s_dev, l.up_q_dev, l.up_s_dev, l.down_q_dev, l.down_s_dev};
-    for (const void* p : req)
-        if (!p || !aligned16(p) || !is_device_ptr(p)) return MOE_ERR_INVALID_ARG;
+    if (!l.router_w_dev || !aligned16(l.router_w_dev) || !is_device_ptr(l.router_w_dev)) return MOE_ERR_INVALID_ARG;
+    // the experts: the canonical pointers, or the packed buffer (then the canonical ones may be NULL)
+    const void* experts[] = {l.gate_q_dev, l.gate_s_dev, l.up_q_dev, l.up_s_dev, l.down_q_dev, l.down_s_dev};
+    for (const void* p : experts)
+        if (l.packed_dev ? (p && !aligned16(p)) : (!p || !aligned16(p) || !is_device_ptr(p))) return MOE_ERR_INVALID_ARG;
+    if (l.packed_dev && ((reinterpret_cast<uintptr_t>(l.packed_dev) & 255) || !is_device_ptr(l.packed_dev)))
+        return MOE_ERR_INVALID_ARG;
     if (l.router_b_dev && ((reinterpret_cast<uintptr_t>(l.router_b_dev) & 3) || !is_device_ptr(l.router_b_dev)))
         return MOE_ERR_INVALID_ARG;
     if (c.flags & MOE_FLAG_NORM) {
@@ -137,13 +143,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 2D uint8 tensor [rows, row_bytes] with boxes of box_x bytes x 128 rows.
-bool encode_2d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_x, bool swizzle) {
+// 2D uint8 tensor [rows, row_bytes] with boxes of box_x bytes x box_y rows.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_x, bool swizzle,
+               uint32_t box_y = moe::kTmaRows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {row_bytes, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_x, (cuuint32_t)moe::kTmaRows};
+    const cuuint32_t box[2] = {box_x, box_y};
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -155,6 +162,19 @@ bool make_maps(const moe_mxfp4_config& c, const moe_mxfp4_layer& l, moe::TcMaps*
     // codes: [128 B x 128 rows] boxes (one 256-element stage), 128-byte swizzle;
     // scales: boxes of scale_box_width(K) bytes (several stages) x 128 rows
     const uint32_t wh = moe::scale_box_width((int)H), wi = moe::scale_box_width((int)I);
+    m->packed = l.packed_dev ? 1 : 0;
+    m->down_row0 = 0;
+    if (l.packed_dev) {   // tile-major sections (pack.cuh): one box = one contiguous stage or scale group
+        const moe::PackLayout P = moe::pack_layout((int)H, (int)I, (int)E);
+        const uint8_t* b = l.packed_dev;
+        m->down_row0 = (int)(P.down_codes / 128);
+        const bool ok = encode_2d(&m->gate_q, b + P.codes, 128, (P.scales_gu - P.codes) / 128, 128, true, 256) &&
+                        encode_2d(&m->gate_s, b + P.scales_gu, 128, 2 * E * I * (H / 32) / 128, 128, false, 2 * wh) &&
+                        encode_2d(&m->down_s, b + P.scales_d, 128, E * H * (I / 32) / 128, 128, false, 2 * wi);
+        m->up_q = m->down_q = m->gate_q;   // unused with the packed layout; valid maps all the same
+        m->up_s = m->gate_s;
+        return ok;
+    }
     return encode_2d(&m->gate_q, l.gate_q_dev, H / 2, E * I, 128, true) &&
            encode_2d(&m->up_q, l.up_q_dev, H / 2, E * I, 128, true) &&
            encode_2d(&m->down_q, l.down_q_dev, I / 2, E * H, 128, true) &&
@@ -464,10 +484,13 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
         cudaSuccess)
         return MOE_ERR_CUDA;
 
+    bool any_packed = false;
+    for (int l = 0; l < c.num_layers; ++l) any_packed |= layers[l].packed_dev != nullptr;
+    // the tensor-core expert path takes K = H and K = I in 256-element stages whose
+    // scale boxes are multiples of 16 bytes (K a multiple of 512); packed experts need it
+    if (any_packed && ((c.hidden % 512) || (c.inter % 512))) return MOE_ERR_UNSUPPORTED;
     moe_mxfp4_handle* h = new (std::nothrow) moe_mxfp4_handle();
     if (!h) return MOE_ERR_INVALID_ARG;
-    // the tensor-core expert path takes K = H and K = I in 256-element stages whose
-    // scale boxes are multiples of 16 bytes (K a multiple of 512)
     h->tma = (c.hidden % 512 == 0) && (c.inter % 512 == 0);
     if (h->tma) {
         h->maps.resize(c.num_layers);
@@ -496,6 +519,11 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
         }
         cudaGetLastError();
     }
+    if (any_packed && !h->tma) {   // packed experts are read by the tensor-core paths only
+        delete h;
+        return MOE_ERR_CUDA;
+    }
+    h->packed = any_packed;
     h->cfg = c;
     if (h->cfg.timeout_us == 0) h->cfg.timeout_us = kDefaultTimeoutUs;
     h->layers.assign(layers, layers + c.num_layers);
@@ -523,6 +551,8 @@ int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens
         return MOE_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace_dev);
+    const bool tma_fits = num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok;
+    if (h->packed && !tma_fits) return MOE_ERR_UNSUPPORTED;   // the fallback path reads canonical experts
     // the TMA work-item code holds up to 512 token chunks of 8 per expert
     if (h->tma && num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok) {
         const bool events = dbg && dbg->expert_events;

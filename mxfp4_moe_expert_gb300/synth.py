@@ -8,7 +8,9 @@ is the routing-margin condition that the workload definition puts on the
 inputs ("router ... so the top-k logit margin is at least 1e-3"): rows of x are
 re-drawn until the gaps between the top-(k+1) router logits, computed with a
 library fp64 matmul, are all at least ``margin``.  That only *selects* inputs;
-both the CUDA path and the oracle receive the same selected tensors.
+both the CUDA path and the oracle receive the same selected tensors.  A caller
+may add its own condition on a row (``make_inputs(accept_row=...)``), bringing
+whatever arithmetic that condition needs.
 
 Workloads (one MoE verify block of T tokens; page 3 "DFlash: block-level
 masked parallel draft" fixes 8 positions per stream):
@@ -84,6 +86,10 @@ class Workload:
     margin: float = 1e-3
     rms_eps: float = 1e-6
     zipf_s: float = 1.1
+    # > 0: every element of x is also multiplied by 2^u, u a uniform integer in
+    # [-x_spread, x_spread] (drawn from the row's stream after the normal values), so
+    # that one 32-element block of x spans up to 2^(2 x_spread) in magnitude
+    x_spread: int = 0
 
     @property
     def expert_bytes(self) -> int:
@@ -159,8 +165,24 @@ def _row_ok(logits_row: torch.Tensor, k: int, margin: float) -> bool:
     return bool(torch.all(top[:-1] - top[1:] >= margin))
 
 
-def make_inputs(wl: Workload, max_attempts: int = 64) -> Inputs:
-    """Draw x, router and norm weights (all on CPU) for a workload."""
+def _draw_row(wl: Workload, t: int, attempt: int) -> torch.Tensor:
+    """Row t of x, attempt `attempt`: N(0, 1) values (times 2^u with x_spread), bf16 (RNE)."""
+    g = _gen(derive_seed(wl.seed, "x", 0, t, attempt), "cpu")
+    row = torch.randn(wl.H, generator=g, dtype=torch.float64)
+    if wl.x_spread > 0:
+        u = torch.randint(-wl.x_spread, wl.x_spread + 1, (wl.H,), generator=g, dtype=torch.int64)
+        row = row * torch.exp2(u.to(torch.float64))
+    return row.to(torch.bfloat16)
+
+
+def make_inputs(wl: Workload, max_attempts: int = 64, accept_row=None) -> Inputs:
+    """Draw x, router and norm weights (all on CPU) for a workload.
+
+    accept_row(t, row) -> bool, when given, is a further condition on row t of x
+    (bf16 [H]) after the first-layer margin rule: a row it rejects is re-drawn like
+    one that fails the margin rule.  The caller brings the arithmetic it needs (for
+    example the margins of every layer of a stack along a reference trajectory);
+    this module only draws and selects."""
     layers = []
     for l in range(wl.layers):
         g = _gen(derive_seed(wl.seed, "router_w", l), "cpu")
@@ -181,9 +203,8 @@ def make_inputs(wl: Workload, max_attempts: int = 64) -> Inputs:
     rows, redraws = [], {}
     for t in range(wl.T):
         for a in range(max_attempts):
-            g = _gen(derive_seed(wl.seed, "x", 0, t, a), "cpu")
-            row = torch.randn(wl.H, generator=g, dtype=torch.float64).to(torch.bfloat16)
-            if wl.margin <= 0:
+            row = _draw_row(wl, t, a)
+            if wl.margin <= 0 and accept_row is None:
                 break
             xin = row.to(torch.float64)
             if wl.norm:
@@ -191,7 +212,8 @@ def make_inputs(wl: Workload, max_attempts: int = 64) -> Inputs:
                 # rescales per element, so evaluate it with a library routine.
                 xin = torch.nn.functional.rms_norm(xin[None], (wl.H,), layers[0].norm_w.to(torch.float64),
                                                    eps=wl.rms_eps)[0]
-            if _row_ok(xin @ wr0.T + b0, wl.k, wl.margin):
+            if (wl.margin <= 0 or _row_ok(xin @ wr0.T + b0, wl.k, wl.margin)) and \
+                    (accept_row is None or accept_row(t, row)):
                 break
         else:
             raise RuntimeError(f"margin rule failed for token {t} after {max_attempts} draws")

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import torch
 
+from . import pack as _pack
 from . import quantize as _cuda_quantize
 from .synth import Inputs, Workload, expert_weight, make_inputs
 
@@ -24,11 +25,14 @@ def alloc_layer(wl: Workload, device) -> dict:
 
 
 def device_layers(wl: Workload, inputs: Inputs | None = None, device="cuda", weights_device=None,
-                  quantizer=None) -> tuple[Inputs, list]:
+                  quantizer=None, packed=False) -> tuple[Inputs, list]:
     """Returns (inputs, layers): layers[l] is a dict of device tensors accepted by MoeLayers.
 
     weights_device: where the fp32 master weights are drawn (default: `device`).
     quantizer(w_fp32) -> (q, s) tensors; default: the library's CUDA kernel.
+    packed: also add each layer's experts in the packed layout (layers[l]["packed"],
+    made by moe_mxfp4_pack from the canonical tensors, which stay in the dict); the
+    forward then streams the experts from the packed copy.
     """
     inputs = inputs or make_inputs(wl)
     weights_device = weights_device or device
@@ -49,6 +53,8 @@ def device_layers(wl: Workload, inputs: Inputs | None = None, device="cuda", wei
         L["router_w"] = lt.router_w.to(device).contiguous()
         L["router_b"] = lt.router_b.to(device).contiguous()
         L["norm_w"] = lt.norm_w.to(device).contiguous() if lt.norm_w is not None else None
+        if packed:
+            L["packed"] = _pack(L, wl.H, wl.I, wl.E)
         layers.append(L)
     return inputs, layers
 
@@ -64,3 +70,11 @@ def touched_bytes(wl: Workload, counts_per_layer) -> int:
             total += wl.H * 2
     total += wl.T * wl.H * (2 + 4)
     return total
+
+
+def repack(layers: list, wl: Workload) -> None:
+    """(Re)makes layers[l]["packed"] from the canonical tensors of every layer (after
+    the caller changed some expert bytes)."""
+    for L in layers:
+        L.pop("packed", None)
+        L["packed"] = _pack(L, wl.H, wl.I, wl.E)

@@ -7,7 +7,9 @@ oracle.  Routing indices and the token-expert grouping are compared bit-exact.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import json
+import multiprocessing
 import os
 
 import numpy as np
@@ -86,3 +88,68 @@ def oracle_layer_args(inputs: Inputs, layer: int):
     b = L.router_b.double().numpy()
     nw = bf16_np(L.norm_w) if L.norm_w is not None else None
     return wr, b, nw
+
+
+# ---- the oracle's encoding of many experts, in parallel -----------------------------
+
+
+def _worker_init():
+    torch.set_num_threads(1)
+
+
+def _oracle_matrix_bytes(task):
+    """Worker: one expert matrix drawn on the CPU and MXFP4-encoded by the oracle."""
+    wl, layer, e, m = task
+    q, s = O.quantize(expert_weight(wl, layer, e, m, "cpu").numpy())
+    return layer, e, m, q, s
+
+
+class OracleExpertBank:
+    """The oracle's bytes of a workload's experts: fp32 master weights drawn by the
+    generator on the CPU and encoded by oracle.quantize, one matrix per task in a pool of
+    spawned processes (safe whether or not this process has touched the GPU); cached per
+    (layer, expert).  The GPU side receives these same bytes (upload), so the library's
+    quantizer plays no part in the comparison."""
+
+    MATRICES = ("gate", "up", "down")
+
+    def __init__(self, wl: Workload, workers: int | None = None):
+        self.wl = wl
+        self.cache = {}
+        n = workers or max(1, min(48, os.cpu_count() or 1))
+        self.pool = concurrent.futures.ProcessPoolExecutor(
+            n, mp_context=multiprocessing.get_context("spawn"), initializer=_worker_init)
+
+    def ensure(self, layer: int, experts) -> None:
+        todo = sorted({int(e) for e in np.asarray(experts).reshape(-1)} - {e for (l, e) in self.cache if l == layer})
+        tasks = [(self.wl, layer, e, m) for e in todo for m in self.MATRICES]
+        got = {}
+        for l, e, m, q, s in self.pool.map(_oracle_matrix_bytes, tasks, chunksize=1):
+            got.setdefault(e, {})[m] = (q, s)
+        for e, d in got.items():
+            self.cache[(layer, e)] = d
+
+    def expert_fn(self, layer: int):
+        """expert_fn for the oracle's layer functions."""
+        def fn(e):
+            self.ensure(layer, [e])
+            d = self.cache[(layer, int(e))]
+            return O.ExpertMatrices(*d["gate"], *d["up"], *d["down"])
+        return fn
+
+    def upload(self, layer_tensors: dict, layer: int) -> int:
+        """Writes every cached expert of `layer` into a device layer (dict of [E, ...]
+        tensors); returns how many experts were written."""
+        n = 0
+        for (l, e), d in self.cache.items():
+            if l != layer:
+                continue
+            for m in self.MATRICES:
+                q, s = d[m]
+                layer_tensors[m + "_q"][e].copy_(torch.from_numpy(q))
+                layer_tensors[m + "_s"][e].copy_(torch.from_numpy(s))
+            n += 1
+        return n
+
+    def close(self):
+        self.pool.shutdown(cancel_futures=True)

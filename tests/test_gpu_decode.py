@@ -48,8 +48,10 @@ def _crafted_bytes(wl):
     return out
 
 
-@pytest.mark.parametrize("flags", [0, pkg.MOE_FLAG_MULTI_KERNEL], ids=["persistent", "multi_kernel"])
-def test_every_weight_byte_decodes_as_the_format_defines(flags):
+@pytest.mark.parametrize("flags,packed", [(0, False), (pkg.MOE_FLAG_MULTI_KERNEL, False), (0, True),
+                                          (pkg.MOE_FLAG_MULTI_KERNEL, True)],
+                         ids=["persistent", "multi_kernel", "persistent_packed", "multi_kernel_packed"])
+def test_every_weight_byte_decodes_as_the_format_defines(flags, packed):
     wl = WL
     assert (wl.H // 2) == 256 and (wl.I // 2) == 256   # one full byte cycle per row
     inputs = make_inputs(wl)
@@ -65,6 +67,10 @@ def test_every_weight_byte_decodes_as_the_format_defines(flags):
     L["router_w"] = lt.router_w.to(DEV).contiguous()
     L["router_b"] = lt.router_b.to(DEV).contiguous()
     L["norm_w"] = None
+    if packed:   # the experts are read from the packed copy only
+        L["packed"] = pkg.pack(L, wl.H, wl.I, wl.E)
+        for m in ("gate", "up", "down"):
+            L[m + "_q"] = L[m + "_s"] = None
     moe = pkg.MoeLayers(hidden=wl.H, inter=wl.I, num_experts=wl.E, top_k=wl.k, max_tokens=wl.T, layers=[L],
                         flags=flags)
     bufs, dbg = moe.debug_buffers(wl.T)
@@ -79,3 +85,49 @@ def test_every_weight_byte_decodes_as_the_format_defines(flags):
     assert np.array_equal(bufs["perm"][0].cpu().numpy(), ref["perm"])
     assert_rows_close(y.double().cpu().numpy(), ref["y"], what="all bytes")
     moe.close()
+
+
+def test_packed_layout_is_the_documented_tile_order():
+    """moe_mxfp4_pack against the layout stated in include/moe_mxfp4.h, rebuilt here with
+    numpy from random canonical bytes: code tiles of 256 rows x 128 B (gate rows then the
+    same up rows, or 256 down rows) per 256-K stage, scale groups of 256 rows x 8 G B,
+    three 256-byte-aligned sections."""
+    wl = Workload("pack", T=1, H=1536, I=1024, E=3, k=1, seed=0)
+    rng = np.random.default_rng(3)
+    L, canon = {}, {}
+    for m, (rows, K) in {"gate": (wl.I, wl.H), "up": (wl.I, wl.H), "down": (wl.H, wl.I)}.items():
+        q = rng.integers(0, 256, size=(wl.E, rows, K // 2), dtype=np.uint8)
+        sc = rng.integers(0, 255, size=(wl.E, rows, K // 32), dtype=np.uint8)
+        canon[m] = (q, sc)
+        L[m + "_q"] = torch.from_numpy(q).to(DEV)
+        L[m + "_s"] = torch.from_numpy(sc).to(DEV)
+    got = pkg.pack(L, wl.H, wl.I, wl.E).cpu().numpy()
+    E, H, I = wl.E, wl.H, wl.I
+
+    def group(K):
+        return next(g for g in (8, 6, 4, 2) if (K // 256) % g == 0)
+
+    def tiles(a, b, K, width):
+        """[E, rows, K/width] canonical -> [E][blocks][K/width/w][256 rows][w] with w = 128 (codes)
+        or 8 G (scales); a and b give rows 0..127 and 128..255 of a tile (gate / up), or b is
+        None and a tile is 256 consecutive rows of a."""
+        w = 128 if width == 2 else 8 * group(K)
+        cols = a.shape[2]
+        if b is None:
+            t = a.reshape(E, a.shape[1] // 256, 256, cols // w, w)
+        else:
+            t = np.stack([a.reshape(E, a.shape[1] // 128, 128, cols // w, w),
+                          b.reshape(E, b.shape[1] // 128, 128, cols // w, w)], axis=2)
+            t = t.reshape(E, a.shape[1] // 128, 256, cols // w, w)
+        return np.ascontiguousarray(t.transpose(0, 1, 3, 2, 4)).reshape(-1)
+
+    sections = [np.concatenate([tiles(canon["gate"][0], canon["up"][0], H, 2),
+                                tiles(canon["down"][0], None, I, 2)]),
+                tiles(canon["gate"][1], canon["up"][1], H, 32),
+                tiles(canon["down"][1], None, I, 32)]
+    off = 0
+    st, n = pkg.moe_mxfp4_packed_bytes(wl.H, wl.I, wl.E)
+    for sec in sections:
+        assert np.array_equal(got[off:off + sec.size], sec), off
+        off = (off + sec.size + 255) // 256 * 256
+    assert st == pkg.MOE_OK and n == off == got.size

@@ -12,9 +12,10 @@ import torch
 
 import mxfp4_moe_expert_gb300 as pkg
 from mxfp4_moe_expert_gb300.synth import WORKLOADS, Workload, expert_weight, make_inputs
-from mxfp4_moe_expert_gb300.workload import device_layers
+from mxfp4_moe_expert_gb300.workload import device_layers, repack
 from oracle import moe_oracle as O
-from parity_util import (OracleExperts, assert_rows_close, bf16_np, oracle_layer_args, oracle_quantizer_to)
+from parity_util import (OracleExpertBank, OracleExperts, assert_rows_close, bf16_np, oracle_layer_args,
+                         oracle_quantizer_to)
 
 pytestmark = pytest.mark.gpu
 
@@ -130,6 +131,25 @@ def test_layer_parity_full_oracle(wl):
     moe.close()
 
 
+@pytest.mark.parametrize("wl", [w for w in SMALL if w.H % 512 == 0 and w.I % 512 == 0], ids=lambda w: w.name)
+def test_layer_parity_packed_experts(wl):
+    """The same layers with the experts read from the packed copy only (the canonical
+    tensors are dropped from the layer): persistent forward and one-launch-per-phase
+    forward, against the oracle on every row."""
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV),
+                                   packed=True)
+    for m in ("gate", "up", "down"):
+        layers[0][m + "_q"] = layers[0][m + "_s"] = None
+    wr, b, _ = oracle_layer_args(inputs, 0)
+    ref = O.moe_layer(bf16_np(inputs.x), wr, b, wl.k, OracleExperts(wl, 0, "cpu"))
+    for flags in (0, pkg.MOE_FLAG_MULTI_KERNEL):
+        moe = _moe(wl, layers, flags=flags)
+        y, bufs = _run(moe, inputs.x.to(DEV))
+        _check_routing(_dbg_layer(bufs, 0), ref, f"{wl.name} packed flags={flags}")
+        assert_rows_close(y.double().cpu().numpy(), ref["y"], what=f"{wl.name} packed flags={flags}")
+        moe.close()
+
+
 @pytest.mark.parametrize("wl", [
     Workload("stack_small", T=6, H=512, I=256, E=12, k=3, layers=4, norm=True, seed=0x5EED0104),
     Workload("stack_tma", T=7, H=1024, I=512, E=12, k=3, layers=3, norm=True, seed=0x5EED0115),
@@ -150,6 +170,64 @@ def test_stack_parity_small(wl):
         assert min(margins) > 1e-5, (l, min(margins))
         _check_routing(_dbg_layer(bufs, l), ref["layers"][l], f"layer {l}", deep=l > 0)
     assert_rows_close(y.double().cpu().numpy(), ref["y"], what="stack")
+    moe.close()
+
+
+def test_wide_dynamic_range_activations():
+    """Every element of x carries an extra factor 2^u, u uniform in [-20, 20], so one
+    32-element MX block of x spans up to 2^40 in magnitude: the worst case of the
+    expert operand's 8-term E2M1 split, whose terms represent each value relative to
+    its block's maximum (values far below the block maximum are dropped).  The layer
+    output must still meet the output tolerance on every row.  The router logits reach
+    ~1e5 here, where fp32 accumulation moves them by up to ~1, so the margin condition
+    on the input is 16 instead of 1e-3."""
+    wl = Workload("wide_x", T=13, H=1024, I=512, E=16, k=4, seed=0x5EED0119, x_spread=20, margin=16.0)
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    xf = bf16_np(inputs.x)
+    blocks = np.abs(xf).reshape(wl.T, -1, 32)
+    nz = np.where(blocks > 0, blocks, np.nan)
+    assert np.nanmax(np.log2(np.nanmax(nz, axis=2) / np.nanmin(nz, axis=2))) >= 30   # the spread is really there
+    moe = _moe(wl, layers)
+    y, bufs = _run(moe, inputs.x.to(DEV))
+    wr, b, _ = oracle_layer_args(inputs, 0)
+    with np.errstate(over="ignore"):   # silu of very negative gate values: exp overflows to inf, silu -> -0
+        ref = O.moe_layer(xf, wr, b, wl.k, OracleExperts(wl, 0, "cpu"))
+    _check_routing(_dbg_layer(bufs, 0), ref, wl.name)
+    assert_rows_close(y.double().cpu().numpy(), ref["y"], what=wl.name)
+    moe.close()
+
+
+def test_cuda_graph_replay_of_per_phase_forward():
+    """The one-launch-per-phase forward (the comparison path for per-operator execution)
+    captured once in a CUDA graph and replayed: each replay's output matches the fp64
+    oracle, and equals the eagerly launched forward bit for bit."""
+    wl = SMALL[5]
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV))
+    moe = _moe(wl, layers, flags=pkg.MOE_FLAG_MULTI_KERNEL)
+    x = inputs.x.to(DEV)
+    eager = moe.forward(x, check=True)
+    y = torch.empty((wl.T, wl.H), dtype=torch.float32, device=DEV)
+    ws = moe.new_workspace(wl.T)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        moe.forward(x, y, ws, side.cuda_stream)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        moe.forward(x, y, ws, side.cuda_stream)
+    torch.cuda.synchronize()
+    wr, b, _ = oracle_layer_args(inputs, 0)
+    ref = O.moe_layer(bf16_np(inputs.x), wr, b, wl.k, OracleExperts(wl, 0, "cpu"))
+    for replay in range(2):
+        y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pkg.moe_mxfp4_check(moe.handle, ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == pkg.MOE_OK
+        assert torch.equal(y, eager), replay
+        assert_rows_close(y.double().cpu().numpy(), ref["y"], what=f"graph replay {replay}")
+    del graph
     moe.close()
 
 
@@ -242,58 +320,136 @@ def test_empty_and_invalid_calls():
     moe.close()
 
 
-# ----------------------------------------------------------------------------- full sizes, sampled tokens
+# ----------------------------------------------------------------------------- full sizes
+#
+# Oracle first: the routing of the block comes from the oracle; the experts that the
+# checked rows route to are drawn on the CPU and encoded by the oracle's quantizer (in
+# parallel, OracleExpertBank), and exactly those bytes are written into the device layer
+# (whose other experts hold GPU-drawn weights encoded by the library's quantizer: no
+# checked row reads them, and a mis-routed pair would fail the bit-exact routing check
+# first).  The device forward then runs the whole block in the launch configuration the
+# benchmark times.
 
 
-def _full_size(name, sample_tokens):
+def _layer_full_size(name, rows=None, packed=True):
+    """Single layer at full size: routing of every token bit-exact (indices, counts,
+    offsets, perm; gates within 1e-5), and every row in `rows` (default: all) within the
+    output tolerance of the fp64 oracle.  packed: the experts are streamed from the
+    packed copy (the layout the benchmark times)."""
     wl = WORKLOADS[name]
-    inputs, layers = device_layers(wl, device=DEV)          # library quantizer, weights drawn on the GPU
-    moe = _moe(wl, layers)
-    y, bufs = _run(moe, inputs.x.to(DEV))
-    got = y.double().cpu().numpy()
+    inputs = make_inputs(wl)
     xf = bf16_np(inputs.x)
-    if not wl.norm:
-        wr, b, _ = oracle_layer_args(inputs, 0)
-        logits = O.router_logits(xf, wr, b)
-        idx, gate = O.topk_gates(logits, wl.k)
-        counts, offsets, perm = O.assignment(idx, wl.E)
-        _check_routing(_dbg_layer(bufs, 0), dict(idx=idx, gate=gate, counts=counts, offsets=offsets, perm=perm),
-                       name)
-        experts = OracleExperts(wl, 0, DEV, check_against=layers[0])
-        for t in sample_tokens:
-            r = O.moe_token(xf[t], wr, b, wl.k, experts)
-            assert_rows_close(got[t:t + 1], r["y"][None], what=f"{name} token {t}")
-    else:
-        L = []
+    wr, b, _ = oracle_layer_args(inputs, 0)
+    idx, gate = O.topk_gates(O.router_logits(xf, wr, b), wl.k)
+    counts, offsets, perm = O.assignment(idx, wl.E)
+    rows = list(range(wl.T)) if rows is None else sorted(set(int(t) for t in rows))
+    bank = OracleExpertBank(wl)
+    try:
+        bank.ensure(0, idx[rows])
+        _, layers = device_layers(wl, inputs=inputs, device=DEV)
+        assert bank.upload(layers[0], 0) == len(np.unique(idx[rows]))
+        if packed:
+            repack(layers, wl)
+        moe = _moe(wl, layers)
+        y, bufs = _run(moe, inputs.x.to(DEV))
+        _check_routing(_dbg_layer(bufs, 0), dict(idx=idx, gate=gate, counts=counts, offsets=offsets, perm=perm), name)
+        ref = O.moe_layer(xf[rows], wr, b, wl.k, bank.expert_fn(0))
+        assert np.array_equal(ref["idx"], idx[rows])
+        assert_rows_close(y.double().cpu().numpy()[rows], ref["y"], what=f"{name} ({len(rows)} rows)")
+        moe.close()
+        del layers
+    finally:
+        bank.close()
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("packed", [True, False], ids=["packed", "canonical"])
+def test_mid_layer_all_rows(packed):
+    _layer_full_size("mid", packed=packed)
+
+
+def test_large_layer_all_rows():
+    _layer_full_size("large")
+
+
+def batched_rows(wl, idx, n_hot=3, n_total=48, seed=7):
+    """Rows of the 256-token Zipf block to compare: every token of the first and of the
+    last 8-pair chunk of the n_hot most popular experts (the chunks that reuse those
+    experts' weight rows most), tokens 0 and T-1, then seeded random tokens up to n_total."""
+    counts, offsets, perm = O.assignment(idx, wl.E)
+    rows = {0, wl.T - 1}
+    for e in np.argsort(-counts, kind="stable")[:n_hot]:
+        pairs = perm[offsets[e]:offsets[e + 1]]
+        for chunk in (pairs[:8], pairs[-8:]):
+            rows.update(int(p) // wl.k for p in chunk)
+    rng = np.random.default_rng(seed)
+    for t in rng.permutation(wl.T):
+        if len(rows) >= n_total:
+            break
+        rows.add(int(t))
+    return sorted(rows)
+
+
+def test_batched_layer_rows():
+    wl = WORKLOADS["batched"]
+    inputs = make_inputs(wl)
+    wr, b, _ = oracle_layer_args(inputs, 0)
+    idx, _ = O.topk_gates(O.router_logits(bf16_np(inputs.x), wr, b), wl.k)
+    rows = batched_rows(wl, idx)
+    assert len(rows) >= 32
+    _layer_full_size("batched", rows)
+
+
+def stack_inputs_all_layers_conditioned(wl, bank):
+    """The stack's input with every layer's top-(k+1) logit gaps >= wl.margin along the
+    oracle trajectory of every token: a row of x is re-drawn (seeded) until the fp64
+    trajectory of that token through all layers keeps the margin in each layer.  The
+    layer is per token, so each row is decided on its own trajectory."""
+    base = make_inputs(wl)   # router and norm weights do not depend on the rows of x
+    args = [oracle_layer_args(base, l) for l in range(wl.layers)]
+    for l in range(wl.layers):   # every expert of every layer: the trajectories may route anywhere
+        bank.ensure(l, range(wl.E))
+
+    def accept(t, row):
+        r = bf16_np(row)[None]
+        for l, (wr, b, nw) in enumerate(args):
+            n = O.rmsnorm(r, nw, wl.rms_eps)
+            if O.topk_margin(O.router_logits(n, wr, b)[0], wl.k) < wl.margin:
+                return False
+            r = r + O.moe_layer(n, wr, b, wl.k, bank.expert_fn(l))["y"]
+        return True
+
+    return make_inputs(wl, accept_row=accept), args
+
+
+def test_stack_all_tokens_all_layers():
+    """8 layers x 8 tokens at full size: the input conditioned on every layer's margin,
+    then every layer's routing bit-exact for every token and every output row within
+    the tolerance of the fp64 oracle's stack."""
+    wl = WORKLOADS["stack"]
+    bank = OracleExpertBank(wl)
+    try:
+        inputs, args = stack_inputs_all_layers_conditioned(wl, bank)
+        xf = bf16_np(inputs.x)
+        L = [dict(wr=wr, b=b, norm_w=nw, expert_fn=bank.expert_fn(l)) for l, (wr, b, nw) in enumerate(args)]
+        ref = O.moe_stack(xf, L, wl.k, wl.rms_eps)
         for l in range(wl.layers):
-            wr, b, nw = oracle_layer_args(inputs, l)
-            L.append(dict(wr=wr, b=b, norm_w=nw, expert_fn=OracleExperts(wl, l, DEV, check_against=layers[l])))
-        for t in sample_tokens:   # the stack is per token: one token's trajectory needs k experts per layer
-            ref = O.moe_stack(xf[t:t + 1], L, wl.k, wl.rms_eps)
-            for l in range(wl.layers):
-                lr = ref["layers"][l]
-                assert O.topk_margin(lr["logits"][0], wl.k) > 1e-5
-                assert np.array_equal(bufs["topk_idx"][l, t], lr["idx"][0]), (l, t)
-            assert_rows_close(got[t:t + 1], ref["y"], what=f"{name} token {t}")
-    moe.close()
-    del layers
-    torch.cuda.empty_cache()
-
-
-def test_mid_layer_sampled():
-    _full_size("mid", [0, 7])
-
-
-def test_large_layer_sampled():
-    _full_size("large", [2])
-
-
-def test_batched_layer_sampled():
-    _full_size("batched", [0, 255])
-
-
-def test_stack_sampled():
-    _full_size("stack", [1])
+            m = min(O.topk_margin(ref["layers"][l]["logits"][t], wl.k) for t in range(wl.T))
+            assert m >= wl.margin, (l, m)
+        _, layers = device_layers(wl, inputs=inputs, device=DEV)
+        for l in range(wl.layers):
+            bank.upload(layers[l], l)
+        repack(layers, wl)
+        moe = _moe(wl, layers)
+        y, bufs = _run(moe, inputs.x.to(DEV))
+        for l in range(wl.layers):
+            _check_routing(_dbg_layer(bufs, l), ref["layers"][l], f"stack layer {l}", deep=l > 0)
+        assert_rows_close(y.double().cpu().numpy(), ref["y"], what="stack (8 layers, all rows)")
+        moe.close()
+        del layers
+    finally:
+        bank.close()
+        torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("flags", [0, pkg.MOE_FLAG_MULTI_KERNEL], ids=["persistent", "multi_kernel"])

@@ -50,6 +50,29 @@ def test_static_workspace_forward_matches_workspace_forward_twice(layer):
         assert_rows_close(got, ref, what=f"static call {call}")
 
 
+def test_static_workspace_forward_on_a_larger_block_twice():
+    """A block of 24 tokens x top-4 (96 pairs) is routed through the workspace and its
+    input operand is gathered per chunk: the sections of the array that the small
+    block above leaves unused are written and read here, on two calls in a row."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    wl = Workload("no_alloc_larger", T=24, H=1024, I=512, E=12, k=4, seed=0x5EED0201)
+    inputs, layers = device_layers(wl, device="cuda")
+    moe = pkg.MoeLayers(hidden=wl.H, inter=wl.I, num_experts=wl.E, top_k=wl.k, max_tokens=wl.T, layers=layers)
+    assert wl.T * wl.k > 64 and moe.workspace_bytes(wl.T) <= pkg.MOE_MXFP4_STATIC_WORKSPACE_BYTES
+    x = inputs.x.to("cuda")
+    ref = moe.forward(x, check=True).double().cpu().numpy()
+    st = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.float32, device="cuda")
+        status = pkg.moe_mxfp4_forward_static(moe.handle, x.data_ptr(), wl.T, y.data_ptr(), st)
+        assert status == pkg.MOE_OK, pkg.moe_mxfp4_status_string(status)
+        got = y.double().cpu().numpy()
+        assert np.isfinite(got).all(), call
+        assert_rows_close(got, ref, what=f"static call {call} (larger block)")
+    moe.close()
+
+
 def test_static_workspace_rejects_sizes_beyond_its_limit(layer):
     wl, inputs, layers, _ = layer
     big = Workload("no_alloc_big", T=1024, H=wl.H, I=wl.I, E=wl.E, k=wl.k, seed=wl.seed)
