@@ -6,12 +6,16 @@
 // queue and runs them through a ring of shared-memory stages, with the roles of
 // the persistent engine's warp specialisation ("MiMo 把 1T 模型推到每秒千 token",
 // persistent engine kernel and warp specialization section):
-//   producer (one lane)   per stage (256 weight rows x 256 K): two TMA boxes of
-//                         packed E2M1 codes [128 rows x 128 B] (gate and up rows of a
-//                         gate/up item, or two 128-row blocks of a down item) in the
-//                         128-byte swizzled layout, and the activation operand (8
-//                         E2M1 terms per pair, below); the weights' E8M0 scales come
-//                         in pairs of wider boxes (several stages) through their own ring;
+//   producer (one lane)   per stage (256 weight rows x 256 K): the packed E2M1 codes
+//                         (gate and up rows of a gate/up item, or 256 rows of a down
+//                         item) in the 128-byte swizzled layout, as one 32 KB TMA box
+//                         from the packed layout (pack.cuh) or two [128 rows x 128 B]
+//                         boxes from the canonical one, and the activation operand of
+//                         down items and of gathered chunks (8 E2M1 terms per pair,
+//                         below); the weights' E8M0 scales come per group of stages
+//                         through their own ring;
+//   activation loaders    (3 warps) the per-token activation rows and scales of gate/up
+//                         stages, by cp.async (see tc_load);
 //   MMA issuer (one lane) per stage 6 tcgen05.cp of the stage's scale rows and 4
 //                         block-scaled MMAs (kind::mxf4, K = 64 each): A = the
 //                         activation terms (M = 128 rows, rows 8p + j of pair slot p,
@@ -403,10 +407,9 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
         const int idx = next_idx;
         const ItemRec cur = next;
         const bool end = idx >= n_items;
-        if (!end) {
-            next_idx = atomicAdd(a.queue, 1);
-            if (next_idx < n_items) next = a.rt ? table_item(a.rt, next_idx, rbu, rbd) : load_item(a.items + next_idx);
-        }
+        // the following item is claimed now and its record read once this item's stages are
+        // issued, so the claim's round trip overlaps them
+        if (!end) next_idx = atomicAdd(a.queue, 1);
         const int kind = end ? -1 : (cur.code >> 30) & 1;
         const int rb = (cur.code >> 20) & 0x3FF;
         {   // item record for the epilogue
@@ -523,6 +526,7 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
             }
         }
         if (failed) break;
+        if (next_idx < n_items) next = a.rt ? table_item(a.rt, next_idx, rbu, rbd) : load_item(a.items + next_idx);
     }
     if (failed) {
         if (atomicExch(a.abort, 1) == 0) raise_status(a.status, MOE_ERR_TIMEOUT, a.layer * 65536);

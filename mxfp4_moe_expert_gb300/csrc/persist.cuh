@@ -96,15 +96,22 @@ __device__ __forceinline__ bool aborted(const int* abort) {
     return *reinterpret_cast<const volatile int*>(abort) != 0;
 }
 
-// All CTAs of the grid meet; bounded.  Returns false (in every thread) on timeout / abort.
-__device__ __forceinline__ bool grid_sync(unsigned* bar, unsigned& epoch, unsigned long long deadline,
-                                          int* abort, int* status, bool withhold = false) {
+// All CTAs of the grid meet; bounded.  grid_arrive announces this CTA (after every
+// thread's earlier writes), grid_wait waits for every CTA's arrival of the same epoch;
+// work between the two must not depend on the other CTAs.  grid_wait returns false (in
+// every thread) on timeout / abort.
+__device__ __forceinline__ void grid_arrive(unsigned* bar, unsigned& epoch, bool withhold = false) {
     __syncthreads();
     ++epoch;
-    int failed = 0;
     if (threadIdx.x == 0) {
         __threadfence();
         if (!withhold) atomicAdd(bar, 1u);
+    }
+}
+__device__ __forceinline__ bool grid_wait(unsigned* bar, unsigned epoch, unsigned long long deadline, int* abort,
+                                          int* status) {
+    int failed = 0;
+    if (threadIdx.x == 0) {
         const unsigned target = epoch * gridDim.x;
         uint32_t spins = 0;
         while (ld_acquire_u32(bar) < target) {
@@ -116,6 +123,11 @@ __device__ __forceinline__ bool grid_sync(unsigned* bar, unsigned& epoch, unsign
         }
     }
     return __syncthreads_or(failed) == 0;
+}
+__device__ __forceinline__ bool grid_sync(unsigned* bar, unsigned& epoch, unsigned long long deadline,
+                                          int* abort, int* status, bool withhold = false) {
+    grid_arrive(bar, epoch, withhold);
+    return grid_wait(bar, epoch, deadline, abort, status);
 }
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -307,9 +319,12 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
         const bool resident = !pre && rstate[5] == r && rstate[6] == l;
         rstate[2] = rstate[3] = -1;
         rstate[8] = !pre && !resident;
+        rstate[10] = pre && rstate[9];   // this unit's input rows were copied with its weights
+        rstate[9] = 0;
     }
     __syncthreads();
     if (rstate[8]) router_fetch(p, ly, u, sm);
+    const bool x_pre = rstate[10] != 0;
     const uint32_t xs_a = smem_u32(xt), ws_a = smem_u32(sm.slots + wbase);
     for (int t0 = tbeg; t0 < tend; t0 += TP) {
         const int nt = min(TP, tend - t0);
@@ -317,9 +332,9 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
         if (t0 == tbeg) rs(1);
         if constexpr (NT == 1) {
             // the pass's rows of x as they are (rows >= nt keep stale data: their output
-            // columns are not stored)
+            // columns are not stored); already in flight when issued with the weights
             const int n16 = ncols / 8;   // 16-byte pieces per row
-            for (int i = threadIdx.x; i < nt * n16; i += blockDim.x) {
+            for (int i = x_pre ? nt * n16 : threadIdx.x; i < nt * n16; i += blockDim.x) {
                 const int t = i / n16, c = (i % n16) * 8;
                 cp_async_16(xs_a + (uint32_t)t * stride + (uint32_t)c * 2, p.x + (size_t)(t0 + t) * H + c0 + c);
             }
@@ -1183,6 +1198,41 @@ __device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMap
     *rs = r;
 }
 
+// This CTA's first router unit: its weight rows (and, for a plain input of one pass,
+// its input rows) into shared memory, issued before anything else of the launch.
+template <bool kLarge>
+__device__ __forceinline__ void router_first_copies(const PersistParams& p, const TcSmem& sm, int* rstate) {
+    const int units = router_units(p);
+    if (threadIdx.x == 0) {
+        rstate[2] = rstate[3] = -1;
+        rstate[5] = rstate[6] = -1;   // no weight slice resident
+        rstate[9] = 0;
+    }
+    const int u0 = router_first<kLarge>(units);
+    if (u0 >= router_end<kLarge>(units)) return;
+    router_fetch(p, p.layer[0], u0, sm);
+    if (threadIdx.x == 0) {
+        rstate[2] = u0;
+        rstate[3] = 0;
+    }
+    if (!p.norm && p.T <= kPRouteTok && router_tblocks(p) == 1) {   // the pass's x rows, as router_unit copies them
+        const int c0 = (u0 % (p.H / p.rslice)) * p.rslice;
+        const int n16 = p.rslice / 8;
+        const uint32_t xs_a = smem_u32(sm.slots), stride = router_stride(p);
+        for (int i = threadIdx.x; i < p.T * n16; i += blockDim.x) {
+            const int t = i / n16, c = (i % n16) * 8;
+            cp_async_16(xs_a + (uint32_t)t * stride + (uint32_t)c * 2, p.x + (size_t)t * p.H + c0 + c);
+        }
+        if (threadIdx.x == 0) rstate[9] = 1;
+    } else if (!p.norm && threadIdx.x < 32) {   // the first unit's input rows into L2
+        const int lane = threadIdx.x;
+        const int n_tb = router_tblocks(p);
+        const int c0 = ((u0 / n_tb) % (p.H / p.rslice)) * p.rslice, tb0 = (u0 % n_tb) * p.rtok;
+        for (int t = tb0 + lane; t < min(p.T, tb0 + min(p.rtok, 64)); t += 32)
+            prefetch_l2(p.x + (size_t)t * p.H + c0, (uint32_t)p.rslice * 2);
+    }
+}
+
 // All layers of one launch; returns early (in every thread of the block) on a timeout / abort.
 // kLarge: the block is routed through the workspace (route_is_small(p) is false), with
 // the input operand gathered per chunk; the host launches the matching instantiation.
@@ -1203,26 +1253,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     auto stamp = [&](int i) {
         if (blockIdx.x == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[i] = globaltimer_ns();
     };
-    stamp(0);
-    // this CTA's first router unit: weights into shared memory, x into L2
-    if (threadIdx.x == 0) {
-        rstate[2] = rstate[3] = -1;
-        rstate[5] = rstate[6] = -1;   // no weight slice resident
-    }
-    if (router_first<kLarge>(units) < router_end<kLarge>(units)) {
-        router_fetch(p, p.layer[0], router_first<kLarge>(units), sm);
-        if (threadIdx.x == 0) {
-            rstate[2] = router_first<kLarge>(units);
-            rstate[3] = 0;
-        }
-        if (!p.norm && threadIdx.x < 32) {   // the first unit's input rows into L2
-            const int lane = threadIdx.x;
-            const int n_tb = router_tblocks(p), u0 = router_first<kLarge>(units);
-            const int c0 = ((u0 / n_tb) % (p.H / p.rslice)) * p.rslice, tb0 = (u0 % n_tb) * p.rtok;
-            for (int t = tb0 + lane; t < min(p.T, tb0 + min(p.rtok, 64)); t += 32)
-                prefetch_l2(p.x + (size_t)t * p.H + c0, (uint32_t)p.rslice * 2);
-        }
-    }
+    stamp(0);   // (the first router unit's copies were issued before the setup)
     if (p.norm && p.init_from_x) {
         for (int u = blockIdx.x; u < cunits; u += gridDim.x) stack_init_unit(p, u, red);
         if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
@@ -1237,16 +1268,18 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         if (l == 0) stamp(53);
         operand_tasks(p, ly);
         if (l == 0) stamp(54);
+        const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
+        grid_arrive(p.bar, epoch, withhold);
         if (small && blockIdx.x >= units) {
-            // a CTA without a router unit would only wait at the barrier: it runs the routing
-            // code (results discarded; shared memory only) or, on every other such CTA, the
-            // combine code (nothing stored), so that code is in L2 when the whole grid needs it
+            // a CTA without a router unit would only wait at the barrier: after arriving it
+            // runs the routing code (results discarded; shared memory only) or, on every other
+            // such CTA, the combine code (nothing stored), so that code is in L2 when the whole
+            // grid needs it
             if (((blockIdx.x - units) & 1) == 0 || l + 1 < p.L) route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
             else if (p.norm) combine_unit(p, blockIdx.x % cunits, l, red, nullptr, true);
             else combine_elems(p, l, nullptr, sm.slots, true);
         }
-        const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
-        if (!grid_sync(p.bar, epoch, deadline, abort, status, withhold)) return;
+        if (!grid_wait(p.bar, epoch, deadline, abort, status)) return;
         stamp(2 + 4 * l);
         if (small) {
             route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
@@ -1329,6 +1362,7 @@ template <bool kLarge>
 __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_constant__ PersistParams p) {
     extern __shared__ uint8_t smem_raw[];
     const TcSmem sm = tc_smem(smem_raw);
+    router_first_copies<kLarge>(p, sm, reinterpret_cast<int*>(sm.red + 40));   // in flight during the setup
     const uint32_t tmem = tc_setup(sm);
     const unsigned long long deadline = globaltimer_ns() + p.ta.timeout_ns;
     persist_layers<kLarge>(p, smem_raw, tmem, deadline);
