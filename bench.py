@@ -11,8 +11,14 @@ fraction of the measured copy bandwidth.  L2 is flushed between timed steps,
 outside the per-step events (by default a 256 MiB write followed by a 256 MiB
 read, so each step starts from a cold and clean L2).  Prints one JSON line.
 
-`--impl reference` times the fp64 CPU oracle on the host cores on a bounded
-sample of the same workload and prints the same kind of line.
+The line also carries the same K steps timed under the other L2 protocol
+(`l2_other_protocol`: not flushed when the main value is flushed, and the
+reverse), the fractions of the measured copy bandwidth and of the nominal ~8 TB/s
+HBM3e bandwidth, and `cpu_baseline`: the fp64 oracle timed over the whole verify
+block (every routed expert) on all host cores.
+
+`--impl reference` times that oracle harness (OracleHost) over K steps and prints
+the same kind of line.
 """
 from __future__ import annotations
 
@@ -27,11 +33,12 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
-# the CPU oracle legs run single-threaded (BLAS included), so "cores" is 1
+# the CPU oracle legs run one worker process per host core, each single-threaded (BLAS included)
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 ACCEPTANCE_LENGTH = 6.30   # coding-task average accepted tokens per verify (page 3, "DFlash")
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e nominal bandwidth (~8 TB/s), the roofline the target is stated against
 
 
 def _peaks():
@@ -101,56 +108,151 @@ def _dist():
     return ws, rank
 
 
+def _oracle_worker(conn, wl, experts_per_layer):
+    """Worker process of OracleHost: encodes its experts once with the oracle's quantizer,
+    then evaluates the oracle's expert FFN for the (pair, input row) lists it is sent."""
+    import torch
+
+    from mxfp4_moe_expert_gb300.synth import expert_weight
+    from oracle import moe_oracle as O
+
+    torch.set_num_threads(1)
+    enc = {(l, e): [a for m in ("gate", "up", "down") for a in O.quantize(expert_weight(wl, l, e, m).numpy())]
+           for l, es in enumerate(experts_per_layer) for e in es}
+    conn.send("ready")
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            break
+        out = {}
+        for (l, e), items in msg.items():
+            m = O.ExpertMatrices(*enc[(l, e)])   # the oracle dequantises per forward, as in moe_layer
+            for pid, xrow in items:
+                out[pid] = m.ffn(xrow)
+        conn.send(out)
+
+
+class OracleHost:
+    """The fp64 oracle's forward of a verify block on the host cores.  Routing (router
+    logits, top-k, grouping), RMSNorm and the gate-weighted combine run in this process
+    with the oracle's functions; the routed experts' SwiGLU FFNs (the oracle's
+    ExpertMatrices) run in `workers` spawned processes, each owning a fixed share of the
+    block's routed experts, encoded once before timing.  Every routed expert of the block
+    is evaluated (no sampling)."""
+
+    def __init__(self, wl, workers=None):
+        import multiprocessing as mp
+
+        import numpy as np
+        import torch
+
+        from mxfp4_moe_expert_gb300.synth import make_inputs
+        from oracle import moe_oracle as O
+
+        self.O, self.np, self.wl = O, np, wl
+        inputs = make_inputs(wl)
+        b16 = lambda t: O.bf16_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+        self.x = b16(inputs.x)
+        self.layers = [(b16(L.router_w), L.router_b.double().numpy(), b16(L.norm_w) if L.norm_w is not None else None)
+                       for L in inputs.layers]
+        # the routed experts of every layer along the oracle's own trajectory (outside the timing)
+        routed = self._trajectory_experts()
+        self.n = workers or max(1, os.cpu_count() or 1)
+        self.owner = {}
+        shares = [[[] for _ in range(wl.layers)] for _ in range(self.n)]
+        i = 0
+        for l, es in enumerate(routed):
+            for e in es:
+                shares[i % self.n][l].append(e)
+                self.owner[(l, e)] = i % self.n
+                i += 1
+        self.owned = sum(len(es) for es in routed)
+        self.routed = [0] * wl.layers   # routed experts per layer of the last forward
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        for w in range(self.n):
+            a_, b_ = ctx.Pipe()
+            pr = ctx.Process(target=_oracle_worker, args=(b_, wl, shares[w]), daemon=True)
+            pr.start()
+            self.conns.append(a_)
+            self.procs.append(pr)
+        for c in self.conns:
+            assert c.recv() == "ready"
+
+    def _trajectory_experts(self):
+        """Experts the workers own, per layer: a single layer's routed experts (its routing
+        needs only the router); every expert of every layer of a stack (its later layers
+        route a residual that depends on the expert outputs)."""
+        O, wl = self.O, self.wl
+        if wl.layers == 1:
+            idx, _ = O.topk_gates(O.router_logits(self.x, *self.layers[0][:2]), wl.k)
+            return [sorted(set(int(e) for e in idx.reshape(-1)))]
+        return [list(range(wl.E)) for _ in range(wl.layers)]
+
+    def forward(self):
+        """One timed forward of the block; returns y (fp64 [T, H])."""
+        O, np, wl = self.O, self.np, self.wl
+        r = self.x.copy()
+        for l, (wr, b, nw) in enumerate(self.layers):
+            xin = O.rmsnorm(r, nw, wl.rms_eps) if wl.norm else r
+            idx, gate = O.topk_gates(O.router_logits(xin, wr, b), wl.k)
+            counts, offsets, perm = O.assignment(idx, wl.E)
+            msgs = [dict() for _ in range(self.n)]
+            self.routed[l] = int((counts > 0).sum())
+            for e in np.nonzero(counts)[0]:
+                items = [(int(p), xin[int(p) // wl.k]) for p in perm[offsets[e]:offsets[e + 1]]]
+                msgs[self.owner[(l, int(e))]][(l, int(e))] = items
+            for c, m in zip(self.conns, msgs):
+                c.send(m)
+            d = {}
+            for c in self.conns:
+                d.update(c.recv())
+            y = np.zeros_like(xin)
+            for t in range(wl.T):
+                for j in range(wl.k):   # slot order, as the oracle's moe_layer
+                    y[t] += gate[t, j] * d[t * wl.k + j]
+            r = r + y if wl.norm else y
+        return r
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except Exception:
+                pass
+        for pr in self.procs:
+            pr.join(timeout=10)
+
+
 def run_reference(args):
-    """The oracle, as it stands, on the host cores: one verify block's layer output
-    for a bounded sample of its routed experts, scaled to the whole layer."""
+    """The oracle, as it stands, on the host cores (OracleHost): every routed expert of
+    one verify block per step."""
     ws, rank = _dist()
     if rank != 0:
         return
-    import numpy as np
-    import torch
-
-    from mxfp4_moe_expert_gb300.synth import WORKLOADS, expert_weight, make_inputs
-    from oracle import moe_oracle as O
+    from mxfp4_moe_expert_gb300.synth import WORKLOADS
 
     wl = WORKLOADS[args.workload]
-    inputs = make_inputs(wl)
-    xf = O.bf16_to_f64(inputs.x.view(torch.int16).numpy().view(np.uint16))
-    wr = O.bf16_to_f64(inputs.layers[0].router_w.view(torch.int16).numpy().view(np.uint16))
-    b = inputs.layers[0].router_b.double().numpy()
-    logits = O.router_logits(xf, wr, b)
-    idx, gate = O.topk_gates(logits, wl.k)
-    counts, offsets, perm = O.assignment(idx, wl.E)
-    active = [int(e) for e in np.nonzero(counts)[0]]
-    n_sample = min(len(active), args.ref_experts)
-    # encoded bytes of the sampled experts (prepared outside the timed region)
-    enc = {}
-    for e in active[:n_sample]:
-        enc[e] = {m: O.quantize(expert_weight(wl, 0, e, m).numpy()) for m in ("gate", "up", "down")}
-
-    def one_step():
-        t0 = time.perf_counter()
-        lg = O.router_logits(xf, wr, b)
-        O.topk_gates(lg, wl.k)
-        for e in active[:n_sample]:
-            m = O.ExpertMatrices(*enc[e]["gate"], *enc[e]["up"], *enc[e]["down"])
-            for p in perm[offsets[e]:offsets[e + 1]]:
-                m.ffn(xf[int(p) // wl.k])
-        dt = time.perf_counter() - t0
-        return dt * len(active) / n_sample   # scaled to every routed expert of the block
-
-    for _ in range(args.warmup):
-        one_step()
-    times = [one_step() for _ in range(args.steps)]
-    us = statistics.mean(times) * 1e6
-    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
-    sample = f"{n_sample} of {len(active)} routed experts of one {wl.T}-token verify block, scaled by {len(active)}/{n_sample}"
+    host = OracleHost(wl)
+    try:
+        for _ in range(args.warmup):
+            host.forward()
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            host.forward()
+            times.append(time.perf_counter() - t0)
+    finally:
+        host.close()
+    us = statistics.mean(times) * 1e6 / wl.layers
+    sample = (f"the whole {wl.T}-token verify block: all {sum(host.routed)} routed experts "
+              f"({wl.layers} layer{'s' if wl.layers > 1 else ''}), no sampling; {host.n} worker processes")
     line = {
         "impl": "reference", "metric": "us_per_moe_layer_per_verify_block", "value": round(us, 1), "unit": "us",
-        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us * wl.layers / 1e3, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k},
-        "cpu_baseline": {"value": round(us, 1), "unit": "us", "cores": cores, "kind": "oracle", "sample": sample},
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "layers": wl.layers},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us", "cores": host.n, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(us, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -198,7 +300,7 @@ def run_gpu(args):
     n_active = [int((counts[l] > 0).sum()) for l in range(wl.layers)]
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    clean = torch.ones(64 << 20, dtype=torch.float32, device=dev) if args.flush == "clean" else None
+    clean = torch.ones(64 << 20, dtype=torch.float32, device=dev)
     graph = None
     if args.path == "graph":
         # the one-launch-per-phase forward captured once and replayed: the launch gaps of
@@ -214,14 +316,14 @@ def run_gpu(args):
             moe.forward(x, y, wsp, side.cuda_stream)
         torch.cuda.synchronize()
 
-    def flush_l2(i):
+    def flush_l2(i, mode=args.flush):
         # "write": a 256 MiB write (L2 is 129 MB) leaves L2 full of dirty lines of the
         # flush buffer; "clean" then reads another 256 MiB buffer, so the write-back of
         # those lines happens here and the timed forward starts from a clean, cold L2
-        if args.flush == "none":
+        if mode == "none":
             return
         flush.fill_(i & 0xFF)
-        if clean is not None:
+        if mode == "clean":
             clean.sum()
     def step(dbg_i=None):
         if graph is not None:
@@ -269,6 +371,18 @@ def run_gpu(args):
         kern = [sum(evs[2 * l].elapsed_time(evs[2 * l + 1]) for l in range(L)) * 1e3 / L for evs in kev]
     us = statistics.mean(per)
     kern_us = statistics.mean(kern)
+    # the same K steps under the other L2 protocol (not flushed <-> flushed clean), for reference
+    other = "none" if args.flush != "none" else "clean"
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_l2(i, other)
+        ev2[i][0].record(stream)
+        step()
+        ev2[i][1].record(stream)
+    torch.cuda.synchronize()
+    per2 = [a.elapsed_time(b) * 1e3 / wl.layers for a, b in ev2]
+    l2_other = {"l2": FLUSH_DESC[other], "us_per_layer": round(statistics.mean(per2), 2),
+                "dist_us_per_layer": _percentiles(per2)}
     st_code = pkg.moe_mxfp4_check(moe.handle, wsp.data_ptr(), st)
     if st_code != 0:
         raise pkg.MoeError(st_code, "forward")
@@ -340,6 +454,7 @@ def run_gpu(args):
         "implied_tokens_per_s": round(ACCEPTANCE_LENGTH / (us * 1e-6), 1),
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(kern_gbs / peak, 4),
+                     "frac_nominal": round(kern_gbs / NOMINAL_HBM_GBS, 4),
                      "traffic": layer_traffic(wl) if persistent else None, "peak_kind": peak_kind,
                      "kernel": "persistent forward kernel" if persistent else
                                "whole forward (CUDA graph of the per-phase launches)" if graph is not None else
@@ -347,6 +462,8 @@ def run_gpu(args):
                      "kernel_us_per_layer": round(kern_us, 2),
                      "kernel_bytes_per_layer": int(kern_bytes)},
         "forward_hbm_frac": round(gbs / peak, 4),
+        "forward_hbm_frac_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+        "l2_other_protocol": l2_other,
         "dist_us_per_layer": _percentiles([v / wl.layers for v in per]),
         "phases_us": phases,
         "e2e": {"value": round(e2e_us / wl.layers, 2), "unit": "us", "h2d_bytes_per_step": wl.T * wl.H * 2,
@@ -478,35 +595,19 @@ def moe_tma(wl):
 
 
 def cpu_baseline(wl):
-    """The oracle on the host cores, on a bounded sample (a few routed experts)."""
-    import numpy as np
-    import torch
-
-    from mxfp4_moe_expert_gb300.synth import expert_weight, make_inputs
-    from oracle import moe_oracle as O
-
-    inputs = make_inputs(wl)
-    xf = O.bf16_to_f64(inputs.x.view(torch.int16).numpy().view(np.uint16))
-    wr = O.bf16_to_f64(inputs.layers[0].router_w.view(torch.int16).numpy().view(np.uint16))
-    b = inputs.layers[0].router_b.double().numpy()
-    if wl.norm:
-        xf = O.rmsnorm(xf, O.bf16_to_f64(inputs.layers[0].norm_w.view(torch.int16).numpy().view(np.uint16)),
-                       wl.rms_eps)
-    idx, _ = O.topk_gates(O.router_logits(xf, wr, b), wl.k)
-    counts, offsets, perm = O.assignment(idx, wl.E)
-    active = [int(e) for e in np.nonzero(counts)[0]]
-    n = min(3, len(active))
-    enc = {e: {m: O.quantize(expert_weight(wl, 0, e, m).numpy()) for m in ("gate", "up", "down")}
-           for e in active[:n]}
-    t0 = time.perf_counter()
-    O.topk_gates(O.router_logits(xf, wr, b), wl.k)
-    for e in active[:n]:
-        m = O.ExpertMatrices(*enc[e]["gate"], *enc[e]["up"], *enc[e]["down"])
-        for p in perm[offsets[e]:offsets[e + 1]]:
-            m.ffn(xf[int(p) // wl.k])
-    dt = (time.perf_counter() - t0) * len(active) / n * wl.layers
-    return {"value": round(dt * 1e6 / wl.layers, 1), "unit": "us", "cores": 1, "kind": "oracle",
-            "sample": f"{n} of {len(active)} routed experts of layer 0, scaled to all routed experts"}
+    """The oracle on the host cores (OracleHost): one warm-up and one timed forward of the
+    whole verify block, every routed expert evaluated."""
+    host = OracleHost(wl)
+    try:
+        host.forward()
+        t0 = time.perf_counter()
+        host.forward()
+        dt = time.perf_counter() - t0
+    finally:
+        host.close()
+    return {"value": round(dt * 1e6 / wl.layers, 1), "unit": "us", "cores": host.n, "kind": "oracle",
+            "sample": f"the whole verify block: all {sum(host.routed)} routed experts, no sampling "
+                      f"({host.n} worker processes)"}
 
 
 def main():
@@ -516,7 +617,6 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="large", choices=["tiny", "mid", "large", "batched", "stack"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ref-experts", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default="", help="keep the nvidia-smi clock samples of the timed region here")
     ap.add_argument("--flush", default="clean", choices=["write", "clean", "none"],
