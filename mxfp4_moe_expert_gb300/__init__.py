@@ -59,7 +59,6 @@ class moe_mxfp4_config(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("expert_begin", ctypes.c_int32),
         ("expert_end", ctypes.c_int32),
-        ("dense_threshold", ctypes.c_int32),
         ("timeout_us", ctypes.c_int32),
     ]
 
@@ -276,10 +275,10 @@ class MoeLayers:
     """
 
     def __init__(self, *, hidden, inter, num_experts, top_k, max_tokens, layers, flags=0, rms_eps=1e-6,
-                 expert_begin=0, expert_end=0, dense_threshold=0, timeout_us=0):
+                 expert_begin=0, expert_end=0, timeout_us=0):
         self._keep = layers
         self.cfg = moe_mxfp4_config(len(layers), hidden, inter, num_experts, top_k, max_tokens, rms_eps, flags,
-                                    expert_begin, expert_end, dense_threshold, timeout_us)
+                                    expert_begin, expert_end, timeout_us)
         descs = [_layer_desc(L) for L in layers]
         self.handle = None
         st, h = moe_mxfp4_create(self.cfg, descs)

@@ -141,6 +141,7 @@ struct TcArgs {
     int debug_stall;          // testing aid: chunk 0 never signals its gate/up items
     const RouteTable* rt;     // shared-memory routing table, or NULL
     unsigned long long* trace;   // [6][256] per-stage timestamps of CTA 0 (profiling), or NULL
+    int dense;                // gathered chunks hold 16 pairs x 4 E2M1 terms (rows 4p + j) instead of 8 x 8
 };
 
 // Profiling aid: event `ev` of ring stage / item i of CTA 0.
@@ -163,7 +164,7 @@ struct TcSlotMeta {
 
 struct TcItemInfo {
     int kind, e, chunk, rb, ntok, pad0, pad1, pad2;
-    int ids[kTmaTok];   // gate/up: tokens; down: pair ids
+    int ids[kMaxChunk];   // gate/up: tokens; down: pair ids
 };
 
 struct TcSmem {
@@ -423,7 +424,7 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
             inf.ntok = end ? 0 : cur.ntok;
             inf.pad0 = inf.pad1 = inf.pad2 = 0;
 #pragma unroll
-            for (int q = 0; q < kTmaTok; ++q) inf.ids[q] = cur.tok[q];
+            for (int q = 0; q < kMaxChunk; ++q) inf.ids[q] = cur.tok[q];
             s.ring[re] = inf;
             mbar_arrive(&s.ringf[re]);
             ++rs.n;
@@ -786,19 +787,47 @@ __device__ __forceinline__ void group8_reduce_scatter(const float (&v)[32], floa
     // out[i]: k = (lane & 7) | i << 3
 }
 
+// The same over the 4 lanes of each lane group (lane & 3): lane j returns the group sums
+// of values j + 4i, i = 0..7 (partner offsets 2, 1; a fixed order).
+__device__ __forceinline__ void group4_reduce_scatter(const float (&v)[32], float (&out)[8], int lane) {
+    float a16[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {   // pairs differing in bit 1 of the index
+        const int k0 = (i & 1) | ((i >> 1) << 2), k1 = k0 | 2;
+        const bool hi = (lane & 2) != 0;
+        const float send = hi ? v[k0] : v[k1], keep = hi ? v[k1] : v[k0];
+        a16[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+    }
+    // a16[i]: k = (i & 1) | (bit1 of lane) << 1 | (i >> 1) << 2
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {   // pairs differing in bit 0: a16 indices 2i and 2i+1
+        const bool hi = (lane & 1) != 0;
+        const float send = hi ? a16[2 * i] : a16[2 * i + 1], keep = hi ? a16[2 * i + 1] : a16[2 * i];
+        out[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+    }
+    // out[i]: k = (lane & 3) | i << 2
+}
+
 // ---- epilogue warps (lane quarter q = warp % 4 < 2, column chunk c = warp / 4) -----
-// Accumulator lane 32q + l is activation row 32q + l: pair slot 4q + l / 8, term l % 8.
-// The warp reads columns 32c.. (gate rows / first down block) and 128 + 32c.. (up
-// rows / second down block): after the reduce-scatter lane l holds, for its pair,
+// kDense = false: accumulator lane 32q + l is activation row 32q + l: pair slot 4q + l / 8,
+// term l % 8; after the reduce-scatter over groups of 8 lanes, lane l holds, for its pair,
 // the sums of columns 32c + 8s + (l % 8) and 128 + 32c + 8s + (l % 8), s = 0..3.
+// kDense = true (16 pairs x 4 terms): pair slot 8q + l / 4, term l % 4; lane l holds the
+// sums of columns 32c + 4s + (l % 4) and 128 + .., s = 0..7.
+// The warp reads columns 32c.. (gate rows / first down block) and 128 + 32c.. (up rows /
+// second down block).
+template <bool kDense>
 __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in, uint32_t tmem, TcRoleState& rs_in,
                                          int warp, int lane, unsigned long long deadline) {
+    constexpr int kT = kDense ? 4 : kTcTerms;   // terms per activation: lanes (accumulator rows) per pair
+    constexpr int kV = 32 / kT;                 // columns per lane of each 32-column chunk
     const TcArgs a = a_in;
     const TcSmem s = s_in;
     TcRoleState rs = rs_in;
     const int q = warp & 3, c = warp >> 2;
     const int H = a.H, I = a.I;
-    const int p = 4 * q + (lane >> 3), j = lane & 7;   // pair slot and term of this lane's row
+    const int p = (32 / kT) * q + lane / kT, j = lane % kT;   // pair slot and term of this lane's row
+    const int base = lane & ~(kT - 1);                        // first lane of the pair
     bool failed = false;
     // barrier of the epilogue warps (bounded)
     auto epi_sync = [&]() -> bool {
@@ -815,11 +844,12 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
             failed = true;
             break;
         }
-        const TcItemInfo inf = s.ring[re];
+        const int kind = s.ring[re].kind, chunk = s.ring[re].chunk, rb = s.ring[re].rb, ntok = s.ring[re].ntok;
+        const int my_id = s.ring[re].ids[p];   // this lane's pair: token (gate/up) or pair id (down)
         tc_fence_after();
         if (warp == 0 && lane == 0) tc_trace(a, 5, rs.n);
-        float G[4], U[4];
-        if (inf.kind >= 0) {
+        float G[kV], U[kV];
+        if (kind >= 0) {
             uint32_t r0[32], r1[32];
             const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemAcc + 32 * c;
             tc_ld_x32(ta, r0);
@@ -828,10 +858,10 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
-            group8_reduce_scatter(v, G, lane);
+            if constexpr (kDense) group4_reduce_scatter(v, G, lane); else group8_reduce_scatter(v, G, lane);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r1[i]);
-            group8_reduce_scatter(v, U, lane);
+            if constexpr (kDense) group4_reduce_scatter(v, U, lane); else group8_reduce_scatter(v, U, lane);
         }
         tc_fence_before();
         __syncwarp();
@@ -840,23 +870,27 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
             mbar_arrive(&s.ringe[re]);
         }
         ++rs.n;
-        if (inf.kind < 0) break;
-        const bool mine = p < inf.ntok;
-        if (inf.kind == kItemGateUp) {
-            // h = silu(g) * u for rows 32c + 8s + j of the item's 128 (s = 0..3); the 32
-            // rows 32c.. are one MX block of the down projection's K.  Split into 8 E2M1
-            // terms with block scales over the pair's 8 lanes, stored as rows 8p + t of
-            // the chunk's down operand at K = rb * 128 + 32c + 8s + j.
-            float hv[4];
+        if (kind < 0) break;
+        const bool mine = p < ntok;
+        if (kind == kItemGateUp) {
+            // h = silu(g) * u for rows 32c + kT s + j of the item's 128 (s < kV); the 32 rows
+            // 32c.. are one MX block of the down projection's K.  Split into kT E2M1 terms
+            // with block scales over the pair's kT lanes, stored as rows kT p + t of the
+            // chunk's down operand at K = rb * 128 + 32c + kT s + j.
+            float hv[kV];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) hv[i] = silu(G[i]) * U[i];
-            uint32_t codes[4] = {0u, 0u, 0u, 0u};   // per s: term t in bits 4t..4t+3
-            uint32_t sbt = 0;                        // this lane's scale byte: term j
+            for (int i = 0; i < kV; ++i) hv[i] = silu(G[i]) * U[i];
+            uint32_t codes[kV];   // per s: term t in bits 4t..4t+3
 #pragma unroll
-            for (int t = 0; t < kTcTerms; ++t) {
-                float mx = fmaxf(fmaxf(fabsf(hv[0]), fabsf(hv[1])), fmaxf(fabsf(hv[2]), fabsf(hv[3])));
+            for (int i = 0; i < kV; ++i) codes[i] = 0u;
+            uint32_t sbt = 0;     // this lane's scale byte: term j
 #pragma unroll
-                for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+            for (int t = 0; t < kT; ++t) {
+                float mx = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kV; ++i) mx = fmaxf(mx, fabsf(hv[i]));
+#pragma unroll
+                for (int o = 1; o < kT; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
                 const uint32_t eb = __float_as_uint(mx) >> 23;
                 if (eb >= 8u && eb < 255u) {
                     uint32_t xb = eb - 2u;
@@ -864,7 +898,7 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
                     const float X = __uint_as_float(xb << 23);
                     const float inv = __uint_as_float((254u - xb) << 23);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < kV; ++i) {
                         const uint32_t cd = f32_to_e2m1(hv[i] * inv);
                         hv[i] = fmaf(-e2m1_code_to_f32(cd), X, hv[i]);
                         codes[i] |= cd << (4 * t);
@@ -872,31 +906,35 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
                     if (t == j) sbt = xb;
                 }
             }
-            // lane j of the pair gets term j's codes of the pair's 8 lanes, for each s
-            uint32_t wd[4];
+            // lane j of the pair gathers term j's codes of the pair's kT lanes: column n (0..31)
+            // of the chunk is value n / kT of lane n % kT
+            uint32_t wd[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) wd[i] = transpose_oct(codes[i], lane);
+            for (int n = 0; n < 32; ++n) {
+                const uint32_t v = __shfl_sync(0xFFFFFFFFu, codes[n / kT], base + n % kT);
+                wd[n / 8] |= ((v >> (4 * j)) & 0xFu) << (4 * (n % 8));
+            }
             if (mine) {
-                uint8_t* hb = a.hb4 + (size_t)inf.chunk * hb4_chunk_bytes(I) + (size_t)(inf.rb >> 1) * 8192;
-                const int n = 8 * p + j;                        // operand row: pair slot p, term j
-                const int chunk16 = (inf.rb & 1) * 4 + c;       // 16-byte chunk of K (rb&1)*128 + 32c .. +31
+                uint8_t* hb = a.hb4 + (size_t)chunk * hb4_chunk_bytes(I) + (size_t)(rb >> 1) * 8192;
+                const int n = kT * p + j;                    // operand row: pair slot p, term j
+                const int chunk16 = (rb & 1) * 4 + c;        // 16-byte chunk of K (rb&1)*128 + 32c .. +31
                 *reinterpret_cast<uint4*>(hb + n * 128 + ((chunk16 ^ (n & 7)) << 4)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-                a.hsf[(size_t)inf.chunk * hsf_chunk_bytes(I) + (size_t)(inf.rb >> 1) * 512 + n * 8 + 4 * (inf.rb & 1) + c] =
+                a.hsf[(size_t)chunk * hsf_chunk_bytes(I) + (size_t)(rb >> 1) * 512 + n * 8 + 4 * (rb & 1) + c] =
                     (uint8_t)sbt;
             }
             fence_proxy_async_global();   // read next by bulk copies
             if (!epi_sync()) { failed = true; break; }
-            if (warp == 0 && lane == 0 && !(a.debug_stall && inf.chunk == 0)) {
+            if (warp == 0 && lane == 0 && !(a.debug_stall && chunk == 0)) {
                 __threadfence();
                 fence_proxy_async_global();
-                red_release_add_gpu(a.done + inf.chunk, 1);
+                red_release_add_gpu(a.done + chunk, 1);
             }
-        } else if (mine) {   // down: rows rb * 256 + 32c + 8s + j and + 128
-            float* dst = a.partial + (size_t)inf.ids[p] * H + (size_t)inf.rb * kTcN + 32 * c + j;
+        } else if (mine) {   // down: rows rb * 256 + 32c + kT s + j and + 128
+            float* dst = a.partial + (size_t)my_id * H + (size_t)rb * kTcN + 32 * c + j;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                dst[8 * i] = G[i];
-                dst[128 + 8 * i] = U[i];
+            for (int i = 0; i < kV; ++i) {
+                dst[kT * i] = G[i];
+                dst[128 + kT * i] = U[i];
             }
         }
     }
@@ -919,7 +957,8 @@ __device__ __forceinline__ void tc_phase(const TcMaps& maps, const TcArgs& a, co
     } else if (tc_loader_index(warp) >= 0) {
         tc_load(a, s, rs, tc_loader_index(warp), lane, deadline);
     } else if (tc_is_epi_warp(warp)) {
-        tc_epilogue(a, s, tmem, rs, warp, lane, deadline);
+        if (kGathered && a.dense) tc_epilogue<true>(a, s, tmem, rs, warp, lane, deadline);
+        else tc_epilogue<false>(a, s, tmem, rs, warp, lane, deadline);
     }
 }
 

@@ -357,9 +357,16 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     p.ta.n_items = p.wl.n_items;
     p.wl.abort = reinterpret_cast<int*>(ws + L.status + 24);   // cleared with the status words
     const bool small_block = (size_t)T * k <= 64 && (size_t)T * E <= 8192;   // routed in shared memory
-    if (!small_block) {   // larger blocks: gathered input operand
+    p.chunk = moe::kTmaTok;
+    p.terms = moe::kTcTerms;
+    if (!small_block) {   // larger blocks: gathered input operand, dense unless disabled
         p.ta.xc4 = reinterpret_cast<uint8_t*>(ws + L.xc4);
         p.ta.xcs = reinterpret_cast<uint8_t*>(ws + L.xcs);
+        if (!(c.flags & MOE_FLAG_NO_DENSE)) {
+            p.chunk = moe::kDenseTok;
+            p.terms = 4;
+            p.ta.dense = 1;
+        }
     }
     p.ta.abort = p.wl.abort;
     if (c.flags & MOE_FLAG_TRACE) p.ta.trace = reinterpret_cast<unsigned long long*>(ws + L.status + 4096);
@@ -465,7 +472,7 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
     if (c.top_k < 1 || c.top_k > c.num_experts || c.top_k > moe::kMaxTopK) return MOE_ERR_INVALID_ARG;
     if (c.max_tokens < 1 || c.max_tokens > 4096) return MOE_ERR_INVALID_ARG;
     if ((c.flags & MOE_FLAG_NORM) && !(c.rms_eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
-    if (c.timeout_us < 0 || c.dense_threshold < 0) return MOE_ERR_INVALID_ARG;
+    if (c.timeout_us < 0) return MOE_ERR_INVALID_ARG;
     int eb = c.expert_begin, ee = c.expert_end;
     if (eb == 0 && ee == 0) ee = c.num_experts;
     if (eb < 0 || ee > c.num_experts || eb >= ee) return MOE_ERR_INVALID_ARG;

@@ -72,6 +72,8 @@ struct PersistParams {
     float* ss;         // [T, H / 256] sums of squares of the residual per column block
     float* rpart;      // [H / rslice, T, E] router slice partials
     int rslice;        // columns per router unit (256, 512 or 1024; divides H)
+    int chunk;         // pairs per chunk of a block routed through the workspace (8, or 16 dense)
+    int terms;         // E2M1 terms per activation in those chunks (8, or 4 dense)
     int rtok;          // tokens per router unit (T for blocks routed in shared memory; else a multiple of 8 G)
     int* rcnt;         // [kMaxPersistLayers, 32] finished router units per expert group (zeroed per launch)
     unsigned long long* tstamp;   // CTA 0's %globaltimer at phase ends (or NULL)
@@ -988,12 +990,12 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
     }
     __syncthreads();
     sub(3);
-    // ---- first chunk of each routed expert (chunks of <= 8 pairs) and the item counts
+    // ---- first chunk of each routed expert (chunks of <= p.chunk pairs) and the item counts
     const int n_active = misc[0];
     const int rbu = p.I / kTmaRows, rbd = H / kDownRows;
     int* chunk0 = flag;                 // [n_active + 1]
     for (int a = threadIdx.x; a < n_active; a += blockDim.x)
-        chunk0[a] = (__ldcg(rb.counts + __ldcg(rb.active + 1 + a)) + kTmaTok - 1) / kTmaTok;
+        chunk0[a] = (__ldcg(rb.counts + __ldcg(rb.active + 1 + a)) + p.chunk - 1) / p.chunk;
     __syncthreads();
     if (warp == 0) {
         const int total_chunks = warp_excl_scan(chunk0, n_active);
@@ -1050,18 +1052,18 @@ __device__ __noinline__ void build_items_slice(const PersistParams& p, int* scra
             const int mid = (lo + hi + 1) >> 1;
             if (s_c0[mid] * nrb <= j) lo = mid; else hi = mid - 1;
         }
-        const int nch = (s_cnt[lo] + kTmaTok - 1) / kTmaTok;
+        const int nch = (s_cnt[lo] + p.chunk - 1) / p.chunk;
         const int rr = j - s_c0[lo] * nrb, rbi = rr / nch, tc = rr % nch;   // row block major, chunk minor
         ItemRec r;
         r.code = item_code(down ? kItemDown : kItemGateUp, rbi, tc, lo);
         r.e = s_act[lo];
-        r.beg = s_beg[lo] + tc * kTmaTok;
-        r.ntok = min(kTmaTok, s_cnt[lo] - tc * kTmaTok);
-        int pq[kTmaTok];
+        r.beg = s_beg[lo] + tc * p.chunk;
+        r.ntok = min(p.chunk, s_cnt[lo] - tc * p.chunk);
+        int pq[kMaxChunk];
 #pragma unroll
-        for (int q = 0; q < kTmaTok; ++q) pq[q] = q < r.ntok ? __ldcg(rb.perm + r.beg + q) : 0;
+        for (int q = 0; q < kMaxChunk; ++q) pq[q] = q < r.ntok ? __ldcg(rb.perm + r.beg + q) : 0;
 #pragma unroll
-        for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? pq[q] : pq[q] / k) : 0;
+        for (int q = 0; q < kMaxChunk; ++q) r.tok[q] = q < r.ntok ? (down ? pq[q] : pq[q] / k) : 0;
         r.chunk = s_c0[lo] + tc;
         r.pad[0] = nch;
         r.pad[1] = r.pad[2] = 0;
@@ -1074,7 +1076,9 @@ static_assert(kGatherBufBase + 16 * kGatherBufBytes <= (uint32_t)kTcStages * kTc
 static_assert(4 * (kMaxExperts + 1) * sizeof(int) <= kGatherBufBase, "routing arrays below the gather buffers");
 // The layer input's expert operand gathered per chunk (larger blocks, every CTA, after
 // the grouping is published): unit = (chunk, 256-wide stage), one warp per unit; pair
-// slot p of the chunk gets its token's 8 term rows (1 KB) and their scales (64 B).
+// slot p of the chunk gets the first p.terms of its token's 8 term rows (rows
+// p.terms * p + j; the first 4 terms of the 8-term split are the 4-term split) and their
+// scales.
 // scratch: the routing arrays staged by build_items_slice.
 __device__ __noinline__ void gather_chunk_operand(const PersistParams& p, const int* scratch, uint8_t* slots) {
     const int n_active = __ldcg(p.rb.active);
@@ -1092,23 +1096,32 @@ __device__ __noinline__ void gather_chunk_operand(const PersistParams& p, const 
             const int mid = (lo + hi + 1) >> 1;
             if (s_c0[mid] <= c) lo = mid; else hi = mid - 1;
         }
-        const int tc = c - s_c0[lo], beg = s_beg[lo] + tc * kTmaTok, ntok = min(kTmaTok, s_cnt[lo] - tc * kTmaTok);
+        const int tc = c - s_c0[lo], beg = s_beg[lo] + tc * p.chunk, ntok = min(p.chunk, s_cnt[lo] - tc * p.chunk);
         uint8_t* dst = const_cast<uint8_t*>(p.ta.xc4) + ((size_t)c * nst + st) * 8192;   // workspace memory
         uint8_t* dsf = const_cast<uint8_t*>(p.ta.xcs) + ((size_t)c * nst + st) * 512;
+        const int rows = p.terms, pp = rows * 8;   // term rows per pair; 16-byte pieces per pair
         // the chunk's tokens (lane q: pair q), then every pair's rows and scales into this
         // warp's shared-memory buffer (all copies in flight at once), then out in one run
         const int tq = lane < ntok ? __ldcg(p.rb.perm + beg + lane) / p.k : 0;
         for (int q = 0; q < ntok; ++q) {
             const int t = __shfl_sync(0xFFFFFFFFu, tq, q);
             const uint8_t* src = p.xb4 + ((size_t)t * nst + st) * 1024;
-            cp_async_16(buf + q * 1024 + lane * 16, src + lane * 16);
-            cp_async_16(buf + q * 1024 + 512 + lane * 16, src + 512 + lane * 16);
-            if (lane < 4) cp_async_16(buf + 8192 + q * 64 + lane * 16, p.xsf + ((size_t)t * nst + st) * 64 + lane * 16);
+            for (int i = lane; i < pp; i += 32) cp_async_16(buf + (q * pp + i) * 16, src + i * 16);
+            if (lane < rows / 2)
+                cp_async_16(buf + 8192 + q * rows * 8 + lane * 16, p.xsf + ((size_t)t * nst + st) * 64 + lane * 16);
         }
         cp_async_wait_all();
         __syncwarp();
-        for (int i = lane; i < ntok * 64; i += 32) reinterpret_cast<int4*>(dst)[i] = ld_shared_v4(buf + i * 16);
-        if (lane < ntok * 4) reinterpret_cast<int4*>(dsf)[lane] = ld_shared_v4(buf + 8192 + lane * 16);
+        // rows are 128-byte swizzled by their row index mod 8 (the source by term j): with 4
+        // terms an odd pair slot's rows 4q + j have phase j ^ 4, so their 16-byte pieces
+        // swap places c <-> c ^ 4
+        for (int i = lane; i < ntok * pp; i += 32) {
+            const int qq = i / pp, w = i % pp;
+            const int o = (rows == 4 && (qq & 1)) ? (w ^ 4) : w;
+            reinterpret_cast<int4*>(dst)[qq * pp + o] = ld_shared_v4(buf + i * 16);
+        }
+        for (int i = lane; i < ntok * rows / 2; i += 32)
+            reinterpret_cast<int4*>(dsf)[i] = ld_shared_v4(buf + 8192 + i * 16);
         __syncwarp();   // the buffer is read before the next unit's copies land
     }
 }

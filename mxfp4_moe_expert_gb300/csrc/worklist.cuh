@@ -15,7 +15,9 @@ namespace moe {
 
 constexpr int kTmaRows = 128;   // rows per gate/up item (of each of the two matrices)
 constexpr int kDownRows = 256;  // rows per down item
-constexpr int kTmaTok = 8;      // pairs per chunk
+constexpr int kTmaTok = 8;      // pairs per chunk (8 E2M1 terms per activation)
+constexpr int kDenseTok = 16;   // pairs per chunk of the dense operand (4 terms per activation)
+constexpr int kMaxChunk = 16;
 
 enum : int { kItemGateUp = 0, kItemDown = 1 };
 
@@ -25,15 +27,15 @@ __host__ __device__ __forceinline__ int item_code(int kind, int rb, int tc, int 
     return (kind << 30) | (rb << 20) | (tc << 11) | a;
 }
 
-// One work item as the producer reads it (64 bytes).
+// One work item as the producer reads it (96 bytes).
 struct __align__(16) ItemRec {
-    int code;          // item_code(kind, rb, tc, a)
-    int e;             // expert id
-    int beg;           // first position of the chunk's pairs in perm
-    int ntok;          // pairs in the chunk (1..8)
-    int tok[kTmaTok];  // gate/up items: token of each pair; down items: pair id (t*k + j)
-    int chunk;         // chunk index within the layer
-    int pad[3];        // pad[0]: chunks of the expert (the items of one row block are adjacent)
+    int code;            // item_code(kind, rb, tc, a)
+    int e;               // expert id
+    int beg;             // first position of the chunk's pairs in perm
+    int ntok;            // pairs in the chunk (1..8, or 1..16 with the dense operand)
+    int tok[kMaxChunk];  // gate/up items: token of each pair; down items: pair id (t*k + j)
+    int chunk;           // chunk index within the layer
+    int pad[3];          // pad[0]: chunks of the expert (the items of one row block are adjacent)
 };
 
 // Routing state of one layer kept in shared memory by every CTA when the verify
@@ -81,7 +83,7 @@ __device__ __forceinline__ ItemRec table_item(const RouteTable* rt, int idx, int
     r.beg = rt->beg[lo] + tc * kTmaTok;
     r.ntok = min(kTmaTok, rt->cnt[lo] - tc * kTmaTok);
 #pragma unroll
-    for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? rt->pair[r.beg + q] : rt->tok[r.beg + q]) : 0;
+    for (int q = 0; q < kMaxChunk; ++q) r.tok[q] = q < r.ntok ? (down ? rt->pair[r.beg + q] : rt->tok[r.beg + q]) : 0;
     r.chunk = chunk;
     r.pad[0] = nch;
     r.pad[1] = r.pad[2] = 0;
@@ -94,7 +96,7 @@ __device__ __forceinline__ ItemRec load_item(const ItemRec* src) {
     const int4* s = reinterpret_cast<const int4*>(src);
     int4* d = reinterpret_cast<int4*>(&r);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = __ldcg(s + i);
+    for (int i = 0; i < (int)(sizeof(ItemRec) / 16); ++i) d[i] = __ldcg(s + i);
     return r;
 }
 
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(1024) build_items_kernel(RouteBufs rb, int H, 
         r.beg = s_beg[aa] + tc * kTmaTok;
         r.ntok = min(kTmaTok, s_cnt[aa] - tc * kTmaTok);
 #pragma unroll
-        for (int q = 0; q < kTmaTok; ++q) r.tok[q] = q < r.ntok ? (down ? s_perm[r.beg + q] : s_perm[r.beg + q] / k) : 0;
+        for (int q = 0; q < kMaxChunk; ++q) r.tok[q] = q < r.ntok ? (down ? s_perm[r.beg + q] : s_perm[r.beg + q] / k) : 0;
         r.chunk = chunk;
         r.pad[0] = nch;
         r.pad[1] = r.pad[2] = 0;

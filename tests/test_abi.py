@@ -46,11 +46,11 @@ def test_status_strings_and_host_side_validation(lib_path):
     assert pkg.moe_mxfp4_status_string(pkg.MOE_OK) == "ok"
     assert "workspace" in pkg.moe_mxfp4_status_string(pkg.MOE_ERR_WORKSPACE)
     # argument checks that return before touching a device
-    st, h = pkg.moe_mxfp4_create(pkg.moe_mxfp4_config(0, 256, 128, 8, 2, 8, 1e-6, 0, 0, 0, 0, 0), [pkg.moe_mxfp4_layer()])
+    st, h = pkg.moe_mxfp4_create(pkg.moe_mxfp4_config(0, 256, 128, 8, 2, 8, 1e-6, 0, 0, 0, 0), [pkg.moe_mxfp4_layer()])
     assert st == pkg.MOE_ERR_INVALID_ARG and not h
-    st, h = pkg.moe_mxfp4_create(pkg.moe_mxfp4_config(1, 200, 128, 8, 2, 8, 1e-6, 0, 0, 0, 0, 0), [pkg.moe_mxfp4_layer()])
+    st, h = pkg.moe_mxfp4_create(pkg.moe_mxfp4_config(1, 200, 128, 8, 2, 8, 1e-6, 0, 0, 0, 0), [pkg.moe_mxfp4_layer()])
     assert st == pkg.MOE_ERR_INVALID_ARG
-    st, h = pkg.moe_mxfp4_create(pkg.moe_mxfp4_config(1, 256, 128, 8, 9, 8, 1e-6, 0, 0, 0, 0, 0), [pkg.moe_mxfp4_layer()])
+    st, h = pkg.moe_mxfp4_create(pkg.moe_mxfp4_config(1, 256, 128, 8, 9, 8, 1e-6, 0, 0, 0, 0), [pkg.moe_mxfp4_layer()])
     assert st == pkg.MOE_ERR_INVALID_ARG
     assert pkg.moe_mxfp4_quantize(None, 1, 32, None, None, None) == pkg.MOE_ERR_INVALID_ARG
     assert pkg.moe_mxfp4_forward(None, None, 8, None, None, 0, None) == pkg.MOE_ERR_INVALID_ARG

@@ -48,11 +48,15 @@ def _crafted_bytes(wl):
     return out
 
 
-@pytest.mark.parametrize("flags,packed", [(0, False), (pkg.MOE_FLAG_MULTI_KERNEL, False), (0, True),
-                                          (pkg.MOE_FLAG_MULTI_KERNEL, True)],
-                         ids=["persistent", "multi_kernel", "persistent_packed", "multi_kernel_packed"])
-def test_every_weight_byte_decodes_as_the_format_defines(flags, packed):
-    wl = WL
+@pytest.mark.parametrize("flags,packed,T", [(0, False, 8), (pkg.MOE_FLAG_MULTI_KERNEL, False, 8), (0, True, 8),
+                                            (pkg.MOE_FLAG_MULTI_KERNEL, True, 8), (0, True, 40),
+                                            (pkg.MOE_FLAG_NO_DENSE, True, 40)],
+                         ids=["persistent", "multi_kernel", "persistent_packed", "multi_kernel_packed",
+                              "persistent_dense", "persistent_gathered_8x8"])
+def test_every_weight_byte_decodes_as_the_format_defines(flags, packed, T):
+    """T = 40 (80 pairs) is routed through the workspace: its chunks take the dense operand
+    (16 pairs x 4 terms), or 8 pairs x 8 terms with MOE_FLAG_NO_DENSE."""
+    wl = WL.scaled(T=T)
     assert (wl.H // 2) == 256 and (wl.I // 2) == 256   # one full byte cycle per row
     inputs = make_inputs(wl)
     crafted = _crafted_bytes(wl)

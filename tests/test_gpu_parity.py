@@ -150,6 +150,25 @@ def test_layer_parity_packed_experts(wl):
         moe.close()
 
 
+@pytest.mark.parametrize("wl", [w for w in SMALL if w.name in ("tma_many_tokens", "tma_max_pairs")], ids=lambda w: w.name)
+def test_gathered_blocks_with_and_without_the_dense_operand(wl):
+    """Blocks routed through the workspace run chunks of 16 pairs x 4 E2M1 terms (dense
+    operand) by default and of 8 pairs x 8 terms with MOE_FLAG_NO_DENSE: both against the
+    oracle on every row, and the 8 x 8 result nearer to it."""
+    inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV),
+                                   packed=True)
+    wr, b, _ = oracle_layer_args(inputs, 0)
+    ref = O.moe_layer(bf16_np(inputs.x), wr, b, wl.k, OracleExperts(wl, 0, "cpu"))
+    worst = {}
+    for flags in (0, pkg.MOE_FLAG_NO_DENSE):
+        moe = _moe(wl, layers, flags=flags)
+        y, bufs = _run(moe, inputs.x.to(DEV))
+        _check_routing(_dbg_layer(bufs, 0), ref, f"{wl.name} flags={flags}")
+        worst[flags] = assert_rows_close(y.double().cpu().numpy(), ref["y"], what=f"{wl.name} flags={flags}")
+        moe.close()
+    assert worst[pkg.MOE_FLAG_NO_DENSE][0] < worst[0][0]
+
+
 @pytest.mark.parametrize("wl", [
     Workload("stack_small", T=6, H=512, I=256, E=12, k=3, layers=4, norm=True, seed=0x5EED0104),
     Workload("stack_tma", T=7, H=1024, I=512, E=12, k=3, layers=3, norm=True, seed=0x5EED0115),
