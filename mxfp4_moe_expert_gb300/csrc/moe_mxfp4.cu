@@ -405,6 +405,15 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
             }
         }
     }
+    // a single layer on a block of at most 8 tokens: whole-row router units of F experts when
+    // x and F weight rows fit in the slot area (no cross-CTA sum of column slices)
+    p.rfull = 0;
+    if (!p.norm && small_block && T <= moe::kPRouteTok) {
+        const int F = (E + h->persist_grid - 1) / h->persist_grid;
+        const size_t row = (size_t)H * 2 + 16;
+        const size_t need = ((size_t)T * row + 1023) / 1024 * 1024 + (size_t)F * row;
+        if (need <= (size_t)moe::kTcStages * moe::kTcSlotBytes) p.rfull = F;
+    }
     p.bar = reinterpret_cast<unsigned*>(ws + L.status + 16);
     p.route_flag = reinterpret_cast<int*>(ws + L.status + 20);
     p.tstamp = reinterpret_cast<unsigned long long*>(ws + L.status + 64);

@@ -72,6 +72,7 @@ struct PersistParams {
     float* ss;         // [T, H / 256] sums of squares of the residual per column block
     float* rpart;      // [H / rslice, T, E] router slice partials
     int rslice;        // columns per router unit (256, 512 or 1024; divides H)
+    int rfull;         // experts per whole-row router unit (router_full_unit), or 0: column-sliced units
     int chunk;         // pairs per chunk of a block routed through the workspace (8, or 16 dense)
     int terms;         // E2M1 terms per activation in those chunks (8, or 4 dense)
     int rtok;          // tokens per router unit (T for blocks routed in shared memory; else a multiple of 8 G)
@@ -477,6 +478,68 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
             }
             p.rb.logits[(size_t)t * E + e] = z + (ly.router_b ? __ldg(ly.router_b + e) : 0.0f);
         }
+    }
+}
+
+// Whole-row router units (a single layer on a block of at most 8 tokens, when x and a
+// unit's weight rows fit in shared memory): unit u = experts [u F, u F + F) over all H
+// columns, so every logit is complete inside one CTA and no cross-CTA sum is needed.
+// Shared memory (slot area): x [T rows][H * 2 + 16 B] at 0, the unit's weight rows at
+// router_full_wbase (rows padded by 16 bytes: conflict-free ldmatrix).
+__device__ __forceinline__ uint32_t router_full_stride(const PersistParams& p) { return (uint32_t)p.H * 2 + 16; }
+__device__ __forceinline__ uint32_t router_full_wbase(const PersistParams& p) {
+    return ((uint32_t)p.T * router_full_stride(p) + 1023u) & ~1023u;
+}
+__device__ __forceinline__ int router_full_units(const PersistParams& p) { return (p.E + p.rfull - 1) / p.rfull; }
+// The copies of unit u (x and its weight rows), 16-byte cp.async over the whole CTA.
+__device__ __forceinline__ void router_full_fetch(const PersistParams& p, const PersistLayer& ly, int u,
+                                                  const TcSmem& sm) {
+    const int n16 = p.H / 8, e0 = u * p.rfull, ne = min(p.rfull, p.E - e0);
+    const uint32_t stride = router_full_stride(p), xs = smem_u32(sm.slots), wsb = xs + router_full_wbase(p);
+    const uint64_t pol = l2_evict_first_policy();
+    for (int i = threadIdx.x; i < ne * n16; i += blockDim.x) {
+        const int r = i / n16, c = (i % n16) * 8;
+        cp_async_16_hint(wsb + (uint32_t)r * stride + (uint32_t)c * 2, ly.router_w + (size_t)(e0 + r) * p.H + c, pol);
+    }
+    for (int i = threadIdx.x; i < p.T * n16; i += blockDim.x) {
+        const int t = i / n16, c = (i % n16) * 8;
+        cp_async_16(xs + (uint32_t)t * stride + (uint32_t)c * 2, p.x + (size_t)t * p.H + c);
+    }
+}
+// logit[t][e] = sum_h x[t,h] Wr[e,h] + b[e] for the unit's experts: the 16 warps split
+// H, each with mma.sync m16n8k16 (rows = experts, columns = tokens; bf16 products are
+// exact, fp32 sums), then the warps' partial sums are added in warp order.
+__device__ __noinline__ void router_full_unit(const PersistParams& p, const PersistLayer& ly, int u, const TcSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e0 = u * p.rfull, ne = min(p.rfull, p.E - e0);
+    const uint32_t stride = router_full_stride(p), xs = smem_u32(sm.slots), wsb = xs + router_full_wbase(p);
+    cp_async_wait_all();
+    __syncthreads();
+    const int kw = p.H / 16;                                   // columns per warp (multiple of 16)
+    const int arow = min(lane & 15, ne - 1), brow = min(lane & 7, p.T - 1);   // rows past the unit / block: repeats
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int ks = 0; ks < kw; ks += 16) {
+        const int k0 = warp * kw + ks;
+        uint32_t a0, a1, a2, a3, b0, b1;
+        ldmatrix_x4(wsb + (uint32_t)arow * stride + (uint32_t)(k0 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+        ldmatrix_x2(xs + (uint32_t)brow * stride + (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2, b0, b1);
+        mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
+    }
+    __syncthreads();   // every warp's reads of the staged rows are done: the sums reuse the area
+    float* red = reinterpret_cast<float*>(sm.slots);           // [16 warps][16 experts][8 tokens]
+    {
+        const int e = lane >> 2, t = 2 * (lane & 3);
+        red[(warp * 16 + e) * 8 + t] = d[0];
+        red[(warp * 16 + e) * 8 + t + 1] = d[1];
+        red[(warp * 16 + e + 8) * 8 + t] = d[2];
+        red[(warp * 16 + e + 8) * 8 + t + 1] = d[3];
+    }
+    __syncthreads();
+    if (threadIdx.x < ne * p.T) {
+        const int e = threadIdx.x / p.T, t = threadIdx.x % p.T;
+        float z = 0.0f;
+        for (int w = 0; w < 16; ++w) z += red[(w * 16 + e) * 8 + t];
+        p.rb.logits[(size_t)t * p.E + e0 + e] = z + (ly.router_b ? __ldg(ly.router_b + e0 + e) : 0.0f);
     }
 }
 
@@ -1215,6 +1278,10 @@ __device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMap
 // its input rows) into shared memory, issued before anything else of the launch.
 template <bool kLarge>
 __device__ __forceinline__ void router_first_copies(const PersistParams& p, const TcSmem& sm, int* rstate) {
+    if (p.rfull) {   // whole-row units: unit b on CTA b
+        if ((int)blockIdx.x < router_full_units(p)) router_full_fetch(p, p.layer[0], blockIdx.x, sm);
+        return;
+    }
     const int units = router_units(p);
     if (threadIdx.x == 0) {
         rstate[2] = rstate[3] = -1;
@@ -1260,7 +1327,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     unsigned epoch = 0;
     TcRoleState rs{0u, 0u, 0u, 0u};
     int* rstate = reinterpret_cast<int*>(sm.red + 40);     // router-weight copy state (router_fetch)
-    const int units = router_units(p);
+    const int units = p.rfull ? router_full_units(p) : router_units(p);
     const int cunits = p.T * (p.H / kCombineChunk);
     constexpr bool small = !kLarge;
     auto stamp = [&](int i) {
@@ -1275,8 +1342,12 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
 
     for (int l = 0; l < p.L; ++l) {
         const PersistLayer& ly = p.layer[l];
-        for (int u = router_first<kLarge>(units); u < router_end<kLarge>(units); u += router_step<kLarge>())
-            p.norm ? router_unit<3>(p, ly, l, u, sm, rstate) : router_unit<1>(p, ly, l, u, sm, rstate);
+        if (p.rfull) {
+            if ((int)blockIdx.x < units) router_full_unit(p, ly, blockIdx.x, sm);
+        } else {
+            for (int u = router_first<kLarge>(units); u < router_end<kLarge>(units); u += router_step<kLarge>())
+                p.norm ? router_unit<3>(p, ly, l, u, sm, rstate) : router_unit<1>(p, ly, l, u, sm, rstate);
+        }
         if (threadIdx.x == 0) rstate[5] = -1;   // the slot area is reused from here on
         if (l == 0) stamp(53);
         operand_tasks(p, ly);
