@@ -1420,6 +1420,11 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         ta.rt = small ? sm.rt : nullptr;
         if (l != 0 || p.layer_base != 0) ta.trace = nullptr;
         persist_expert_phase<kLarge>(ta, &ly.maps, smem_raw, tmem, &rs, deadline);
+        // the loader warps are done with the phase before the other roles (once the producer
+        // has no more items): they run the combine code once without storing, so this SM's
+        // instruction cache holds it when the combine starts after the barrier
+        if (!p.norm && tc_loader_index((int)(threadIdx.x >> 5)) >= 0)
+            combine_elems(p, l, small ? sm.rt : nullptr, sm.slots, true);
         // the next layer's first router unit, ahead of time
         if (l + 1 < p.L && router_first<kLarge>(units) < router_end<kLarge>(units)) {
             fence_proxy_async_shared();
