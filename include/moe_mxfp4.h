@@ -252,6 +252,21 @@ int moe_mxfp4_packed_bytes(int32_t hidden, int32_t inter, int32_t num_experts, s
 int moe_mxfp4_pack(int32_t hidden, int32_t inter, int32_t num_experts, const moe_mxfp4_layer* layer,
                    void* packed_dev, size_t packed_bytes, void* stream);
 
+/* The activation encoding of the expert kernels, on its own (see moe_mxfp4_forward's
+ * arithmetic note): each fp32 value of a 32-element block becomes the sum of E2M1 terms
+ * with one E8M0 scale per term and block.  Term j has scale X_j = 2^(floor(log2 m_j) - 2),
+ * doubled when m_j > 6 X_j, where m_j is the largest magnitude of the block's residual
+ * after terms 0..j-1; its codes round residual / X_j to the nearest E2M1 value (ties to
+ * the even code); a residual below 2^-119 ends the sum (its terms are code 0, scale byte
+ * 0).  Each term at least quarters the block's largest residual, so the first t terms
+ * are within 4^-t of the block's largest magnitude (the kernels use t = 8, or t = 4 for
+ * the dense operand of larger blocks).  x_dev: fp32 [n_blocks, 32]; codes_dev: uint32
+ * [n_blocks, 32] (element i: term j's code in bits 4j..4j+3, 8 terms); scales_dev: uint8
+ * [n_blocks, 8] (term j's E8M0 byte).  Device pointers, asynchronous on stream; NaN
+ * inputs are not supported.  MOE_ERR_INVALID_ARG for n_blocks < 0 or a NULL pointer. */
+int moe_mxfp4_split_terms(const float* x_dev, int64_t n_blocks, uint32_t* codes_dev, uint8_t* scales_dev,
+                          void* stream);
+
 /* MXFP4 conversion of an fp32 matrix w_dev [rows, cols] (cols a multiple of 32)
  * into nibbles q_dev [rows, cols/2] and E8M0 scales s_dev [rows, cols/32], by the
  * OCP MX v1.0 rule: per block of 32, X = 2^(floor(log2 amax) - 2) (byte clamped to

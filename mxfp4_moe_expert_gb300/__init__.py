@@ -42,6 +42,7 @@ EXPORTED = (
     "moe_mxfp4_accept",
     "moe_mxfp4_packed_bytes",
     "moe_mxfp4_pack",
+    "moe_mxfp4_split_terms",
 )
 
 MOE_MXFP4_STATIC_WORKSPACE_BYTES = 16 << 20
@@ -130,6 +131,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_mxfp4_pack.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(moe_mxfp4_layer),
                                    P, ctypes.c_size_t, P]
     lib.moe_mxfp4_pack.restype = ctypes.c_int
+    lib.moe_mxfp4_split_terms.argtypes = [P, ctypes.c_int64, P, P, P]
+    lib.moe_mxfp4_split_terms.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -207,6 +210,10 @@ def moe_mxfp4_pack(hidden, inter, num_experts, layer: moe_mxfp4_layer, packed_pt
                                          stream_ptr)
 
 
+def moe_mxfp4_split_terms(x_ptr, n_blocks, codes_ptr, scales_ptr, stream_ptr) -> int:
+    return load_library().moe_mxfp4_split_terms(x_ptr, n_blocks, codes_ptr, scales_ptr, stream_ptr)
+
+
 # ----------------------------------------------------------------------------- torch convenience
 
 
@@ -252,6 +259,17 @@ def accept(logits, tokens, stream=None):
     _check(moe_mxfp4_accept(logits.data_ptr(), tokens.data_ptr(), S, B, V, target.data_ptr(), acc.data_ptr(),
                             nxt.data_ptr(), st), "moe_mxfp4_accept")
     return target, acc, nxt
+
+
+def split_terms(x, stream=None):
+    """x: fp32 CUDA [n, 32] blocks.  Returns (codes uint32 [n, 32], scales uint8 [n, 8])."""
+    import torch
+    n = x.shape[0]
+    codes = torch.empty((n, 32), dtype=torch.int32, device=x.device)
+    scales = torch.empty((n, 8), dtype=torch.uint8, device=x.device)
+    st = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+    _check(moe_mxfp4_split_terms(x.data_ptr(), n, codes.data_ptr(), scales.data_ptr(), st), "moe_mxfp4_split_terms")
+    return codes, scales
 
 
 def quantize(w, q=None, s=None, stream=None):

@@ -661,3 +661,36 @@ extern "C" int moe_mxfp4_forward_static(moe_mxfp4_handle* h, const void* x_dev, 
     if (r != MOE_OK) return r;
     return moe_mxfp4_check(h, ws, stream);
 }
+
+// ---- the activation encoding on its own (moe_mxfp4_split_terms) -----------------------
+// Each value of a 32-element block becomes a sum of E2M1 terms with per-block E8M0
+// scales (split_e2m1_terms, the same device function the kernels use), so callers and
+// tests can check the encoding against its error bound directly.
+
+namespace moe {
+
+// One warp per 32-element block (lane = element): codes[b * 32 + lane] = the element's 8
+// term codes (term j in bits 4j..4j+3), scales[b * 8 + j] = term j's E8M0 byte.
+__global__ void split_terms_kernel(const float* __restrict__ x, int64_t n_blocks, uint32_t* __restrict__ codes,
+                                   uint8_t* __restrict__ scales) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks; b += warps) {
+        uint32_t sb0, sb1;
+        const uint32_t c = split_e2m1_terms(x[b * 32 + lane], sb0, sb1);
+        codes[b * 32 + lane] = c;
+        if (lane < kTcTerms) scales[b * kTcTerms + lane] = (uint8_t)((lane < 4 ? sb0 : sb1) >> (8 * (lane & 3)));
+    }
+}
+
+}  // namespace moe
+
+extern "C" int moe_mxfp4_split_terms(const float* x_dev, int64_t n_blocks, uint32_t* codes_dev, uint8_t* scales_dev,
+                                     void* stream) {
+    if (n_blocks < 0 || (n_blocks > 0 && (!x_dev || !codes_dev || !scales_dev))) return MOE_ERR_INVALID_ARG;
+    if (n_blocks == 0) return MOE_OK;
+    const int64_t blocks = (n_blocks + 7) / 8;
+    moe::split_terms_kernel<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        x_dev, n_blocks, codes_dev, scales_dev);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
