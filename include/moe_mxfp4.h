@@ -31,8 +31,14 @@
  *  - Calls are asynchronous on the given stream (a cudaStream_t passed as void*,
  *    NULL = legacy default stream) unless stated otherwise.  Errors the host can
  *    see are returned at once; errors found on the device (a NaN scale byte, a
- *    device wait that timed out) are written to a status word in the workspace
- *    and returned by moe_mxfp4_check.  No call aborts or throws.
+ *    device wait that timed out, a workspace whose state section was overwritten)
+ *    are written to a status word in the workspace and returned by moe_mxfp4_check.
+ *    In the persistent forward (the default) such an error stays there: later
+ *    forwards on that workspace do nothing until moe_mxfp4_check (or
+ *    moe_mxfp4_forward_host, or moe_mxfp4_forward_static) reads it, which also
+ *    returns the workspace's state section to rest.  The per-phase paths
+ *    (MOE_FLAG_MULTI_KERNEL) clear the status words at the start of each forward.
+ *    No call aborts or throws.
  *  - One handle + one workspace may be used by one stream at a time.
  *
  * Layouts (row-major, contraction dimension contiguous):
@@ -74,7 +80,8 @@ extern "C" {
 #define MOE_ERR_CUDA        (-3) /* a CUDA runtime call failed */
 #define MOE_ERR_TIMEOUT     (-4) /* a device-side wait gave up (grid barrier / expert counter) */
 #define MOE_ERR_BAD_SCALE   (-5) /* an E8M0 scale byte of a routed expert is 0xFF (NaN) */
-#define MOE_ERR_WORKSPACE   (-6) /* workspace NULL, misaligned (256 B) or too small */
+#define MOE_ERR_WORKSPACE   (-6) /* workspace NULL, misaligned (256 B) or too small; on the device:
+                                      its state section was overwritten between forwards */
 
 /* ---- config flags ------------------------------------------------------- */
 #define MOE_FLAG_NORM         (1u << 0) /* pre-norm residual stack (see above) */
@@ -147,7 +154,9 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
                      moe_mxfp4_handle** out);
 
 /* Bytes of device workspace a forward over num_tokens tokens needs.  The first 512
- * bytes hold the status words; in a persistent forward, bytes 64..511 receive CTA 0's
+ * bytes hold the status words (code at 0, detail at 4), the grid-barrier word (16), the
+ * routing flag (20), the abort flag (24) and the state tag (32, uint64); in a persistent
+ * forward, bytes 64..511 receive CTA 0's
  * %globaltimer (uint64 ns) at the end of each phase (entry i at 64 + 8 i: start,
  * input staging, and per layer l < 8: router 2+4l, routing 3+4l, experts 4+4l, combine
  * 5+4l; for the first layer also the routing sub-steps at 34..38 (blocks routed through
@@ -163,7 +172,15 @@ int moe_mxfp4_workspace_bytes(const moe_mxfp4_handle* h, int32_t num_tokens, siz
 
 /* Runs the layer (stack) on num_tokens rows of x_dev into y_dev.  workspace_dev
  * must be 256-byte aligned and at least moe_mxfp4_workspace_bytes long; its
- * contents need no initialisation and are overwritten.  x_dev and y_dev may not
+ * contents need no initialisation.  The persistent forward keeps a state section at
+ * the start of the workspace (16 KB of status words, then the counters of its work
+ * queues; the same bytes for every num_tokens) between forwards: each launch leaves it
+ * at rest, so the forward is one kernel launch with no clearing copy before it.  The
+ * library zeroes the section (one small extra launch) the first time this handle's
+ * persistent forward meets the workspace, after another handle or a per-phase forward
+ * used it, and after an error was read from it.  Between forwards the caller leaves
+ * the section's bytes alone; if something else wrote them, the forward finds a wrong
+ * state tag, records MOE_ERR_WORKSPACE and does nothing.  x_dev and y_dev may not
  * alias each other or the workspace.  num_tokens == 0 is a no-op.  dbg may be NULL.
  * Arithmetic: the router's products are exact and summed in fp32; each expert weight
  * is its exact MXFP4 value; each activation (the layer input, and h = silu(g) * u)
@@ -189,8 +206,11 @@ int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens
 int moe_mxfp4_forward_host(moe_mxfp4_handle* h, const void* x_host, int32_t num_tokens, void* y_host,
                            void* workspace_dev, size_t workspace_bytes, void* stream);
 
-/* Synchronises the stream and returns the device status word of the last
- * forward that used this workspace (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_BAD_SCALE). */
+/* Synchronises the stream and returns the device status word of this workspace: the
+ * first error a persistent forward recorded since the status was last read, or the
+ * last per-phase forward's status (MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_BAD_SCALE or
+ * MOE_ERR_WORKSPACE).  After an error it returns the state section to rest, so the
+ * next forward runs normally. */
 int moe_mxfp4_check(moe_mxfp4_handle* h, const void* workspace_dev, void* stream);
 
 /* Frees the handle (its host memory, including the pinned status buffer of

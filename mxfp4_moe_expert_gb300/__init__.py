@@ -315,6 +315,18 @@ class MoeLayers:
         import torch
         return torch.empty(self.workspace_bytes(num_tokens), dtype=torch.uint8, device=device)
 
+    def _own_workspace(self, num_tokens: int, device):
+        """The workspace forward() uses when the caller passes none: one per device, kept
+        here and grown when a larger block needs more (a workspace carries the persistent
+        forward's state section from one forward to the next, so it is not re-allocated)."""
+        cache = self.__dict__.setdefault("_ws", {})
+        key = str(device)
+        need = self.workspace_bytes(num_tokens)
+        ws = cache.get(key)
+        if ws is None or ws.numel() < need:
+            ws = cache[key] = self.new_workspace(num_tokens, device)
+        return ws
+
     def debug_buffers(self, num_tokens: int, device="cuda"):
         import torch
         L, T, k, E = self.num_layers, num_tokens, self.top_k, self.num_experts
@@ -343,7 +355,7 @@ class MoeLayers:
             y = torch.empty((T, self.hidden), dtype=torch.bfloat16 if self.out_bf16 else torch.float32,
                             device=x.device)
         if workspace is None:
-            workspace = self.new_workspace(T, x.device)
+            workspace = self._own_workspace(T, x.device)
         st = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
         _check(moe_mxfp4_forward(self.handle, x.data_ptr(), T, y.data_ptr(), workspace.data_ptr(),
                                  workspace.numel(), st, dbg), "moe_mxfp4_forward")
@@ -361,6 +373,7 @@ class MoeLayers:
         if getattr(self, "handle", None):
             moe_mxfp4_destroy(self.handle)
             self.handle = None
+        self.__dict__.pop("_ws", None)
 
     def __del__(self):
         try:

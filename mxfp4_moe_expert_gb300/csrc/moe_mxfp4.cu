@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -57,21 +58,27 @@ size_t max_items(const moe_mxfp4_config& c, int T) {
     return max_chunks(c, T) * (size_t)(c.inter / moe::kTmaRows + c.hidden / moe::kTmaRows);
 }
 
-// Per-launch counters of the persistent forward: per layer the expert-phase queue,
-// per-chunk done counters and per-expert-group router counters.
-size_t tickets_bytes(const moe_mxfp4_config& c, int T) {
-    return (size_t)moe::kMaxPersistLayers * (1 + max_chunks(c, T) + 32) * 4;
+// Counters of the persistent forward: per layer the expert-phase queue, per-chunk done
+// counters and per-expert-group router counters.  Sized for the handle's largest block,
+// so that the section sits at the same place, with the same size, whatever the block.
+size_t tickets_bytes(const moe_mxfp4_config& c) {
+    return (size_t)moe::kMaxPersistLayers * (1 + max_chunks(c, c.max_tokens) + 32) * 4;
 }
+
+// The workspace's state words: status words, grid-barrier word, flags, state tag, phase
+// timestamps and trace (16 KB), then the counters.  At rest between persistent forwards.
+constexpr size_t kStatusBytes = 16384;
+constexpr size_t kStateTagOffset = 32;
+size_t state_bytes(const moe_mxfp4_config& c) { return kStatusBytes + tickets_bytes(c); }
 
 WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     WsLayout L{};
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     const size_t H = (size_t)c.hidden, I = (size_t)c.inter, E = (size_t)c.num_experts, k = (size_t)c.top_k;
-    L.status = take(16384);   // status words, grid-barrier counters, phase timestamps, expert-phase trace
-    // the persistent forward's per-launch counters follow directly, so that one memset
-    // clears the status words and the counters
-    L.tickets = take(tickets_bytes(c, T));
+    L.status = take(kStatusBytes);   // status words, grid-barrier word, state tag, timestamps, trace
+    // the persistent forward's counters follow directly: one contiguous state section
+    L.tickets = take(tickets_bytes(c));
     L.xstage = take((size_t)T * H * 2);
     L.ystage = take((size_t)T * H * 4);
     L.act = take((size_t)T * H * 4);
@@ -101,6 +108,60 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     L.xcs = take(gathered ? chunks * (H / 256) * 512 : 0);
     L.total = o;
     return L;
+}
+
+// ---- the workspace's state section at rest ----
+// A persistent forward leaves the state section as it found it (zero counters, the
+// barrier word at rest), so it issues no clearing copy.  The host zeroes the section,
+// and writes the state tag, the first time a handle's persistent forward meets a
+// workspace, after any other forward wrote the section, and after an error was read.
+// The table records which handle last left each workspace's section at rest.
+std::mutex g_state_mu;
+std::unordered_map<const void*, const moe_mxfp4_handle*> g_state_owner;
+
+unsigned long long state_tag(const moe_mxfp4_handle* h) {
+    return 0x6d6f652d73746174ull ^ ((unsigned long long)reinterpret_cast<uintptr_t>(h) * 0x9E3779B97F4A7C15ull) ^
+           (unsigned long long)state_bytes(h->cfg);
+}
+
+__global__ void state_init_kernel(uint4* base, size_t n16, unsigned long long tag) {
+    for (size_t i = threadIdx.x; i < n16; i += blockDim.x) base[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (threadIdx.x == 0) reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(base) + kStateTagOffset)[0] = tag;
+}
+
+// Zeroes the state section of ws and writes h's tag, unless h's persistent forward left
+// it at rest (force: always).  Caller holds no lock.
+int state_to_rest(const moe_mxfp4_handle* h, char* ws, cudaStream_t st, bool force) {
+    std::lock_guard<std::mutex> lock(g_state_mu);
+    auto it = g_state_owner.find(ws);
+    if (!force && it != g_state_owner.end() && it->second == h) return MOE_OK;
+    state_init_kernel<<<1, 512, 0, st>>>(reinterpret_cast<uint4*>(ws), state_bytes(h->cfg) / 16, state_tag(h));
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    // a launch captured into a graph has not run: the section is at rest only once it does
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return MOE_OK;
+    if (g_state_owner.size() >= 4096) g_state_owner.clear();   // forgetting only costs a re-zeroing
+    g_state_owner[ws] = h;
+    return MOE_OK;
+}
+
+// Another forward path writes the state section of ws: its next persistent forward re-zeroes it.
+void state_forget(const void* ws) {
+    std::lock_guard<std::mutex> lock(g_state_mu);
+    g_state_owner.erase(ws);
+}
+
+// After an error was read from ws: re-zero the state section if h's persistent forward owns it.
+void state_after_error(const moe_mxfp4_handle* h, char* ws, cudaStream_t st) {
+    bool owned;
+    {
+        std::lock_guard<std::mutex> lock(g_state_mu);
+        auto it = g_state_owner.find(ws);
+        owned = it != g_state_owner.end() && it->second == h;
+    }
+    if (owned) state_to_rest(h, ws, st, true);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -370,7 +431,7 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     }
     p.ta.abort = p.wl.abort;
     if (c.flags & MOE_FLAG_TRACE) p.ta.trace = reinterpret_cast<unsigned long long*>(ws + L.status + 4096);
-    const int chunks = (int)max_chunks(c, T);
+    const int chunks = (int)max_chunks(c, c.max_tokens);   // the counter section's layout (tickets_bytes)
     p.chunk_stride = chunks;
     p.queues = reinterpret_cast<int*>(ws + L.tickets);
     p.dones = p.queues + moe::kMaxPersistLayers;
@@ -417,6 +478,8 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     p.bar = reinterpret_cast<unsigned*>(ws + L.status + 16);
     p.route_flag = reinterpret_cast<int*>(ws + L.status + 20);
     p.tstamp = reinterpret_cast<unsigned long long*>(ws + L.status + 64);
+    p.state_tag = reinterpret_cast<const unsigned long long*>(ws + L.status + kStateTagOffset);
+    p.tag = state_tag(h);
     if (dbg) {
         p.dbg.idx = dbg->topk_idx_dev;
         p.dbg.gate = dbg->topk_gate_dev;
@@ -424,9 +487,8 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
         p.dbg.offsets = dbg->expert_offsets_dev;
         p.dbg.perm = dbg->perm_dev;
     }
-    // one memset: status words, abort flag, grid-barrier counter and the first launch's counters
-    if (cudaMemsetAsync(ws + L.status, 0, (L.tickets - L.status) + tickets_bytes(c, T), st) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    // the state section is at rest (every launch returns it there), so nothing is cleared here
+    if (const int r = state_to_rest(h, ws, st, false)) return r;
     for (int l0 = 0; l0 < c.num_layers; l0 += moe::kMaxPersistLayers) {
         const int nl = std::min(moe::kMaxPersistLayers, c.num_layers - l0);
         p.L = nl;
@@ -440,9 +502,6 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
             p.layer[l].router_b = ly.router_b_dev;
             p.layer[l].norm_w = reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev);
         }
-        if (l0 > 0 && (cudaMemsetAsync(ws + L.status + 16, 0, 8, st) != cudaSuccess ||
-                        cudaMemsetAsync(ws + L.tickets, 0, tickets_bytes(c, T), st) != cudaSuccess))
-            return MOE_ERR_CUDA;
         void* kargs[] = {&p};
         const void* kern = p.ta.xc4 ? reinterpret_cast<const void*>(moe::persist_kernel<true>)
                                     : reinterpret_cast<const void*>(moe::persist_kernel<false>);
@@ -573,8 +632,10 @@ int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens
     if (h->tma && num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok) {
         const bool events = dbg && dbg->expert_events;
         if (h->persist_grid > 0 && !(h->cfg.flags & MOE_FLAG_MULTI_KERNEL) && !events)
-            return forward_persistent(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);   // clears the status itself
+            return forward_persistent(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
     }
+    // the per-phase paths clear the status words per forward (and with them the state tag)
+    state_forget(ws);
     if (cudaMemsetAsync(ws + L.status, 0, 64, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (h->tma && num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok)
         return forward_tma(h, x_dev, num_tokens, y_dev, ws, L, st, dbg);
@@ -608,7 +669,9 @@ int moe_mxfp4_forward_host(moe_mxfp4_handle* h, const void* x_host, int32_t num_
     if (cudaMemcpyAsync(h->status_host, workspace_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
-    return h->status_host[0];
+    const int s0 = h->status_host[0];
+    if (s0 != MOE_OK) state_after_error(h, ws, st);
+    return s0;
 }
 
 int moe_mxfp4_check(moe_mxfp4_handle* h, const void* workspace_dev, void* stream) {
@@ -617,10 +680,19 @@ int moe_mxfp4_check(moe_mxfp4_handle* h, const void* workspace_dev, void* stream
     if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
     int s[2] = {0, 0};
     if (cudaMemcpy(s, workspace_dev, sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (s[0] != MOE_OK) state_after_error(h, static_cast<char*>(const_cast<void*>(workspace_dev)), st);
     return s[0];
 }
 
-void moe_mxfp4_destroy(moe_mxfp4_handle* h) { delete h; }
+void moe_mxfp4_destroy(moe_mxfp4_handle* h) {
+    if (!h) return;
+    {
+        std::lock_guard<std::mutex> lock(g_state_mu);
+        for (auto it = g_state_owner.begin(); it != g_state_owner.end();)
+            it = it->second == h ? g_state_owner.erase(it) : std::next(it);
+    }
+    delete h;
+}
 
 }  // extern "C"
 

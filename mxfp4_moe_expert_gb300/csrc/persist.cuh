@@ -76,16 +76,18 @@ struct PersistParams {
     int chunk;         // pairs per chunk of a block routed through the workspace (8, or 16 dense)
     int terms;         // E2M1 terms per activation in those chunks (8, or 4 dense)
     int rtok;          // tokens per router unit (T for blocks routed in shared memory; else a multiple of 8 G)
-    int* rcnt;         // [kMaxPersistLayers, 32] finished router units per expert group (zeroed per launch)
+    int* rcnt;         // [kMaxPersistLayers, 32] finished router units per expert group (0 at rest)
     unsigned long long* tstamp;   // CTA 0's %globaltimer at phase ends (or NULL)
     TcArgs ta;         // expert phase: operands, partial, status, timeout (per-layer fields set per layer)
     RouteBufs rb;
     WorkList wl;       // items / n_items / abort for larger blocks
-    int* queues;       // [kMaxPersistLayers] expert-phase queue per layer (zeroed per launch)
-    int* dones;        // [kMaxPersistLayers, chunk_stride] finished gate/up items per chunk (zeroed per launch)
+    int* queues;       // [kMaxPersistLayers] expert-phase queue per layer (0 at rest)
+    int* dones;        // [kMaxPersistLayers, chunk_stride] finished gate/up items per chunk (0 at rest)
     int chunk_stride;
-    unsigned* bar;     // grid barrier counter (zeroed per forward)
-    int* route_flag;   // layers routed so far (zeroed per forward)
+    unsigned* bar;     // grid barrier word (low 31 bits 0 at rest; see grid_arrive)
+    int* route_flag;   // layers routed so far in this launch (0 at rest)
+    const unsigned long long* state_tag;   // the workspace's state tag (see persist_kernel)
+    unsigned long long tag;                // its expected value
     PersistDebug dbg;
 };
 
@@ -100,24 +102,29 @@ __device__ __forceinline__ bool aborted(const int* abort) {
 }
 
 // All CTAs of the grid meet; bounded.  grid_arrive announces this CTA (after every
-// thread's earlier writes), grid_wait waits for every CTA's arrival of the same epoch;
+// thread's earlier writes), grid_wait waits for every CTA's arrival at the same barrier;
 // work between the two must not depend on the other CTAs.  grid_wait returns false (in
 // every thread) on timeout / abort.
-__device__ __forceinline__ void grid_arrive(unsigned* bar, unsigned& epoch, bool withhold = false) {
+// One 32-bit word serves every barrier of every launch and returns to its resting value
+// by itself: each CTA adds 1, except CTA 0, which adds 2^31 - (G - 1).  The G additions
+// of one barrier sum to 2^31, so the low 31 bits are back to 0 and bit 31 has flipped;
+// bit 31 flips only with the last addition (before it, the sum is short of 2^31 or CTA
+// 0's term has borrowed from bit 31), and each CTA waits until bit 31 differs from the
+// value its own addition returned.  No launch needs the word cleared.
+__device__ __forceinline__ void grid_arrive(unsigned* bar, unsigned& token, bool withhold = false) {
     __syncthreads();
-    ++epoch;
     if (threadIdx.x == 0) {
         __threadfence();
-        if (!withhold) atomicAdd(bar, 1u);
+        const unsigned add = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1u) : 1u;
+        token = withhold ? ld_acquire_u32(bar) : atomicAdd(bar, add);
     }
 }
-__device__ __forceinline__ bool grid_wait(unsigned* bar, unsigned epoch, unsigned long long deadline, int* abort,
+__device__ __forceinline__ bool grid_wait(unsigned* bar, unsigned token, unsigned long long deadline, int* abort,
                                           int* status) {
     int failed = 0;
     if (threadIdx.x == 0) {
-        const unsigned target = epoch * gridDim.x;
         uint32_t spins = 0;
-        while (ld_acquire_u32(bar) < target) {
+        while (((ld_acquire_u32(bar) ^ token) & 0x80000000u) == 0u) {
             if ((++spins & 63u) == 0 && (globaltimer_ns() > deadline || aborted(abort))) {
                 failed = 1;
                 if (atomicExch(abort, 1) == 0) raise_status(status, MOE_ERR_TIMEOUT, -1);
@@ -127,10 +134,10 @@ __device__ __forceinline__ bool grid_wait(unsigned* bar, unsigned epoch, unsigne
     }
     return __syncthreads_or(failed) == 0;
 }
-__device__ __forceinline__ bool grid_sync(unsigned* bar, unsigned& epoch, unsigned long long deadline,
+__device__ __forceinline__ bool grid_sync(unsigned* bar, unsigned& token, unsigned long long deadline,
                                           int* abort, int* status, bool withhold = false) {
-    grid_arrive(bar, epoch, withhold);
-    return grid_wait(bar, epoch, deadline, abort, status);
+    grid_arrive(bar, token, withhold);
+    return grid_wait(bar, token, deadline, abort, status);
 }
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -459,6 +466,7 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
         __threadfence();
         const int old = atomicAdd(p.rcnt + l * 32 + eg, 1);
         *flag = old == n_sl - 1;
+        if (old == n_sl - 1) atomicExch(p.rcnt + l * 32 + eg, 0);   // every unit counted: back to rest
         __threadfence();
     }
     __syncthreads();
@@ -1324,7 +1332,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     int* status = p.ta.status;
     float* red = sm.red;                                   // block reductions (<= 32 floats)
     float* xs = reinterpret_cast<float*>(sm.slots);        // routing scratch
-    unsigned epoch = 0;
+    unsigned btok = 0;   // thread 0: the grid-barrier word as this CTA's last arrival found it
     TcRoleState rs{0u, 0u, 0u, 0u};
     int* rstate = reinterpret_cast<int*>(sm.red + 40);     // router-weight copy state (router_fetch)
     const int units = p.rfull ? router_full_units(p) : router_units(p);
@@ -1336,7 +1344,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     stamp(0);   // (the first router unit's copies were issued before the setup)
     if (p.norm && p.init_from_x) {
         for (int u = blockIdx.x; u < cunits; u += gridDim.x) stack_init_unit(p, u, red);
-        if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
+        if (!grid_sync(p.bar, btok, deadline, abort, status)) return;
     }
     stamp(1);
 
@@ -1353,7 +1361,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         operand_tasks(p, ly);
         if (l == 0) stamp(54);
         const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
-        grid_arrive(p.bar, epoch, withhold);
+        grid_arrive(p.bar, btok, withhold);
         if (small && blockIdx.x >= units) {
             // a CTA without a router unit would only wait at the barrier: after arriving it
             // runs the routing code (results discarded; shared memory only) or, on every other
@@ -1363,7 +1371,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
             else if (p.norm) combine_unit(p, blockIdx.x % cunits, l, red, nullptr, true);
             else combine_elems(p, l, nullptr, sm.slots, true);
         }
-        if (!grid_wait(p.bar, epoch, deadline, abort, status)) return;
+        if (!grid_wait(p.bar, btok, deadline, abort, status)) return;
         stamp(2 + 4 * l);
         if (small) {
             route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
@@ -1375,10 +1383,10 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
                 if (l == 0) stamp(34 + i);
             };
             logits_reduce(p, ly);
-            if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
+            if (!grid_sync(p.bar, btok, deadline, abort, status)) return;
             lstamp(0);
             topk_tokens(p);
-            if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
+            if (!grid_sync(p.bar, btok, deadline, abort, status)) return;
             lstamp(1);
             if (blockIdx.x == 0) {
                 route_phase(p, ly, l, reinterpret_cast<int*>(xs));
@@ -1407,7 +1415,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
             gather_chunk_operand(p, reinterpret_cast<const int*>(xs), sm.slots);
             fence_proxy_async_global();   // read next by the expert phase's bulk copies
             lstamp(4);
-            if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
+            if (!grid_sync(p.bar, btok, deadline, abort, status)) return;
             stamp(3 + 4 * l);
         }
         // the slots were written through the generic proxy; TMA writes them next
@@ -1436,25 +1444,52 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
             }
         }
         if (small && blockIdx.x == 0) publish_small(p, l, sm.rt);
-        if (!grid_sync(p.bar, epoch, deadline, abort, status)) return;
+        if (!grid_sync(p.bar, btok, deadline, abort, status)) return;
         stamp(4 + 4 * l);
+        // the layer's expert phase is over in every CTA: its queue, done counters and the
+        // routing flag go back to rest for the next launch (nothing reads them again here)
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= p.chunk_stride; i += gridDim.x * blockDim.x) {
+            if (i == 0) p.queues[l] = 0;
+            else p.dones[(size_t)l * p.chunk_stride + i - 1] = 0;
+        }
+        if (!small && blockIdx.x == 0 && threadIdx.x == 0) *p.route_flag = 0;
         if (p.norm)
             for (int u = blockIdx.x; u < cunits; u += gridDim.x) combine_unit(p, u, l, red, small ? sm.rt : nullptr);
         else
             combine_elems(p, l, small ? sm.rt : nullptr, sm.slots);
         stamp(5 + 4 * l);
-        if (l + 1 < p.L && !grid_sync(p.bar, epoch, deadline, abort, status)) return;
+        if (l + 1 < p.L && !grid_sync(p.bar, btok, deadline, abort, status)) return;
     }
 }
 
+// The counters, flags and the grid-barrier word in the workspace are at rest (zero) when
+// a launch starts and are returned to rest by the launch itself, so a forward issues no
+// clearing copy before its kernel.  The host zeroes them once per workspace and writes
+// the state tag beside them; a launch that finds another tag (the memory was used for
+// something else since) records MOE_ERR_WORKSPACE and does nothing, and one that finds
+// the abort flag of an earlier failed launch (its counters may not be at rest) does
+// nothing either: the error stays in the status words until the host reads it and
+// re-zeroes the state.
 template <bool kLarge>
 __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_constant__ PersistParams p) {
     extern __shared__ uint8_t smem_raw[];
     const TcSmem sm = tc_smem(smem_raw);
+    // every thread reads the tag and the abort flag (nothing in this launch writes either
+    // before its first grid barrier, so all threads see the same values); used after the setup
+    const unsigned long long tag = *reinterpret_cast<const volatile unsigned long long*>(p.state_tag);
+    const int aborted_before = *reinterpret_cast<const volatile int*>(p.wl.abort);
     router_first_copies<kLarge>(p, sm, reinterpret_cast<int*>(sm.red + 40));   // in flight during the setup
     const uint32_t tmem = tc_setup(sm);
     const unsigned long long deadline = globaltimer_ns() + p.ta.timeout_ns;
-    persist_layers<kLarge>(p, smem_raw, tmem, deadline);
+    if (tag != p.tag) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            p.ta.status[0] = MOE_ERR_WORKSPACE;
+            p.ta.status[1] = 0;
+            *p.wl.abort = 1;
+        }
+    } else if (aborted_before == 0) {
+        persist_layers<kLarge>(p, smem_raw, tmem, deadline);
+    }
     __syncthreads();
     if (threadIdx.x == 0 && p.tstamp && blockIdx.x < 256)   // when each CTA finished (profiling)
         p.tstamp[56 + blockIdx.x] = globaltimer_ns();
