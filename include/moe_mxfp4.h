@@ -182,7 +182,11 @@ int moe_mxfp4_workspace_bytes(const moe_mxfp4_handle* h, int32_t num_tokens, siz
  * the section's bytes alone; if something else wrote them, the forward finds a wrong
  * state tag, records MOE_ERR_WORKSPACE and does nothing.  x_dev and y_dev may not
  * alias each other or the workspace.  num_tokens == 0 is a no-op.  dbg may be NULL.
- * Arithmetic: the router's products are exact and summed in fp32; each expert weight
+ * Arithmetic: the router's products of x are exact and summed in fp32; in a residual
+ * stack, RMSNorm(r) = (r * w_norm) / rms(r) with one factor 1 / rms(r) per token, so the
+ * router sums the fp32 products of y = r * w_norm (fp32) with its bf16 weights per
+ * 256-column block, in block order, and scales the sum by the factor, and the experts
+ * take y as their input and scale their gate/up outputs by it; each expert weight
  * is its exact MXFP4 value; each activation (the layer input, and h = silu(g) * u)
  * enters the tensor cores as a sum of E2M1 terms with per-32 E8M0 scales, each term
  * encoding the residual of the previous ones.  A block of at most 64 (token, slot)

@@ -816,7 +816,10 @@ __device__ __forceinline__ void group4_reduce_scatter(const float (&v)[32], floa
 // sums of columns 32c + 4s + (l % 4) and 128 + .., s = 0..7.
 // The warp reads columns 32c.. (gate rows / first down block) and 128 + 32c.. (up rows /
 // second down block).
-template <bool kDense>
+// kNorm (residual stack): the layer input's operand is r * w_norm without the per-token
+// factor 1 / rms(r), which the gate/up outputs take here, from the shared-memory routing
+// table: its tscale (a.rt set: the block was routed in shared memory) or tscale_g.
+template <bool kDense, bool kNorm>
 __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in, uint32_t tmem, TcRoleState& rs_in,
                                          int warp, int lane, unsigned long long deadline) {
     constexpr int kT = kDense ? 4 : kTcTerms;   // terms per activation: lanes (accumulator rows) per pair
@@ -877,6 +880,14 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
             // 32c.. are one MX block of the down projection's K.  Split into kT E2M1 terms
             // with block scales over the pair's kT lanes, stored as rows kT p + t of the
             // chunk's down operand at K = rb * 128 + 32c + kT s + j.
+            if constexpr (kNorm) {   // g and u of RMSNorm(r) = (g and u of r * w_norm) / rms(r), per token
+                const float sc = mine ? (a.rt ? a.rt->tscale[my_id] : __ldcg(s.rt->tscale_g + my_id)) : 1.0f;
+#pragma unroll
+                for (int i = 0; i < kV; ++i) {
+                    G[i] *= sc;
+                    U[i] *= sc;
+                }
+            }
             float hv[kV];
 #pragma unroll
             for (int i = 0; i < kV; ++i) hv[i] = silu(G[i]) * U[i];
@@ -944,7 +955,7 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
 }
 
 // One expert phase, dispatched by warp role; every thread of the block calls it.
-template <bool kGathered>
+template <bool kGathered, bool kNorm = false>
 __device__ __forceinline__ void tc_phase(const TcMaps& maps, const TcArgs& a, const TcSmem& s, uint32_t tmem,
                                          TcRoleState& rs, unsigned long long deadline) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -957,8 +968,8 @@ __device__ __forceinline__ void tc_phase(const TcMaps& maps, const TcArgs& a, co
     } else if (tc_loader_index(warp) >= 0) {
         tc_load(a, s, rs, tc_loader_index(warp), lane, deadline);
     } else if (tc_is_epi_warp(warp)) {
-        if (kGathered && a.dense) tc_epilogue<true>(a, s, tmem, rs, warp, lane, deadline);
-        else tc_epilogue<false>(a, s, tmem, rs, warp, lane, deadline);
+        if (kGathered && a.dense) tc_epilogue<true, kNorm>(a, s, tmem, rs, warp, lane, deadline);
+        else tc_epilogue<false, kNorm>(a, s, tmem, rs, warp, lane, deadline);
     }
 }
 

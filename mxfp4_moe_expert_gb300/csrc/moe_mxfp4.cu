@@ -45,7 +45,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // Byte offsets of the workspace sections for T tokens.
 struct WsLayout {
     size_t status, xstage, ystage, act, resid, logits, idx, gate, counts, offsets, perm, active, hbuf, partial;
-    size_t xb4, xsf, ss, tickets, hb4, hsf, items, sync, rpart, chunk0, xc4, xcs, total;
+    size_t xb4, xsf, ss, tickets, hb4, hsf, items, sync, rpart, chunk0, xc4, xcs, tsc, total;
 };
 
 // Upper bound of the chunks of one layer: every routed expert contributes
@@ -100,12 +100,13 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     L.hsf = take(chunks * moe::hsf_chunk_bytes((int)I));
     L.items = take(max_items(c, T) * sizeof(moe::ItemRec));
     L.sync = take((8 + chunks) * 4);   // n_items[2], queue, abort, ..., done[chunks]
-    L.rpart = take((size_t)(H / 256 + 1) * T * E * 4);   // router partials per column slice (>= 256 columns)
+    L.rpart = take((size_t)(H / 256 + 1) * T * E * 4);   // router partials per column slice / block (>= 256 columns)
     L.chunk0 = take((E + 1) * 4);
     // larger blocks (routed through the workspace): the input operand gathered per chunk
     const bool gathered = !((size_t)T * k <= 64 && (size_t)T * E <= 8192);
     L.xc4 = take(gathered ? chunks * (H / 256) * 8192 : 0);
     L.xcs = take(gathered ? chunks * (H / 256) * 512 : 0);
+    L.tsc = take((size_t)T * 4);   // per-token 1 / rms of a residual stack (larger blocks)
     L.total = o;
     return L;
 }
@@ -430,6 +431,7 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
         }
     }
     p.ta.abort = p.wl.abort;
+    p.tscale = reinterpret_cast<float*>(ws + L.tsc);
     if (c.flags & MOE_FLAG_TRACE) p.ta.trace = reinterpret_cast<unsigned long long*>(ws + L.status + 4096);
     const int chunks = (int)max_chunks(c, c.max_tokens);   // the counter section's layout (tickets_bytes)
     p.chunk_stride = chunks;
@@ -453,7 +455,7 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
         long best = -1, best_units = 0;
         for (int w = 1024; w >= 256; w /= 2) {
             if (H % w) continue;
-            const int tp = moe::kPRouteTok * (p.norm ? 2 : 4) * (w >= 1024 ? 1 : 2);   // tokens per pass (router_groups)
+            const int tp = moe::kPRouteTok * 4 * (w >= 1024 ? 1 : 2);   // tokens per pass (router_groups)
             for (int rt = tp; rt < T + tp; rt += tp) {
                 const long units = (long)egroups * (H / w) * ((T + rt - 1) / rt);
                 const long cost = ((units + h->persist_grid - 1) / h->persist_grid) * ((rt + tp - 1) / tp);
@@ -503,8 +505,11 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
             p.layer[l].norm_w = reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev);
         }
         void* kargs[] = {&p};
-        const void* kern = p.ta.xc4 ? reinterpret_cast<const void*>(moe::persist_kernel<true>)
-                                    : reinterpret_cast<const void*>(moe::persist_kernel<false>);
+        const void* kern =
+            p.norm ? (p.ta.xc4 ? reinterpret_cast<const void*>(moe::persist_kernel<true, true>)
+                               : reinterpret_cast<const void*>(moe::persist_kernel<false, true>))
+                   : (p.ta.xc4 ? reinterpret_cast<const void*>(moe::persist_kernel<true, false>)
+                               : reinterpret_cast<const void*>(moe::persist_kernel<false, false>));
         if (cudaLaunchCooperativeKernel(kern, dim3(h->persist_grid),
                                         dim3(moe::kTcThreads), kargs, moe::kTcSmemBytes, st) != cudaSuccess)
             return MOE_ERR_CUDA;
@@ -579,18 +584,26 @@ int moe_mxfp4_create(const moe_mxfp4_config* cfg, const moe_mxfp4_layer* layers,
                                            (int)(std::min<size_t>((size_t)c.max_tokens * c.top_k, 512u * moe::kTmaTok) *
                                                  sizeof(int))) != cudaSuccess)
             h->tma = false;
-        if (h->tma &&
-            cudaFuncSetAttribute(moe::persist_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 moe::kTcSmemBytes) == cudaSuccess &&
-            cudaFuncSetAttribute(moe::persist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           moe::kTcSmemBytes) == cudaSuccess) {
-            int per_sm = 0;
+        const void* persist_kernels[] = {reinterpret_cast<const void*>(moe::persist_kernel<false, false>),
+                                         reinterpret_cast<const void*>(moe::persist_kernel<true, false>),
+                                         reinterpret_cast<const void*>(moe::persist_kernel<false, true>),
+                                         reinterpret_cast<const void*>(moe::persist_kernel<true, true>)};
+        bool persist_ok = h->tma;
+        for (const void* k : persist_kernels)
+            persist_ok = persist_ok && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                            moe::kTcSmemBytes) == cudaSuccess;
+        if (persist_ok) {
             int coop = 0;
             cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-            if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe::persist_kernel<false>, moe::kTcThreads,
-                                                                      moe::kTcSmemBytes) == cudaSuccess &&
-                per_sm >= 1)
-                h->persist_grid = prop.multiProcessorCount;
+            // one CTA per SM for every instantiation (they share the launch configuration)
+            bool fits = coop != 0;
+            for (const void* k : persist_kernels) {
+                int per_sm = 0;
+                fits = fits && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, moe::kTcThreads,
+                                                                             moe::kTcSmemBytes) == cudaSuccess &&
+                       per_sm >= 1;
+            }
+            if (fits) h->persist_grid = prop.multiProcessorCount;
         }
         cudaGetLastError();
     }

@@ -88,6 +88,7 @@ struct PersistParams {
     int* route_flag;   // layers routed so far in this launch (0 at rest)
     const unsigned long long* state_tag;   // the workspace's state tag (see persist_kernel)
     unsigned long long tag;                // its expected value
+    float* tscale;     // [T] per-token 1 / rms of a residual stack (blocks routed through the workspace)
     PersistDebug dbg;
 };
 
@@ -204,21 +205,17 @@ __device__ __forceinline__ bool route_is_small(const PersistParams& p) {
     return p.T * p.k <= kRtMaxPairs && p.T * p.E <= 8192;
 }
 
-// bf16 terms per input value of the router: the RMSNorm output of a stack is fp32 (three
-// terms hi + mid + lo carry it to 2^-24); the plain input x is bf16 already (one term).
-__device__ __forceinline__ int router_terms(const PersistParams& p) { return p.norm ? 3 : 1; }
-// Router units process G groups of 8 tokens per pass: G = 1 for a single 8-token block
-// (the 16 warps split K); larger blocks G = 2 / 4 (three terms; 1024-column slices /
-// narrower) or 4 / 8 (one term).
+// Router units (a plain input x; a residual stack forms its router products in prep_unit)
+// process G groups of 8 tokens per pass: G = 1 for a single 8-token block (the 16 warps
+// split K); larger blocks G = 4 (1024-column slices) or 8 (narrower).
 __device__ __forceinline__ int router_groups(const PersistParams& p) {
     if (p.T <= kPRouteTok) return 1;
-    return (p.norm ? 2 : 4) * (p.rslice >= 1024 ? 1 : 2);
+    return 4 * (p.rslice >= 1024 ? 1 : 2);
 }
-// Shared-memory layout of a router unit (slot area): the staged input terms
-// [8 NT G rows][stride] at 0 (NT = router_terms), the weight rows [32][stride] at
-// router_wbase, then the inverse RMS of the pass's tokens (TP floats).  stride = rslice *
-// 2 + 16 bytes (rows padded by 16 bytes: conflict-free ldmatrix).  The warps' sums
-// [16][32][24] floats (48 KB) reuse offset 0 after the MMAs.
+// Shared-memory layout of a router unit (slot area): the staged input rows
+// [8 G rows][stride] at 0, the weight rows [32][stride] at router_wbase.  stride =
+// rslice * 2 + 16 bytes (rows padded by 16 bytes: conflict-free ldmatrix).  The warps'
+// sums [16][32][24] floats (48 KB) reuse offset 0 after the MMAs.
 __device__ __forceinline__ uint32_t router_stride(const PersistParams& p) { return (uint32_t)p.rslice * 2 + 16; }
 // Router units: (weight slice r = (expert group eg of 32, column slice sl), token block tb),
 // u = r * token blocks + tb with r = eg * slices + sl: the token blocks of one weight
@@ -242,7 +239,7 @@ __device__ __forceinline__ int router_end(int units) {
 template <bool kContiguous>
 __device__ __forceinline__ int router_step() { return kContiguous ? 1 : (int)gridDim.x; }
 __device__ __forceinline__ uint32_t router_wbase(const PersistParams& p) {
-    const uint32_t a = max(8u * router_terms(p) * router_groups(p) * router_stride(p), 16u * 768u * 4u);
+    const uint32_t a = max(8u * router_groups(p) * router_stride(p), 16u * 768u * 4u);
     return (a + 1023u) & ~1023u;
 }
 
@@ -270,36 +267,18 @@ __device__ __forceinline__ void router_fetch(const PersistParams& p, const Persi
     }
 }
 
-// x = hi + mid + lo with each term a bf16 (round to nearest): the remainder is below
-// 2^-24 |x|, and every product with a bf16 weight is exact in fp32.
-__device__ __forceinline__ void split_bf16x3(float x, uint16_t& hi, uint16_t& mid, uint16_t& lo) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    const float r1 = x - __bfloat162float(h);
-    const __nv_bfloat16 m = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(m);
-    const __nv_bfloat16 l = __float2bfloat16_rn(r2);
-    hi = __bfloat16_as_ushort(h);
-    mid = __bfloat16_as_ushort(m);
-    lo = __bfloat16_as_ushort(l);
-}
-
 // Router unit u = (token block of p.rtok tokens, expert group g of 32, column slice s of
 // p.rslice columns): partial logits of the group over the slice for the block's tokens,
-// 8 G tokens per pass, on the tensor cores: per 8-token group D [32 experts x 8 NT] =
-// W [32 x K] . X^T where the 8 NT columns of X are the NT bf16 terms of the 8 tokens'
-// inputs (fp32 accumulation; every bf16 x bf16 product is exact).  NT = 3 for the
-// RMSNorm output of a stack (hi / mid / lo carry the fp32 value to within 2^-24), staged
-// through registers; NT = 1 for the bf16 input x, copied into shared memory as it is
-// (cp.async, no register round trip).  The 16 / G warps of a group split K; their
-// results are summed in a fixed order, the terms last (hi + (mid + lo)).  The weight rows
-// come into shared memory by router_fetch (issued ahead of time where possible).  The
-// unit that finishes a group last (a counter per group) sums the group's slice partials
-// in slice order and writes its logits (+ bias): the result does not depend on which
-// unit comes last.
-template <int NT>
+// 8 G tokens per pass, on the tensor cores: per 8-token group D [32 experts x 8 tokens] =
+// W [32 x K] . X^T with the bf16 input x as it is (fp32 accumulation; every bf16 x bf16
+// product is exact), copied into shared memory by cp.async.  The 16 / G warps of a group
+// split K; their results are summed in a fixed order.  The weight rows come into shared
+// memory by router_fetch (issued ahead of time where possible).  The unit that finishes a
+// group last (a counter per group) sums the group's slice partials in slice order and
+// writes its logits (+ bias): the result does not depend on which unit comes last.
 __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLayer& ly, int l, int u,
                                          const TcSmem& sm, int* rstate) {
-    static_assert(NT == 1 || NT == 3, "router input terms");
+    constexpr int NT = 1;   // bf16 terms per input value
     const int H = p.H, E = p.E, T = p.T;
     const int n_sl = H / p.rslice;
     const int n_tb = router_tblocks(p);
@@ -313,9 +292,8 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
     const int gw = warp / wpg, kp = warp % wpg;          // this warp's token group and K part
     const int ne = min(kPRouteExperts, E - eg * kPRouteExperts);
     const uint32_t stride = router_stride(p), wbase = router_wbase(p);
-    uint8_t* xt = sm.slots;                              // [8 NT G][stride]: row 8 (NT g + q) + t = term q of token t of group g
+    uint8_t* xt = sm.slots;                              // [8 G][stride]: row 8 g + t = token t of group g
     float* red = reinterpret_cast<float*>(sm.slots);     // [16 warps][32 experts][24] after the MMAs
-    float* sinv = reinterpret_cast<float*>(sm.slots + wbase + 32 * stride);   // [TP] (three terms)
     int* flag = rstate + 4;
     auto rs = [&](int i) {   // router timestamps of unit 0, or 1 with token blocks (CTA 0's second unit; profiling)
         if (u == (n_tb > 1 ? 1 : 0) && l == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[48 + i] = globaltimer_ns();
@@ -340,58 +318,12 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
         const int nt = min(TP, tend - t0);
         if (t0 > tbeg) __syncthreads();   // the previous pass's sums have been read
         if (t0 == tbeg) rs(1);
-        if constexpr (NT == 1) {
-            // the pass's rows of x as they are (rows >= nt keep stale data: their output
-            // columns are not stored); already in flight when issued with the weights
-            const int n16 = ncols / 8;   // 16-byte pieces per row
-            for (int i = x_pre ? nt * n16 : threadIdx.x; i < nt * n16; i += blockDim.x) {
-                const int t = i / n16, c = (i % n16) * 8;
-                cp_async_16(xs_a + (uint32_t)t * stride + (uint32_t)c * 2, p.x + (size_t)(t0 + t) * H + c0 + c);
-            }
-        } else {
-            for (int t = warp; t < nt; t += 16) {
-                const float v = inv_rms(p, t0 + t);
-                if (lane == 0) sinv[t] = v;
-            }
-            __syncthreads();
-            // stage the three bf16 terms of the pass's inputs (tokens >= nt: zero)
-            const int n4 = ncols / 4;
-            constexpr int kLd = 4;   // items per thread per round (loads in flight together)
-            for (int i0 = threadIdx.x; i0 < TP * n4; i0 += kLd * blockDim.x) {
-                float4 v[kLd];
-#pragma unroll
-                for (int j = 0; j < kLd; ++j) {   // loads first (in flight together), then the stores
-                    const int i = i0 + j * blockDim.x;
-                    const int t = i / n4, c = (i % n4) * 4;
-                    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (i < TP * n4 && t < nt) {
-                        const size_t o = (size_t)(t0 + t) * H + c0 + c;
-                        const float4 r = __ldcg(reinterpret_cast<const float4*>(p.resid + o));
-                        const uint2 wv = __ldg(reinterpret_cast<const uint2*>(ly.norm_w + c0 + c));
-                        const float iv = sinv[t];
-                        v[j] = make_float4(r.x * iv * bf16_lo(wv.x), r.y * iv * bf16_hi(wv.x),
-                                           r.z * iv * bf16_lo(wv.y), r.w * iv * bf16_hi(wv.y));
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < kLd; ++j) {
-                    const int i = i0 + j * blockDim.x;
-                    if (i >= TP * n4) continue;
-                    const int t = i / n4, c = (i % n4) * 4;
-                    uint16_t h[4], m[4], lo[4];
-                    split_bf16x3(v[j].x, h[0], m[0], lo[0]);
-                    split_bf16x3(v[j].y, h[1], m[1], lo[1]);
-                    split_bf16x3(v[j].z, h[2], m[2], lo[2]);
-                    split_bf16x3(v[j].w, h[3], m[3], lo[3]);
-                    uint8_t* base = xt + (size_t)(8 * NT * (t >> 3) + (t & 7)) * stride + c * 2;
-                    *reinterpret_cast<uint2*>(base) =
-                        make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
-                    *reinterpret_cast<uint2*>(base + 8 * stride) =
-                        make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
-                    *reinterpret_cast<uint2*>(base + 16 * stride) =
-                        make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
-                }
-            }
+        // the pass's rows of x as they are (rows >= nt keep stale data: their output
+        // columns are not stored); already in flight when issued with the weights
+        const int n16 = ncols / 8;   // 16-byte pieces per row
+        for (int i = x_pre ? nt * n16 : threadIdx.x; i < nt * n16; i += blockDim.x) {
+            const int t = i / n16, c = (i % n16) * 8;
+            cp_async_16(xs_a + (uint32_t)t * stride + (uint32_t)c * 2, p.x + (size_t)(t0 + t) * H + c0 + c);
         }
         cp_async_wait_all();   // this thread's weight and input copies have landed
         __syncthreads();
@@ -418,10 +350,6 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
                 ldmatrix_x4(ws_a + (uint32_t)(mt * 16 + (lane & 15)) * stride + (uint32_t)(k0 + (lane >> 4) * 8) * 2,
                             af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
             uint32_t b[NT][2];
-            if constexpr (NT == 3)   // terms hi and mid (rows 0..15), then lo below
-                ldmatrix_x4(xg + (uint32_t)((lane >> 4) * 8 + (lane & 7)) * stride +
-                                (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2,
-                            b[0][0], b[0][1], b[1][0], b[1][1]);
             ldmatrix_x2(xg + (uint32_t)(8 * (NT - 1) + (lane & 7)) * stride + (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2,
                         b[NT - 1][0], b[NT - 1][1]);
 #pragma unroll
@@ -445,16 +373,9 @@ __device__ __noinline__ void router_unit(const PersistParams& p, const PersistLa
         __syncthreads();
         for (int i = threadIdx.x; i < kPRouteExperts * TP; i += blockDim.x) {   // (expert, token): K parts in order, then the terms
             const int e = i / TP, t = i % TP, g = t >> 3, t8 = t & 7;
-            float sh = 0.0f, sm_ = 0.0f, slo = 0.0f;
-            for (int w = 0; w < wpg; ++w) {
-                const float* r = red + (g * wpg + w) * 768 + e * 24;
-                sh += r[t8];
-                if (NT == 3) {
-                    sm_ += r[8 + t8];
-                    slo += r[16 + t8];
-                }
-            }
-            if (t < nt && e < ne) p.rpart[((size_t)sl * T + t0 + t) * E + eg * kPRouteExperts + e] = sh + (sm_ + slo);
+            float sh = 0.0f;
+            for (int w = 0; w < wpg; ++w) sh += red[(g * wpg + w) * 768 + e * 24 + t8];
+            if (t < nt && e < ne) p.rpart[((size_t)sl * T + t0 + t) * E + eg * kPRouteExperts + e] = sh;
         }
         if (t0 == tbeg) rs(3);
     }
@@ -521,6 +442,8 @@ __device__ __noinline__ void router_full_unit(const PersistParams& p, const Pers
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = u * p.rfull, ne = min(p.rfull, p.E - e0);
     const uint32_t stride = router_full_stride(p), xs = smem_u32(sm.slots), wsb = xs + router_full_wbase(p);
+    const bool writer = threadIdx.x < ne * p.T;   // thread (e, t) writes logit[t][e0 + e]
+    const float bias = writer && ly.router_b ? __ldg(ly.router_b + e0 + threadIdx.x / p.T) : 0.0f;   // loaded early
     cp_async_wait_all();
     __syncthreads();
     const int kw = p.H / 16;                                   // columns per warp (multiple of 16)
@@ -543,19 +466,29 @@ __device__ __noinline__ void router_full_unit(const PersistParams& p, const Pers
         red[(warp * 16 + e + 8) * 8 + t + 1] = d[3];
     }
     __syncthreads();
-    if (threadIdx.x < ne * p.T) {
+    if (writer) {
         const int e = threadIdx.x / p.T, t = threadIdx.x % p.T;
         float z = 0.0f;
         for (int w = 0; w < 16; ++w) z += red[(w * 16 + e) * 8 + t];
-        p.rb.logits[(size_t)t * p.E + e0 + e] = z + (ly.router_b ? __ldg(ly.router_b + e0 + e) : 0.0f);
+        p.rb.logits[(size_t)t * p.E + e0 + e] = z + bias;
     }
 }
 
 // Logits of a larger block from the router slice partials (slices in order) + bias,
-// over every thread of the grid.
+// over every thread of the grid.  Residual stack: the partials are the router products
+// of r * w_norm per 256-column block (prep_unit), times 1 / rms(r_t), which is also
+// written to tscale[t] for the gate/up epilogue.
 __device__ __noinline__ void logits_reduce(const PersistParams& p, const PersistLayer& ly) {
-    const int TE = p.T * p.E, n_sl = p.H / p.rslice;
+    const int TE = p.T * p.E, n_sl = p.norm ? p.H / kCombineChunk : p.H / p.rslice;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < TE; i += gridDim.x * blockDim.x) {
+        float iv = 1.0f;
+        if (p.norm) {   // the sum of the token's block sums of squares in block order, as inv_rms
+            const int t = i / p.E, nc = p.H / kCombineChunk;
+            float tot = 0.0f;
+            for (int c = 0; c < nc; ++c) tot += __ldcg(p.ss + (size_t)t * nc + c);
+            iv = 1.0f / sqrtf(tot / (float)p.H + p.eps);
+            if (i % p.E == 0) p.tscale[t] = iv;
+        }
         const float* src = p.rpart + i;
         float z = 0.0f;
         for (int s0 = 0; s0 < n_sl; s0 += 8) {   // 8 loads in flight, summed in slice order
@@ -566,12 +499,13 @@ __device__ __noinline__ void logits_reduce(const PersistParams& p, const Persist
             for (int q = 0; q < 8; ++q)
                 if (s0 + q < n_sl) z += a[q];
         }
-        p.rb.logits[i] = z + (ly.router_b ? __ldg(ly.router_b + i % p.E) : 0.0f);
+        p.rb.logits[i] = (p.norm ? z * iv : z) + (ly.router_b ? __ldg(ly.router_b + i % p.E) : 0.0f);
     }
 }
 
-// The expert operand of the layer input: task i = (token t, MX block kb) splits the
-// block's 32 values (x, or RMSNorm of the residual) into 8 E2M1 terms.  Whole warps;
+// The expert operand of the layer input x (a residual stack forms its operand in
+// prep_unit): task i = (token t, MX block kb) splits the block's 32 values into 8 E2M1
+// terms.  Whole warps;
 // the tasks are spread over every warp of the grid, starting from the last CTA
 // (the first CTAs run the router units).
 __device__ __noinline__ void operand_tasks(const PersistParams& p, const PersistLayer& ly) {
@@ -583,8 +517,7 @@ __device__ __noinline__ void operand_tasks(const PersistParams& p, const Persist
         if (gw < n) {
             const int t = gw / nb, kb = gw % nb;
             const size_t o = (size_t)t * H + kb * 32 + lane;
-            const float v = p.norm ? __ldcg(p.resid + o) * inv_rms(p, t) * __bfloat162float(ly.norm_w[kb * 32 + lane])
-                                   : __bfloat162float(p.x[o]);
+            const float v = __bfloat162float(p.x[o]);
             uint32_t sb0, sb1;
             const uint32_t codes = split_e2m1_terms(v, sb0, sb1);
             store_act_terms(p.xb4, p.xsf, H, t, kb, lane, codes, sb0, sb1);
@@ -601,12 +534,7 @@ __device__ __noinline__ void operand_tasks(const PersistParams& p, const Persist
             v[j] = 0.0f;
             if (i >= n) continue;
             const size_t o = (size_t)t * H + kb * 32 + lane;
-            if (p.norm) {
-                const float iv = inv_rms(p, t);
-                v[j] = __ldcg(p.resid + o) * iv * __bfloat162float(ly.norm_w[kb * 32 + lane]);
-            } else {
-                v[j] = __bfloat162float(p.x[o]);
-            }
+            v[j] = __bfloat162float(p.x[o]);
         }
         uint32_t codes[kB], sb0[kB], sb1[kB];
 #pragma unroll
@@ -728,17 +656,42 @@ __device__ __noinline__ void route_small(const PersistParams& p, int l, int* scr
     int* off = cnt + E;                              // [E]
     int* wsum = off + E;                             // [32 + 4]
     const int n = T * E;
-    for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {   // 8 loads in flight per thread
-        float v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = i0 + q * blockDim.x;
-            v[q] = i < n ? __ldcg(p.rb.logits + i) : 0.0f;
+    if (p.norm) {
+        // residual stack: logit[t][e] = (1 / rms(r_t)) * sum over column blocks of the
+        // router products of r * w_norm (prep_unit), in block order, + bias
+        for (int t = warp; t < T; t += nw) {
+            const float iv = inv_rms(p, t);
+            if (lane == 0) rt->tscale[t] = iv;
         }
+        __syncthreads();
+        const PersistLayer& ly = p.layer[l];
+        const int nc = p.H / kCombineChunk;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const float* src = p.rpart + i;
+            float z = 0.0f;
+            for (int c0 = 0; c0 < nc; c0 += 8) {   // 8 loads in flight, summed in block order
+                float a[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = i0 + q * blockDim.x;
-            if (i < n) lg[i] = v[q];
+                for (int q = 0; q < 8; ++q) a[q] = c0 + q < nc ? __ldcg(src + (size_t)(c0 + q) * n) : 0.0f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (c0 + q < nc) z += a[q];
+            }
+            lg[i] = z * rt->tscale[i / E] + (ly.router_b ? __ldg(ly.router_b + i % E) : 0.0f);
+        }
+    } else {
+        for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {   // 8 loads in flight per thread
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int i = i0 + q * blockDim.x;
+                v[q] = i < n ? __ldcg(p.rb.logits + i) : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int i = i0 + q * blockDim.x;
+                if (i < n) lg[i] = v[q];
+            }
         }
     }
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
@@ -875,13 +828,58 @@ __device__ __noinline__ void publish_small(const PersistParams& p, int l, const 
     if (threadIdx.x == 0) rb.active[0] = na;
 }
 
+// The next layer's inputs from 256 columns of a token's residual (residual stack).
+// RMSNorm(r) = (r * w_norm) / rms(r), and 1 / rms(r) is one factor per token: it is
+// applied to the router's logits (route_small / logits_reduce) and to the gate/up
+// outputs (tc_epilogue), so what is formed here, column block by column block, is
+// y = r * w_norm: its E2M1 terms (the experts' input operand, as operand_tasks stores
+// them) and its router products P[cb][t][e] = sum over the block's columns of
+// y[h] * W_router[e][h] (fp32, in a fixed order), kept in rpart.  Thread i < 64 holds
+// r[4i .. 4i + 3] of block cb in v (have); ys: 256 floats of shared memory.
+__device__ __noinline__ void prep_unit(const PersistParams& p, const PersistLayer& lyn, int t, int cb, float4 v,
+                                       bool have, float* ys) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = cb * kCombineChunk;
+    __syncthreads();   // an earlier unit's reads of ys are done
+    if (have) {
+        const int h = threadIdx.x * 4;
+        const uint2 wv = __ldg(reinterpret_cast<const uint2*>(lyn.norm_w + c0 + h));
+        *reinterpret_cast<float4*>(ys + h) =
+            make_float4(v.x * bf16_lo(wv.x), v.y * bf16_hi(wv.x), v.z * bf16_lo(wv.y), v.w * bf16_hi(wv.y));
+    }
+    __syncthreads();
+    if (warp < kCombineChunk / 32) {   // the expert operand: MX block c0 / 32 + warp (lane = element)
+        uint32_t sb0, sb1;
+        const uint32_t codes = split_e2m1_terms(ys[warp * 32 + lane], sb0, sb1);
+        store_act_terms(p.xb4, p.xsf, p.H, t, c0 / 32 + warp, lane, codes, sb0, sb1);
+    }
+    // router products: warp w takes experts w, w + 16, ...; lane l the columns 8l .. 8l + 7
+    const float4 y0 = *reinterpret_cast<const float4*>(ys + lane * 8);
+    const float4 y1 = *reinterpret_cast<const float4*>(ys + lane * 8 + 4);
+    for (int e = warp; e < p.E; e += blockDim.x >> 5) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(lyn.router_w + (size_t)e * p.H + c0 + lane * 8));
+        float z = y0.x * bf16_lo(w.x);
+        z = fmaf(y0.y, bf16_hi(w.x), z);
+        z = fmaf(y0.z, bf16_lo(w.y), z);
+        z = fmaf(y0.w, bf16_hi(w.y), z);
+        z = fmaf(y1.x, bf16_lo(w.z), z);
+        z = fmaf(y1.y, bf16_hi(w.z), z);
+        z = fmaf(y1.z, bf16_lo(w.w), z);
+        z = fmaf(y1.w, bf16_hi(w.w), z);
+        z = warp_sum(z);
+        if (lane == 0) p.rpart[((size_t)cb * p.T + t) * p.E + e] = z;
+    }
+    fence_proxy_async_global();   // the operand is read next by bulk copies
+}
+
 // Combine unit (token t, 256-column block c): out = sum_j gate[t, j] * partial[t*k + j]
 // (slots in order, pairs outside the expert shard skipped); with a residual stack
-// r += out and the block's sum of squares of r is kept for the next RMSNorm.  The last
-// layer writes y.
+// r += out and the block's sum of squares of r is kept for the next RMSNorm, and when
+// the next layer runs in this launch its inputs are prepared from r (prep_unit).  The
+// last layer writes y.
 // dry: read everything but store nothing (runs the code once to bring it into the caches).
 __device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, float* red, const RouteTable* rt,
-                                          bool dry = false) {
+                                          float* ys, bool dry = false) {
     const int H = p.H, k = p.k;
     const int nc = H / kCombineChunk;
     const int t = u / nc, c = u % nc;
@@ -901,8 +899,8 @@ __device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, 
     }
     float ssl = 0.0f;
     const int h = threadIdx.x * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (h < ncols) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j0 = 0; j0 < kMaxTopK; j0 += 8) {   // 8 slots' loads in flight, summed in slot order
             if (j0 >= k) break;
@@ -946,26 +944,34 @@ __device__ __noinline__ void combine_unit(const PersistParams& p, int u, int l, 
     if (p.norm) {
         const float tot = block_sum(ssl, red);
         if (threadIdx.x == 0 && !dry) p.ss[(size_t)t * nc + c] = tot;
+        if (!dry && l + 1 < p.L) prep_unit(p, p.layer[l + 1], t, c, acc, h < ncols, ys);
     }
 }
 
-// Residual start of a stack, unit (token t, chunk c): r = fp32(x) and the chunk's sum of squares.
-__device__ __noinline__ void stack_init_unit(const PersistParams& p, int u, float* red) {
+// Start of a launch of a residual stack, unit (token t, 256-column block c): the residual
+// (r = fp32(x) on the first launch of the stack, stored; else the residual left by the
+// previous launch), its block sum of squares, and the first layer's inputs (prep_unit).
+__device__ __noinline__ void stack_prep_unit(const PersistParams& p, int u, float* red, float* ys) {
     const int H = p.H;
-    const int nc = (H + kCombineChunk - 1) / kCombineChunk;
+    const int nc = H / kCombineChunk;
     const int t = u / nc, c = u % nc;
-    const int c0 = c * kCombineChunk, ncols = min(kCombineChunk, H - c0);
-    const size_t o = (size_t)t * H + c0;
+    const size_t o = (size_t)t * H + (size_t)c * kCombineChunk;
     float ssl = 0.0f;
     const int h = threadIdx.x * 4;
-    if (h < ncols) {
-        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(p.x + o + h));
-        const float4 v = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
-        *reinterpret_cast<float4*>(p.resid + o + h) = v;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (h < kCombineChunk) {
+        if (p.init_from_x) {
+            const uint2 xv = __ldg(reinterpret_cast<const uint2*>(p.x + o + h));
+            v = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
+            *reinterpret_cast<float4*>(p.resid + o + h) = v;
+        } else {
+            v = __ldcg(reinterpret_cast<const float4*>(p.resid + o + h));
+        }
         ssl = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     }
     const float tot = block_sum(ssl, red);
     if (threadIdx.x == 0) p.ss[(size_t)t * nc + c] = tot;
+    prep_unit(p, p.layer[0], t, c, v, h < kCombineChunk, ys);
 }
 
 
@@ -1264,7 +1270,7 @@ __device__ __noinline__ void combine_elems(const PersistParams& p, int l, const 
 
 // The expert phase of one layer, compiled as its own function (its register
 // allocation does not carry the rest of the persistent kernel's live state).
-template <bool kGathered>
+template <bool kGathered, bool kNorm>
 __device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMaps* maps, uint8_t* smem_raw,
                                                   uint32_t tmem, TcRoleState* rs, unsigned long long deadline) {
     const TcSmem s = tc_smem(smem_raw);
@@ -1278,7 +1284,7 @@ __device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMap
         prefetch_tensormap(&maps->down_s);
     }
     TcRoleState r = *rs;
-    tc_phase<kGathered>(*maps, args, s, tmem, r, deadline);
+    tc_phase<kGathered, kNorm>(*maps, args, s, tmem, r, deadline);
     *rs = r;
 }
 
@@ -1286,6 +1292,7 @@ __device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMap
 // its input rows) into shared memory, issued before anything else of the launch.
 template <bool kLarge>
 __device__ __forceinline__ void router_first_copies(const PersistParams& p, const TcSmem& sm, int* rstate) {
+    if (p.norm) return;   // a residual stack has no router units (prep_unit forms the router products)
     if (p.rfull) {   // whole-row units: unit b on CTA b
         if ((int)blockIdx.x < router_full_units(p)) router_full_fetch(p, p.layer[0], blockIdx.x, sm);
         return;
@@ -1323,8 +1330,9 @@ __device__ __forceinline__ void router_first_copies(const PersistParams& p, cons
 
 // All layers of one launch; returns early (in every thread of the block) on a timeout / abort.
 // kLarge: the block is routed through the workspace (route_is_small(p) is false), with
-// the input operand gathered per chunk; the host launches the matching instantiation.
-template <bool kLarge>
+// the input operand gathered per chunk; kNorm: a residual stack (p.norm).  The host
+// launches the matching instantiation.
+template <bool kLarge, bool kNorm>
 __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* smem_raw, uint32_t tmem,
                                             unsigned long long deadline) {
     const TcSmem sm = tc_smem(smem_raw);
@@ -1341,37 +1349,47 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
     auto stamp = [&](int i) {
         if (blockIdx.x == 0 && threadIdx.x == 0 && p.tstamp) p.tstamp[i] = globaltimer_ns();
     };
+    float* ys = reinterpret_cast<float*>(sm.slots);        // prep_unit scratch (256 floats)
     stamp(0);   // (the first router unit's copies were issued before the setup)
-    if (p.norm && p.init_from_x) {
-        for (int u = blockIdx.x; u < cunits; u += gridDim.x) stack_init_unit(p, u, red);
-        if (!grid_sync(p.bar, btok, deadline, abort, status)) return;
+    if constexpr (kNorm) {
+        // residual stack: the first layer's inputs (its router products and operand); later
+        // layers' inputs are prepared by the combine of the layer before
+        for (int u = blockIdx.x; u < cunits; u += gridDim.x) stack_prep_unit(p, u, red, ys);
+        grid_arrive(p.bar, btok, p.ta.debug_stall && blockIdx.x == gridDim.x - 1);
+        // a CTA without a unit runs the routing code meanwhile (results discarded), so
+        // that its code is in the caches when the grid needs it
+        if (small && (int)blockIdx.x >= cunits) route_small(p, 0, reinterpret_cast<int*>(xs), sm.rt);
+        if (!grid_wait(p.bar, btok, deadline, abort, status)) return;
     }
     stamp(1);
 
     for (int l = 0; l < p.L; ++l) {
         const PersistLayer& ly = p.layer[l];
-        if (p.rfull) {
+        if constexpr (kNorm) {
+            // (the inputs of this layer were prepared before the last grid barrier)
+        } else if (p.rfull) {
             if ((int)blockIdx.x < units) router_full_unit(p, ly, blockIdx.x, sm);
         } else {
             for (int u = router_first<kLarge>(units); u < router_end<kLarge>(units); u += router_step<kLarge>())
-                p.norm ? router_unit<3>(p, ly, l, u, sm, rstate) : router_unit<1>(p, ly, l, u, sm, rstate);
+                router_unit(p, ly, l, u, sm, rstate);
         }
-        if (threadIdx.x == 0) rstate[5] = -1;   // the slot area is reused from here on
-        if (l == 0) stamp(53);
-        operand_tasks(p, ly);
-        if (l == 0) stamp(54);
-        const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
-        grid_arrive(p.bar, btok, withhold);
-        if (small && blockIdx.x >= units) {
-            // a CTA without a router unit would only wait at the barrier: after arriving it
-            // runs the routing code (results discarded; shared memory only) or, on every other
-            // such CTA, the combine code (nothing stored), so that code is in L2 when the whole
-            // grid needs it
-            if (((blockIdx.x - units) & 1) == 0 || l + 1 < p.L) route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
-            else if (p.norm) combine_unit(p, blockIdx.x % cunits, l, red, nullptr, true);
-            else combine_elems(p, l, nullptr, sm.slots, true);
+        if constexpr (!kNorm) {
+            if (threadIdx.x == 0) rstate[5] = -1;   // the slot area is reused from here on
+            if (l == 0) stamp(53);
+            operand_tasks(p, ly);
+            if (l == 0) stamp(54);
+            const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
+            grid_arrive(p.bar, btok, withhold);
+            if (small && blockIdx.x >= units) {
+                // a CTA without a router unit would only wait at the barrier: after arriving it
+                // runs the routing code (results discarded; shared memory only) or, on every other
+                // such CTA, the combine code (nothing stored), so that code is in L2 when the whole
+                // grid needs it
+                if (((blockIdx.x - units) & 1) == 0) route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
+                else combine_elems(p, l, nullptr, sm.slots, true);
+            }
+            if (!grid_wait(p.bar, btok, deadline, abort, status)) return;
         }
-        if (!grid_wait(p.bar, btok, deadline, abort, status)) return;
         stamp(2 + 4 * l);
         if (small) {
             route_small(p, l, reinterpret_cast<int*>(xs), sm.rt);
@@ -1418,6 +1436,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
             if (!grid_sync(p.bar, btok, deadline, abort, status)) return;
             stamp(3 + 4 * l);
         }
+        if (kNorm && !small && threadIdx.x == 0) sm.rt->tscale_g = p.tscale;   // for the gate/up epilogue
         // the slots were written through the generic proxy; TMA writes them next
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
@@ -1427,22 +1446,12 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         ta.done = p.dones + (size_t)l * p.chunk_stride;
         ta.rt = small ? sm.rt : nullptr;
         if (l != 0 || p.layer_base != 0) ta.trace = nullptr;
-        persist_expert_phase<kLarge>(ta, &ly.maps, smem_raw, tmem, &rs, deadline);
+        persist_expert_phase<kLarge, kNorm>(ta, &ly.maps, smem_raw, tmem, &rs, deadline);
         // the loader warps are done with the phase before the other roles (once the producer
         // has no more items): they run the combine code once without storing, so this SM's
         // instruction cache holds it when the combine starts after the barrier
-        if (!p.norm && tc_loader_index((int)(threadIdx.x >> 5)) >= 0)
+        if (!kNorm && tc_loader_index((int)(threadIdx.x >> 5)) >= 0)
             combine_elems(p, l, small ? sm.rt : nullptr, sm.slots, true);
-        // the next layer's first router unit, ahead of time
-        if (l + 1 < p.L && router_first<kLarge>(units) < router_end<kLarge>(units)) {
-            fence_proxy_async_shared();
-            __syncthreads();
-            router_fetch(p, p.layer[l + 1], router_first<kLarge>(units), sm);
-            if (threadIdx.x == 0) {
-                rstate[2] = router_first<kLarge>(units);
-                rstate[3] = l + 1;
-            }
-        }
         if (small && blockIdx.x == 0) publish_small(p, l, sm.rt);
         if (!grid_sync(p.bar, btok, deadline, abort, status)) return;
         stamp(4 + 4 * l);
@@ -1453,12 +1462,20 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
             else p.dones[(size_t)l * p.chunk_stride + i - 1] = 0;
         }
         if (!small && blockIdx.x == 0 && threadIdx.x == 0) *p.route_flag = 0;
-        if (p.norm)
-            for (int u = blockIdx.x; u < cunits; u += gridDim.x) combine_unit(p, u, l, red, small ? sm.rt : nullptr);
-        else
+        if constexpr (kNorm) {
+            for (int u = blockIdx.x; u < cunits; u += gridDim.x)
+                combine_unit(p, u, l, red, small ? sm.rt : nullptr, ys);
+        } else {
             combine_elems(p, l, small ? sm.rt : nullptr, sm.slots);
+        }
         stamp(5 + 4 * l);
-        if (l + 1 < p.L && !grid_sync(p.bar, btok, deadline, abort, status)) return;
+        if (l + 1 < p.L) {
+            grid_arrive(p.bar, btok);
+            // a CTA without a combine unit runs the next layer's routing code meanwhile
+            // (results discarded), so that its code is in the caches when the grid needs it
+            if (small && (int)blockIdx.x >= cunits) route_small(p, l + 1, reinterpret_cast<int*>(xs), sm.rt);
+            if (!grid_wait(p.bar, btok, deadline, abort, status)) return;
+        }
     }
 }
 
@@ -1470,7 +1487,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
 // the abort flag of an earlier failed launch (its counters may not be at rest) does
 // nothing either: the error stays in the status words until the host reads it and
 // re-zeroes the state.
-template <bool kLarge>
+template <bool kLarge, bool kNorm>
 __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_constant__ PersistParams p) {
     extern __shared__ uint8_t smem_raw[];
     const TcSmem sm = tc_smem(smem_raw);
@@ -1488,7 +1505,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_con
             *p.wl.abort = 1;
         }
     } else if (aborted_before == 0) {
-        persist_layers<kLarge>(p, smem_raw, tmem, deadline);
+        persist_layers<kLarge, kNorm>(p, smem_raw, tmem, deadline);
     }
     __syncthreads();
     if (threadIdx.x == 0 && p.tstamp && blockIdx.x < 256)   // when each CTA finished (profiling)

@@ -51,6 +51,8 @@ struct RouteTable {
     int pair[kRtMaxPairs];     // per perm position: pair id t*k + j
     int idx[kRtMaxPairs];      // per pair t*k + j: routed expert
     float gate[kRtMaxPairs];   // per pair t*k + j: gate
+    float tscale[kRtMaxPairs]; // per token (residual stack): 1 / rms of its residual
+    const float* tscale_g;     // the same factors in global memory [T] (blocks routed through the workspace)
 };
 
 // Per-forward work list (workspace).
