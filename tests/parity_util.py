@@ -42,7 +42,9 @@ def assert_rows_close(got: np.ndarray, ref: np.ndarray, rows=None, what=""):
     log = os.environ.get("MOE_PARITY_LOG")
     if log:
         with open(log, "a") as f:
-            f.write(json.dumps({"what": what, "worst_rel_l2": worst[0], "worst_maxabs_over_rms": worst[1]}) + "\n")
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], "what": what,
+                                "rows": len(rows), "worst_rel_l2": worst[0],
+                                "worst_maxabs_over_rms": worst[1]}) + "\n")
     return worst
 
 
