@@ -655,6 +655,7 @@ __device__ __noinline__ void route_small(const PersistParams& p, int l, int* scr
     int* cnt = scratch + T * E;                      // [E]
     int* off = cnt + E;                              // [E]
     int* wsum = off + E;                             // [32 + 4]
+    int* cnt0 = wsum + 36;                           // [E] pairs among the first 32 per expert
     const int n = T * E;
     if (p.norm) {
         // residual stack: logit[t][e] = (1 / rms(r_t)) * sum over column blocks of the
@@ -694,7 +695,10 @@ __device__ __noinline__ void route_small(const PersistParams& p, int l, int* scr
             }
         }
     }
-    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        cnt[e] = 0;
+        cnt0[e] = 0;
+    }
     __syncthreads();
     sub(1);
     for (int t = warp; t < T; t += nw) {
@@ -711,7 +715,10 @@ __device__ __noinline__ void route_small(const PersistParams& p, int l, int* scr
     const int npairs = T * k;
     for (int s = threadIdx.x; s < npairs; s += blockDim.x) {
         const int e = rt->idx[s];
-        if (e >= p.e_begin && e < p.e_end) atomicAdd(&cnt[e], 1);
+        if (e >= p.e_begin && e < p.e_end) {
+            atomicAdd(&cnt[e], 1);
+            if (s < 32) atomicAdd(&cnt0[e], 1);
+        }
     }
     __syncthreads();
     // exclusive scans over the experts of (pairs, routed flag), packed in 16-bit
@@ -779,14 +786,18 @@ __device__ __noinline__ void route_small(const PersistParams& p, int l, int* scr
             rt->pad0 = n_in;   // pairs routed into the shard
         }
     }
-    // perm position of pair s: its expert's offset + the same-expert pairs before it
-    for (int s = threadIdx.x; s < npairs; s += blockDim.x) {
-        const int e = rt->idx[s];
-        if (e < p.e_begin || e >= p.e_end) continue;
-        int r = 0;
-        for (int q = 0; q < s; ++q) r += rt->idx[q] == e ? 1 : 0;
-        rt->tok[off[e] + r] = s / k;
-        rt->pair[off[e] + r] = s;
+    // perm position of pair s (< 64: warps 0 and 1): its expert's offset + the same-expert
+    // pairs before it, i.e. the lower lanes of its warp with the same expert (match) and,
+    // in warp 1, the first 32 pairs' count of that expert
+    if (threadIdx.x < 64) {
+        const int s = threadIdx.x;
+        const int e = s < npairs ? rt->idx[s] : -1 - s;   // (absent pairs match nothing)
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+        if (s < npairs && e >= p.e_begin && e < p.e_end) {
+            const int r = __popc(same & ((1u << lane) - 1u)) + (s >= 32 ? cnt0[e] : 0);
+            rt->tok[off[e] + r] = s / k;
+            rt->pair[off[e] + r] = s;
+        }
     }
     __syncthreads();
     sub(4);
