@@ -456,8 +456,9 @@ __device__ __noinline__ void router_full_unit(const PersistParams& p, const Pers
         ldmatrix_x2(xs + (uint32_t)brow * stride + (uint32_t)(k0 + ((lane >> 3) & 1) * 8) * 2, b0, b1);
         mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
     }
-    __syncthreads();   // every warp's reads of the staged rows are done: the sums reuse the area
-    float* red = reinterpret_cast<float*>(sm.slots);           // [16 warps][16 experts][8 tokens]
+    // the warps' sums go to the scale ring (unused until the expert phase), so that x stays
+    // in the slot area for operand_tasks
+    float* red = reinterpret_cast<float*>(sm.scales);          // [16 warps][16 experts][8 tokens]
     {
         const int e = lane >> 2, t = 2 * (lane & 3);
         red[(warp * 16 + e) * 8 + t] = d[0];
@@ -508,7 +509,9 @@ __device__ __noinline__ void logits_reduce(const PersistParams& p, const Persist
 // terms.  Whole warps;
 // the tasks are spread over every warp of the grid, starting from the last CTA
 // (the first CTAs run the router units).
-__device__ __noinline__ void operand_tasks(const PersistParams& p, const PersistLayer& ly) {
+// xsm: this CTA's shared-memory copy of x (rows of router_full_stride bytes; a whole-row
+// router unit's input), or NULL.
+__device__ __noinline__ void operand_tasks(const PersistParams& p, const PersistLayer& ly, const uint8_t* xsm) {
     const int H = p.H, nb = H / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const int gw = (gridDim.x - 1 - blockIdx.x) * nw + warp;
@@ -517,7 +520,9 @@ __device__ __noinline__ void operand_tasks(const PersistParams& p, const Persist
         if (gw < n) {
             const int t = gw / nb, kb = gw % nb;
             const size_t o = (size_t)t * H + kb * 32 + lane;
-            const float v = __bfloat162float(p.x[o]);
+            const float v = xsm ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(
+                                      xsm + (size_t)t * router_full_stride(p))[kb * 32 + lane])
+                                : __bfloat162float(p.x[o]);
             uint32_t sb0, sb1;
             const uint32_t codes = split_e2m1_terms(v, sb0, sb1);
             store_act_terms(p.xb4, p.xsf, H, t, kb, lane, codes, sb0, sb1);
@@ -1387,7 +1392,8 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         if constexpr (!kNorm) {
             if (threadIdx.x == 0) rstate[5] = -1;   // the slot area is reused from here on
             if (l == 0) stamp(53);
-            operand_tasks(p, ly);
+            // a CTA that ran a whole-row router unit holds x in shared memory
+            operand_tasks(p, ly, p.rfull && (int)blockIdx.x < units ? sm.slots : nullptr);
             if (l == 0) stamp(54);
             const bool withhold = p.ta.debug_stall && l == 0 && blockIdx.x == gridDim.x - 1;
             grid_arrive(p.bar, btok, withhold);
