@@ -16,14 +16,15 @@
 //                         through their own ring;
 //   activation loaders    (3 warps) the per-token activation rows and scales of gate/up
 //                         stages, by cp.async (see tc_load);
-//   MMA issuer (one lane) per stage 6 tcgen05.cp of the stage's scale rows and 4
-//                         block-scaled MMAs (kind::mxf4, K = 64 each): A = the
-//                         activation terms (M = 128 rows, rows 8p + j of pair slot p,
-//                         term j; rows 64.. unused), B = the weights (N = 256 rows),
-//                         one E8M0 scale per row and 32-element block, fp32
-//                         accumulator [128 x 256] in tensor memory;
+//   MMA issuer (one lane) per stage 4 block-scaled MMAs (kind::mxf4, K = 64 each):
+//                         A = the activation terms (M = 128 rows, rows 8p + j of pair
+//                         slot p, term j; the dense operand: rows 4p + j, 16 pairs x 4
+//                         terms; rows 64.. unused), B = the weights (N = 256 rows), one
+//                         E8M0 scale per row and 32-element block, fp32 accumulator
+//                         [128 x 256] in tensor memory;
 //   scale-factor warps    rearrange the stage's scales in shared memory into the
-//                         16-byte rows that tcgen05.cp puts into tensor memory;
+//                         16-byte rows that tcgen05.cp puts into tensor memory, and
+//                         issue those copies (3 warps);
 //   epilogue warps (8)    lanes 0..63 of the accumulator (two lane quarters x four
 //                         column chunks): sum each pair's 8 term rows (shuffle
 //                         reduce-scatter over groups of 8 lanes), then gate/up items
@@ -34,9 +35,10 @@
 // weights take the wide operand: 8 KB of weights per MMA.  Every TMA request moves
 // whole 128-byte rows (narrower rows cost as much per request).
 // The weights are exact (E2M1 x E8M0 is what the format defines); each activation x
-// is replaced by the sum of 8 E2M1 terms with per-32 E8M0 scales, term j encoding
-// the residual of terms 0..j-1 (about 3.3 bits per term: the sum is within ~1e-7 of
-// max|x| of its block), and the tensor cores add exact products in fp32.
+// is replaced by the sum of t E2M1 terms with per-32 E8M0 scales, term j encoding
+// the residual of terms 0..j-1; each term at least quarters the block's largest
+// residual, so the sum is within 4^-t of max|x| of its block (t = 8: N(0,1) blocks reach
+// ~1e-7; the dense operand t = 4), and the tensor cores add exact products in fp32.
 #pragma once
 
 #include "common.cuh"

@@ -3,12 +3,13 @@
 // pipeline stays resident instead of one launch per operator; implementation
 // guide "关键实现细节" item 3: per-launch gaps of 5-10 us and 10-30% operator-boundary
 // overhead at high token rates).  One CTA per SM, the expert kernel's block
-// shape (16 warps) and tensor-memory allocation.  Per layer:
-//   [router]           all CTAs, units of (32 experts x 256..1024 columns x a token
-//                      block): partial logits, completed per expert group by the
-//                      group's last unit (small blocks) or by the whole grid (larger
-//                      blocks); every warp of the grid: the layer input as the
-//                      experts' operand (8 E2M1 terms per MX block)
+// shape (16 warps) and tensor-memory allocation.  Per layer of a plain input x:
+//   [router]           one block of <= 8 tokens: CTA b computes whole logit rows of a
+//                      few experts from x and their weight rows in shared memory;
+//                      larger blocks: units of (32 experts x 256..1024 columns x a token
+//                      block), partial logits summed by the whole grid after the
+//                      barrier; every warp of the grid: x as the experts' operand (8
+//                      E2M1 terms per MX block)
 //   -- grid barrier --
 //   [route]            small blocks (T*k <= 64): every CTA takes the top-k and groups
 //                      the pairs in its own shared memory (identical results
@@ -19,12 +20,15 @@
 //   [experts]          the work-queue expert phase of expert_tc.cuh
 //   -- grid barrier --
 //   [combine]          all CTAs: gate-weighted sum of the pair outputs (grid-stride
-//                      over (token, 4 columns)); with a stack, (token, 256 columns)
-//                      units that also add the residual and keep the sums of squares
-//                      for the next layer's RMSNorm
-//   -- grid barrier --  (before the next layer's router)
-// Every wait is bounded by the forward's deadline; a timeout sets the status
-// word and the abort flag, and every CTA leaves at its next wait.
+//                      over (token, 4 columns))
+// A residual stack has no router phase: its combine units (token, 256 columns) add the
+// residual, keep the block sums of squares and form the next layer's router products and
+// operand from r * w_norm (prep_unit); the routing scales the logits and the gate/up
+// epilogue scales g and u by 1 / rms (one factor per token).  Per layer: [route]
+// [experts] -- barrier -- [combine + next layer's inputs] -- barrier --.
+// The counters and the barrier word in the workspace are at rest between launches (see
+// persist_kernel).  Every wait is bounded by the forward's deadline; a timeout sets the
+// status word and the abort flag, and every CTA leaves at its next wait.
 #pragma once
 
 #include "expert_tc.cuh"
