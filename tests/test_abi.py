@@ -71,3 +71,35 @@ def test_every_entry_point_rejects_a_null_handle_or_bad_sizes_without_a_device(l
     assert pkg.moe_mxfp4_accept(None, None, 1, 8, 1 << 31, None, None, None, None) == pkg.MOE_ERR_INVALID_ARG
     assert pkg.moe_mxfp4_accept(None, None, 0, 8, 100, None, None, None, None) == pkg.MOE_OK
     assert pkg.moe_mxfp4_accept(None, None, 1, 8, 100, None, None, None, None) == pkg.MOE_ERR_INVALID_ARG
+    # the activation split: sizes and pointers are checked before any launch; nothing to do is OK
+    assert pkg.moe_mxfp4_split_terms(None, -1, None, None, None) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_split_terms(None, 4, None, None, None) == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_split_terms(None, 0, None, None, None) == pkg.MOE_OK
+
+
+def _up256(v):
+    return (v + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("H,I,E", [(512, 512, 1), (1024, 512, 16), (4096, 1536, 64), (7168, 2048, 384)])
+def test_packed_layout_size_is_the_sum_of_its_sections(lib_path, H, I, E):
+    """moe_mxfp4_packed_bytes (host arithmetic only) against the layout the header states:
+    the codes of gate, up and down (E * 3 * H * I / 2 bytes), the gate/up scales (E * 2 * H * I
+    / 32) and the down scales (E * H * I / 32), each section starting on a 256-byte
+    boundary, nothing else."""
+    pkg.load_library(lib_path)
+    st, n = pkg.moe_mxfp4_packed_bytes(H, I, E)
+    assert st == pkg.MOE_OK
+    codes = E * 3 * H * I // 2
+    scales_gu = E * 2 * H * I // 32
+    scales_d = E * H * I // 32
+    assert n == _up256(_up256(_up256(codes) + scales_gu) + scales_d)
+    assert n - (codes + scales_gu + scales_d) < 3 * 256
+
+
+def test_packed_layout_refuses_shapes_outside_the_tensor_core_path(lib_path):
+    pkg.load_library(lib_path)
+    assert pkg.moe_mxfp4_packed_bytes(768, 512, 4)[0] == pkg.MOE_ERR_UNSUPPORTED   # H not a multiple of 512
+    assert pkg.moe_mxfp4_packed_bytes(1024, 384, 4)[0] == pkg.MOE_ERR_UNSUPPORTED  # I not a multiple of 512
+    assert pkg.moe_mxfp4_packed_bytes(1024, 512, 0)[0] == pkg.MOE_ERR_INVALID_ARG
+    assert pkg.moe_mxfp4_packed_bytes(-512, 512, 4)[0] == pkg.MOE_ERR_INVALID_ARG
