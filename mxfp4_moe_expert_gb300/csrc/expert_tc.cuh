@@ -49,39 +49,86 @@
 namespace moe {
 
 constexpr int kTcKS = 256;                 // K per stage
-constexpr int kTcStages = 4;               // ring slots
+constexpr int kTcStages = 4;               // ring slots (TcSmall)
 constexpr int kTcTerms = 8;                // E2M1 terms per activation
 constexpr int kTcRowsA = kTmaTok * kTcTerms;   // activation rows used: pair slot p, term j -> row 8p + j
 constexpr int kTcN = kDownRows;            // weight rows per MMA (gate 128 | up 128, or 256 down rows)
 constexpr int kTcThreads = 512;            // 16 warps
-// warp roles: epilogue warps are those of lane quarters 0 and 1 (warp % 4 < 2)
-constexpr int kTcWarpProducer = 2, kTcWarpMma = 3;
-__device__ __forceinline__ bool tc_is_sf_warp(int w) { return w == 6 || w == 7 || w == 10; }
-// activation loaders (warps 11, 14, 15): the gate/up stages' activation rows and scales of
-// blocks whose operand is read per token (not gathered per chunk); loader j serves the
-// ring positions it with it % 3 == j
-__device__ __forceinline__ int tc_loader_index(int w) { return w == 11 ? 0 : w == 14 ? 1 : w == 15 ? 2 : -1; }
-constexpr int kTcLoaders = 3;
-__device__ __forceinline__ bool tc_is_epi_warp(int w) { return (w & 3) < 2; }
 constexpr int kTcEpiWarps = 8;
 constexpr int kTcSfWarps = 3;
-// slot layout (bytes)
-constexpr int kSlotB = 0;                  // weights [256 rows x 128 B] packed E2M1, 128-byte swizzle
-constexpr int kSlotA = 32768;              // activation terms [64 rows x 128 B]; the MMA's rows 64..127 read on (unused)
-constexpr int kSlotAtoms = 40960;          // 6 x [32 rows x 16 B] scale rows for tcgen05.cp: SFA g0, g1, SFB (g, half) x 4
-constexpr int kTcSlotBytes = 45056;
-static_assert(kSlotA % 1024 == 0 && kTcSlotBytes % 1024 == 0, "swizzled operands are 1024-aligned");
+constexpr int kTcLoaders = 3;
+// slot layout (bytes): weights [256 rows x 128 B] packed E2M1 (128-byte swizzle) at 0,
+// activation terms [rows x 128 B] at kSlotA, then the scale rows for tcgen05.cp (6 x [32
+// rows x 16 B]: SFA g0, g1, SFB (g, half) x 4) at the geometry's kAtoms
+constexpr int kSlotB = 0;
+constexpr int kSlotA = 32768;
+constexpr int kSlotAtoms = 40960;          // TcSmall
+constexpr int kTcSlotBytes = 45056;        // TcSmall
 // scale ring entry: a pair of weight-scale boxes [128 rows x up to 64 B] (at +0 and
 // +kScaleBox1), then the activation rows' E8M0 scales of the same stages (at +kScaleSfa):
-//   gate/up items: [pair p][stage in group][8 term rows][8 blocks]; down items: [stage][64 rows][8 blocks]
+//   per-token gate/up items: [pair p][stage in group][8 term rows][8 blocks];
+//   down items and gathered chunks: [stage][activation rows][8 blocks]
 constexpr int kScaleBox1 = 8192;
 constexpr int kScaleSfa = 16384;
-constexpr int kTcScaleEntry = 20480;
+constexpr int kTcScaleEntry = 20480;       // TcSmall
 constexpr int kTcScaleRing = 2;
 constexpr int kTcAuxBytes = 4096;
 constexpr int kTcSmemBytes = 1024 /*align slack*/ + kTcStages * kTcSlotBytes + kTcScaleRing * kTcScaleEntry + kTcAuxBytes;
 static_assert(kTcSmemBytes <= 232448, "shared memory of the expert kernel");
+
+// The two geometries of the expert phase, one per kernel instantiation.  Warp w runs on
+// SM sub-partition w % 4 and reads tensor-memory lanes 32 (w % 4) .. +31 only, so the
+// epilogue warps sit on the lane quarters that hold used accumulator rows.
+//   TcSmall  (blocks routed in shared memory; the one-launch-per-phase kernel): 64
+//            activation rows (8 pairs x 8 terms, rows 8p + j; the MMA's rows 64..127 read
+//            on into the scale rows and are never read back), a ring of 4 stages of 44 KB,
+//            epilogue warps 0, 1, 4, 5, 8, 9, 12, 13 (lane quarters 0 and 1, four 32-column
+//            chunks), producer 2, MMA 3, scale-factor warps 6, 7, 10, loaders 11, 14, 15.
+//   TcWide   (blocks routed through the workspace): all 128 rows of the MMA (32 pairs x 4
+//            terms, rows 4p + j, or 16 pairs x 8 terms), a ring of 3 stages of 52 KB,
+//            epilogue warps 0..7 (two per lane quarter, 32-column chunks c and c + 2),
+//            producer 8, MMA 9, scale-factor warps 10, 11, 12, loaders 13, 14, 15.  Each
+//            chunk's weights pass through the SM once for twice as many pairs.
+struct TcSmall {
+    static constexpr bool kWide = false;
+    static constexpr int kRowsA = kTcRowsA, kStages = kTcStages, kSlotBytes = kTcSlotBytes, kAtoms = kSlotAtoms;
+    static constexpr int kScaleEntry = kTcScaleEntry;
+    static constexpr int kProducer = 2, kMma = 3;
+    static constexpr int kChunksPerEpiWarp = 1;
+    __device__ static __forceinline__ int sf_index(int w) { return w == 6 ? 0 : w == 7 ? 1 : w == 10 ? 2 : -1; }
+    __device__ static __forceinline__ int loader_index(int w) { return w == 11 ? 0 : w == 14 ? 1 : w == 15 ? 2 : -1; }
+    __device__ static __forceinline__ bool epi_warp(int w) { return (w & 3) < 2; }
+};
+struct TcWide {
+    static constexpr bool kWide = true;
+    static constexpr int kRowsA = 128, kStages = 3, kSlotBytes = 53248, kAtoms = 49152;
+    static constexpr int kScaleEntry = 24576;
+    static constexpr int kProducer = 8, kMma = 9;
+    static constexpr int kChunksPerEpiWarp = 2;
+    __device__ static __forceinline__ int sf_index(int w) { return (w >= 10 && w < 13) ? w - 10 : -1; }
+    __device__ static __forceinline__ int loader_index(int w) { return (w >= 13) ? w - 13 : -1; }
+    __device__ static __forceinline__ bool epi_warp(int w) { return w < 8; }
+};
+// the geometry of a kernel instantiation: TcWide for blocks routed through the workspace
+template <bool kWide> struct TcGeom { using type = TcSmall; };
+template <> struct TcGeom<true> { using type = TcWide; };
+// bytes of one stage's activation operand and of its E8M0 scales (gathered / down layout)
+template <class C> constexpr int tc_a_tile() { return C::kRowsA * 128; }
+template <class C> constexpr int tc_sfa_stage() { return C::kRowsA * 8; }
+template <class C> constexpr int tc_smem_need() {
+    return 1024 + C::kStages * C::kSlotBytes + kTcScaleRing * C::kScaleEntry + kTcAuxBytes;
+}
+static_assert(tc_smem_need<TcSmall>() == kTcSmemBytes && tc_smem_need<TcWide>() <= kTcSmemBytes,
+              "both geometries fit the launch's shared memory");
 static_assert(kSlotA + 16384 <= kTcStages * kTcSlotBytes, "the MMA's unused activation rows stay inside shared memory");
+static_assert(kSlotA + tc_a_tile<TcWide>() == TcWide::kAtoms && TcWide::kAtoms + 6 * 512 <= TcWide::kSlotBytes,
+              "wide slot: weights, 128 activation rows, scale rows");
+static_assert(kSlotA + tc_a_tile<TcSmall>() == TcSmall::kAtoms && TcSmall::kAtoms + 6 * 512 <= TcSmall::kSlotBytes,
+              "small slot: weights, 64 activation rows, scale rows");
+static_assert(kScaleSfa + 8 * tc_sfa_stage<TcWide>() <= TcWide::kScaleEntry &&
+              kScaleSfa + 8 * tc_sfa_stage<TcSmall>() <= TcSmall::kScaleEntry, "scale ring entries");
+static_assert(TcSmall::kSlotBytes % 1024 == 0 && TcWide::kSlotBytes % 1024 == 0 && TcWide::kScaleEntry % 1024 == 0,
+              "swizzled operands are 1024-aligned");
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemAcc = 0;           // [128 lanes x 256 columns] (gate | up, or two down row blocks)
@@ -92,13 +139,15 @@ constexpr int kItemRing = 8;
 // global activation operand layouts (bytes); a "stage" is 256 consecutive K
 //   xb4: [T][H/256][8 term rows][128 B] packed E2M1, 128-byte swizzle (row phase = term)
 //   xsf: [T][H/256][8 term rows][8 blocks]
-//   hb4: [chunk][I/256][64 rows (8p + j)][128 B] swizzled; hsf: [chunk][I/256][64 rows][8 blocks]
-//   xc4 / xcs (larger blocks): the layer input gathered per chunk in the layout of hb4 / hsf
-//   ([chunk][H/256][64 rows][128 B] / [..][8 blocks]), so a gate/up stage needs one copy
+//   hb4: [chunk][I/256][R rows][128 B] swizzled; hsf: [chunk][I/256][R rows][8 blocks], R =
+//        the geometry's activation rows (TcSmall 64: 8p + j; TcWide 128: 4p + j or 8p + j)
+//   xc4 / xcs (blocks routed through the workspace): the layer input gathered per chunk in
+//   the layout of hb4 / hsf ([chunk][H/256][128 rows][128 B] / [..][8 blocks]), so a
+//   gate/up stage needs one copy
 __host__ __device__ constexpr size_t xb4_bytes(int T, int H) { return (size_t)T * (H / 2) * kTcTerms; }
 __host__ __device__ constexpr size_t xsf_bytes(int T, int H) { return (size_t)T * (H / 32) * kTcTerms; }
-__host__ __device__ constexpr size_t hb4_chunk_bytes(int I) { return (size_t)(I / 2) * kTcRowsA; }
-__host__ __device__ constexpr size_t hsf_chunk_bytes(int I) { return (size_t)(I / 32) * kTcRowsA; }
+__host__ __device__ constexpr size_t hb4_chunk_bytes(int I, int rows = kTcRowsA) { return (size_t)(I / 2) * rows; }
+__host__ __device__ constexpr size_t hsf_chunk_bytes(int I, int rows = kTcRowsA) { return (size_t)(I / 32) * rows; }
 // Width (bytes = 32-element blocks) of a weight-scale box for K: the largest
 // multiple of 16 that divides K / 32 and is at most 64.
 __host__ __device__ constexpr int scale_box_width(int K) {
@@ -171,7 +220,7 @@ struct TcItemInfo {
 
 struct TcSmem {
     uint8_t* slots;
-    uint8_t* scales;    // [kTcScaleRing][2 boxes][kTcScaleEntry / 2]
+    uint8_t* scales;    // [kTcScaleRing][entry]
     uint64_t *full, *empty, *accf, *acce, *ringf, *ringe, *sfull, *sempty, *epib, *drain;
     uint64_t *claim, *sfc, *drain2;   // slot claimed by the producer; scale factors in tensor memory; SF drain
     uint32_t* tmem_slot;
@@ -181,15 +230,18 @@ struct TcSmem {
     float* red;   // 64 floats of scratch for the persistent kernel's block reductions
 };
 
+// Shared memory of geometry C: the ring's slots, the scale ring (contiguous after them:
+// outside the expert phase the two are one scratch span), then barriers and records.
+template <class C>
 __device__ __forceinline__ TcSmem tc_smem(uint8_t* smem_raw) {
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     TcSmem s;
     s.slots = smem;
-    s.scales = smem + kTcStages * kTcSlotBytes;
-    uint8_t* aux = s.scales + kTcScaleRing * kTcScaleEntry;
+    s.scales = smem + C::kStages * C::kSlotBytes;
+    uint8_t* aux = s.scales + kTcScaleRing * C::kScaleEntry;
     uint64_t* b = reinterpret_cast<uint64_t*>(aux);
-    s.full = b; b += kTcStages;
-    s.empty = b; b += kTcStages;
+    s.full = b; b += C::kStages;
+    s.empty = b; b += C::kStages;
     s.accf = b; b += 1;
     s.acce = b; b += 1;
     s.ringf = b; b += kItemRing;
@@ -198,8 +250,8 @@ __device__ __forceinline__ TcSmem tc_smem(uint8_t* smem_raw) {
     s.sempty = b; b += kTcScaleRing;
     s.epib = b; b += 1;
     s.drain = b; b += 1;
-    s.claim = b; b += kTcStages;
-    s.sfc = b; b += kTcStages;
+    s.claim = b; b += C::kStages;
+    s.sfc = b; b += C::kStages;
     s.drain2 = b; b += 1;
     s.tmem_slot = reinterpret_cast<uint32_t*>(aux + 384);
     s.meta = reinterpret_cast<TcSlotMeta*>(aux + 400);
@@ -213,8 +265,9 @@ static_assert(400 + kTcStages * sizeof(TcSlotMeta) <= 640, "slot metadata");
 static_assert(640 + kItemRing * sizeof(TcItemInfo) + sizeof(RouteTable) + 64 * sizeof(float) <= kTcAuxBytes, "aux");
 
 // One thread initialises the barriers; then the block synchronises.
+template <class C>
 __device__ __forceinline__ void tc_smem_init(const TcSmem& s) {
-    for (int i = 0; i < kTcStages; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
         mbar_init(&s.full[i], 2);   // the producer (expect_tx) and the stage's activation loader
         mbar_init(&s.empty[i], 1);
     }
@@ -230,7 +283,7 @@ __device__ __forceinline__ void tc_smem_init(const TcSmem& s) {
     }
     mbar_init(s.epib, kTcEpiWarps);
     mbar_init(s.drain, 1);
-    for (int i = 0; i < kTcStages; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
         mbar_init(&s.claim[i], 1);
         mbar_init(&s.sfc[i], kTcSfWarps);
     }
@@ -388,12 +441,14 @@ __device__ __forceinline__ TcItemGeom tc_item_geom(const TcMaps& maps, const Ite
     }
     return g;
 }
-// kGathered: the gate/up items' activation operand comes per chunk (xc4 / xcs, one copy
-// per stage and one per scale group) instead of per token and pair.
-template <bool kGathered>
+// Geometry C; TcWide: the gate/up items' activation operand comes per chunk (xc4 / xcs,
+// one copy per stage and one per scale group) instead of per token and pair.
+template <class C>
 __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, const TcSmem& s_in,
                                         TcRoleState& rs_in, unsigned long long deadline) {
     // arguments and counters in registers (the caller's copies live in local memory)
+    constexpr bool kGathered = C::kWide;
+    constexpr uint32_t kATile = tc_a_tile<C>(), kSfa = tc_sfa_stage<C>();
     const TcArgs a = a_in;
     const TcSmem s = s_in;
     TcRoleState rs = rs_in;
@@ -432,15 +487,14 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
             ++rs.n;
         }
         if (end) {
-            const int slot = rs.it % kTcStages;
-            if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
+            const int slot = rs.it % C::kStages;
+            if (!wait_phase(&s.empty[slot], ((rs.it / C::kStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
             s.meta[slot] = TcSlotMeta{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};   // its loader adds the second arrival
             mbar_arrive(&s.claim[slot]);
             mbar_arrive(&s.full[slot]);
             ++rs.it;
             break;
         }
-        const int ntok = cur.ntok;
         const bool gu = kind == kItemGateUp;
         // the two 128-row weight boxes of a stage: (gate, up) rows rb*128.. or down rows rb*256.., +128
         const TcItemGeom g = tc_item_geom(maps, cur, H, I, wgu, wd);
@@ -475,9 +529,9 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                     failed = true;
                     break;
                 }
-                uint8_t* sdst = s.scales + se * kTcScaleEntry;
+                uint8_t* sdst = s.scales + se * C::kScaleEntry;
                 // the activation scales of per-token gate/up stages come from the loaders
-                const uint32_t sfa_bytes = (gu && !kGathered) ? 0u : (uint32_t)spb * 512;
+                const uint32_t sfa_bytes = (gu && !kGathered) ? 0u : (uint32_t)spb * kSfa;
                 mbar_arrive_expect_tx(&s.sfull[se], 2u * (uint32_t)sw * kTmaRows + sfa_bytes);
                 if (g.packed) {   // one contiguous box: both 128-row halves of the group
                     const int ys = g.ys0 + (st / spb) * 2 * sw;
@@ -491,24 +545,24 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                     tma_load_2d_stream(sdst + kScaleBox1, ms1, st * 8, r1, &s.sfull[se], pol);
                 }
                 if (gu && kGathered) {   // the chunk's gathered scales of the group's stages
-                    bulk_load(sdst + kScaleSfa, a.xcs + ((size_t)cur.chunk * (H / kTcKS) + st) * 512,
-                              (uint32_t)spb * 512, &s.sfull[se]);
+                    bulk_load(sdst + kScaleSfa, a.xcs + ((size_t)cur.chunk * (H / kTcKS) + st) * kSfa,
+                              (uint32_t)spb * kSfa, &s.sfull[se]);
                 } else if (!gu) {
-                    bulk_load(sdst + kScaleSfa, a.hsf + ((size_t)cur.chunk * (I / kTcKS) + st) * 512,
-                              (uint32_t)spb * 512, &s.sfull[se]);
+                    bulk_load(sdst + kScaleSfa, a.hsf + ((size_t)cur.chunk * (I / kTcKS) + st) * kSfa,
+                              (uint32_t)spb * kSfa, &s.sfull[se]);
                 }
                 ++rs.sc;
             }
-            const int slot = rs.it % kTcStages;
-            if (!wait_phase(&s.empty[slot], ((rs.it / kTcStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
+            const int slot = rs.it % C::kStages;
+            if (!wait_phase(&s.empty[slot], ((rs.it / C::kStages) & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
             s.meta[slot] = TcSlotMeta{kind,  st, nk, (int)rs.sc - 1, (st % spb) * 8, sw, st % spb == spb - 1 ? 1 : 0,
                                       spb,   g.packed ? kTmaRows * sw : kScaleBox1, (int)((rs.n - 1) % kItemRing)};
             mbar_arrive(&s.claim[slot]);   // the scale-factor warps may prepare this slot now
-            const uint32_t abytes = (gu && !kGathered) ? 0u : 8192u;   // per-token rows: the loaders
+            const uint32_t abytes = (gu && !kGathered) ? 0u : kATile;   // per-token rows: the loaders
             mbar_arrive_expect_tx(&s.full[slot], 2 * 16384 + abytes);
             tc_trace(a, 0, rs.it);
             ++rs.it;   // this slot now has copies in flight
-            uint8_t* dst = s.slots + (size_t)slot * kTcSlotBytes;
+            uint8_t* dst = s.slots + (size_t)slot * C::kSlotBytes;
             // rows shared by several chunks (pad[0] > 1) keep the normal L2 policy: the other
             // chunks read them again from L2
             if (g.packed) {   // one contiguous 32 KB box: the stage's 256 weight rows
@@ -522,10 +576,10 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
                 tma_load_2d_stream(dst + kSlotB + 16384, mq1, st * 128, r1, &s.full[slot], pol);
             }
             if (gu && kGathered) {
-                bulk_load(dst + kSlotA, a.xc4 + ((size_t)cur.chunk * (H / kTcKS) + st) * 8192, 8192, &s.full[slot]);
+                bulk_load(dst + kSlotA, a.xc4 + ((size_t)cur.chunk * (H / kTcKS) + st) * kATile, kATile, &s.full[slot]);
             } else if (!gu) {
                 const size_t cs = (size_t)cur.chunk * (I / kTcKS) + st;
-                bulk_load(dst + kSlotA, a.hb4 + cs * 8192, 8192, &s.full[slot]);
+                bulk_load(dst + kSlotA, a.hb4 + cs * kATile, kATile, &s.full[slot]);
             }
         }
         if (failed) break;
@@ -534,10 +588,10 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
     if (failed) {
         if (atomicExch(a.abort, 1) == 0) raise_status(a.status, MOE_ERR_TIMEOUT, a.layer * 65536);
         // every copy this CTA issued must land before the CTA exits
-        const uint32_t issued = rs.it < (uint32_t)kTcStages ? rs.it : (uint32_t)kTcStages;
+        const uint32_t issued = rs.it < (uint32_t)C::kStages ? rs.it : (uint32_t)C::kStages;
         for (uint32_t q = 0; q < issued; ++q) {
             const uint32_t last = rs.it - 1 - q;
-            drain_phase(&s.full[last % kTcStages], (last / kTcStages) & 1, globaltimer_ns() + a.timeout_ns);
+            drain_phase(&s.full[last % C::kStages], (last / C::kStages) & 1, globaltimer_ns() + a.timeout_ns);
         }
         const uint32_t sissued = rs.sc < (uint32_t)kTcScaleRing ? rs.sc : (uint32_t)kTcScaleRing;
         for (uint32_t q = 0; q < sissued; ++q) {
@@ -550,6 +604,7 @@ __device__ __noinline__ bool tc_produce(const TcMaps& maps, const TcArgs& a_in, 
 }
 
 // ---- MMA issuer (one thread) -----------------------------------------------------
+template <class C>
 __device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint32_t tmem, TcRoleState& rs_in,
                                     unsigned long long deadline) {
     const TcArgs a = a_in;
@@ -559,10 +614,10 @@ __device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint
     const uint32_t slots = smem_u32(s.slots);
     bool failed = false;
     for (;;) {
-        const int slot = rs.it % kTcStages;
+        const int slot = rs.it % C::kStages;
         // the stage's operands have landed and its scale factors are in tensor memory
-        if (!wait_phase(&s.full[slot], (rs.it / kTcStages) & 1, deadline, a.abort) ||
-            !wait_phase(&s.sfc[slot], (rs.it / kTcStages) & 1, deadline, a.abort)) {
+        if (!wait_phase(&s.full[slot], (rs.it / C::kStages) & 1, deadline, a.abort) ||
+            !wait_phase(&s.sfc[slot], (rs.it / C::kStages) & 1, deadline, a.abort)) {
             failed = true;
             break;
         }
@@ -581,7 +636,7 @@ __device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint
             if (!wait_phase(s.acce, (rs.n & 1) ^ 1, deadline, a.abort)) { failed = true; break; }
             tc_fence_after();
         }
-        const uint32_t sl = slots + (uint32_t)slot * kTcSlotBytes;
+        const uint32_t sl = slots + (uint32_t)slot * C::kSlotBytes;
         const uint32_t sf = tmem + kTmemSf + kTmemSfSlot * slot;
         const uint64_t ad = smem_desc_sw128(sl + kSlotA), bd = smem_desc_sw128(sl + kSlotB);
 #pragma unroll
@@ -609,8 +664,8 @@ __device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint
 // base + n / 32 (one 32-bit cell = 4 blocks; group g = blocks 4g..4g+3 of the
 // stage).  tcgen05.cp 32x128b.warpx4 puts 16-byte row r of a 512-byte block into
 // columns +0..3 of lane r of every quarter, so the six blocks of a stage are:
-// SFA group g (block g), row r = cells of activation rows r, 32 + r (rows 64..
-// unused, zero); SFB group g, half h (block 2 + 2g + h), row r = cells of weight
+// SFA group g (block g), row r = cells of activation rows r, 32 + r, 64 + r, 96 + r
+// (TcSmall: rows 64.. unused, zero); SFB group g, half h (block 2 + 2g + h), row r = cells of weight
 // rows 128h + r, 128h + 32 + r, 128h + 64 + r, 128h + 96 + r.  Warp w = 0, 1 builds
 // the SFB blocks of half h = w (both groups), warp 2 the SFA blocks; lane r builds
 // row r, and lane 0 copies the warp's two blocks into the slot's tensor-memory
@@ -618,26 +673,28 @@ __device__ __noinline__ bool tc_mma(const TcArgs& a_in, const TcSmem& s_in, uint
 // A slot is prepared as soon as the producer has claimed it (its previous MMAs are
 // done): the scales come from the scale ring, not from the slot's own copies, so
 // the work overlaps the stage's weight copies.
-// kGathered: as for tc_produce (the activation scales of gate/up stages are laid out per
-// stage, like the down items', instead of per pair).
-template <bool kGathered>
+// TcWide: the activation scales of gate/up stages are gathered per chunk and laid out
+// per stage, like the down items', instead of per pair.
+template <class C>
 __device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, uint32_t tmem, TcRoleState& rs_in, int w,
                                    int lane, unsigned long long deadline) {
+    constexpr bool kGathered = C::kWide;
+    constexpr int kQ = C::kRowsA / 32;   // lane quarters of used activation rows
     const TcArgs a = a_in;
     const TcSmem s = s_in;
     TcRoleState rs = rs_in;
     bool failed = false;
     for (;;) {
-        const int slot = rs.it % kTcStages;
-        const uint32_t ph = (rs.it / kTcStages) & 1;
+        const int slot = rs.it % C::kStages;
+        const uint32_t ph = (rs.it / C::kStages) & 1;
         if (!warp_wait_phase(&s.claim[slot], ph, deadline, a.abort)) { failed = true; break; }
         const TcSlotMeta m = s.meta[slot];
         if (w == 0 && lane == 0) tc_trace(a, 1, rs.it);
         if (m.kind >= 0) {
             const int se = m.sc % kTcScaleRing;
             if (!warp_wait_phase(&s.sfull[se], (m.sc / kTcScaleRing) & 1, deadline, a.abort)) { failed = true; break; }
-            const uint8_t* ent = s.scales + se * kTcScaleEntry;
-            uint8_t* at = s.slots + (size_t)slot * kTcSlotBytes + kSlotAtoms;
+            const uint8_t* ent = s.scales + se * C::kScaleEntry;
+            uint8_t* at = s.slots + (size_t)slot * C::kSlotBytes + C::kAtoms;
             int b0, b1;   // the warp's two blocks
             if (w < 2) {
                 uint2 v[4];
@@ -656,27 +713,27 @@ __device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, uint3
                 b1 = 4 + w;
                 *reinterpret_cast<uint4*>(at + b0 * 512 + lane * 16) = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
                 *reinterpret_cast<uint4*>(at + b1 * 512 + lane * 16) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
-            } else {   // activation rows lane and 32 + lane (row 8p + j; sg = stage within the scale group)
+            } else {   // activation rows 32 c + lane (sg = stage within the scale group)
                 const int sg = m.sc_off / 8;
-                uint2 v[2];
+                uint2 v[4];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     const int row = 32 * c + lane;
                     const int off = (!kGathered && m.kind == kItemGateUp)
                                         ? (row >> 3) * m.pad * 64 + sg * 64 + (row & 7) * 8
-                                        : sg * 512 + row * 8;
-                    v[c] = *reinterpret_cast<const uint2*>(ent + kScaleSfa + off);
+                                        : sg * tc_sfa_stage<C>() + row * 8;
+                    v[c] = c < kQ ? *reinterpret_cast<const uint2*>(ent + kScaleSfa + off) : make_uint2(0u, 0u);
                 }
                 b0 = 0;
                 b1 = 1;
-                *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(v[0].x, v[1].x, 0u, 0u);
-                *reinterpret_cast<uint4*>(at + 512 + lane * 16) = make_uint4(v[0].y, v[1].y, 0u, 0u);
+                *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+                *reinterpret_cast<uint4*>(at + 512 + lane * 16) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
             }
             fence_proxy_async_shared();   // read next by tcgen05.cp
             __syncwarp();
             if (lane == 0) {
                 if (m.sc_last) mbar_arrive(&s.sempty[se]);
-                const uint32_t sl = smem_u32(s.slots) + (uint32_t)slot * kTcSlotBytes + kSlotAtoms;
+                const uint32_t sl = smem_u32(s.slots) + (uint32_t)slot * C::kSlotBytes + C::kAtoms;
                 const uint32_t sf = tmem + kTmemSf + kTmemSfSlot * slot;
                 tc_cp_32x128_x4(sf + 4 * b0, smem_desc_rows16(sl + 512 * b0));
                 tc_cp_32x128_x4(sf + 4 * b1, smem_desc_rows16(sl + 512 * b1));
@@ -705,7 +762,9 @@ __device__ __noinline__ bool tc_sf(const TcArgs& a_in, const TcSmem& s_in, uint3
 // waits for its copies, makes them visible to the tensor cores' proxy and arrives on
 // the stage's full barrier (and the group's scale barrier); for every other stage it
 // arrives at once.  All loaders follow every ring position, so that each one sees the
-// END slot.
+// END slot.  TcWide: every operand comes by bulk copy (gathered per chunk); the loaders
+// only arrive.
+template <class C>
 __device__ __noinline__ bool tc_load(const TcArgs& a_in, const TcSmem& s_in, TcRoleState& rs_in, int li, int lane,
                                      unsigned long long deadline) {
     const TcArgs a = a_in;
@@ -714,8 +773,8 @@ __device__ __noinline__ bool tc_load(const TcArgs& a_in, const TcSmem& s_in, TcR
     const int nst = a.H / kTcKS;
     bool failed = false;
     for (;;) {
-        const int slot = rs.it % kTcStages;
-        if (!warp_wait_phase(&s.claim[slot], (rs.it / kTcStages) & 1, deadline, a.abort)) { failed = true; break; }
+        const int slot = rs.it % C::kStages;
+        if (!warp_wait_phase(&s.claim[slot], (rs.it / C::kStages) & 1, deadline, a.abort)) { failed = true; break; }
         const TcSlotMeta m = s.meta[slot];
         const bool mine = (int)(rs.it % kTcLoaders) == li;
         ++rs.it;
@@ -724,17 +783,17 @@ __device__ __noinline__ bool tc_load(const TcArgs& a_in, const TcSmem& s_in, TcR
             continue;
         }
         const bool first = m.kind >= 0 && m.sc_off == 0;   // the first stage of a scale group
-        if (m.kind == kItemGateUp && !a.xc4) {
+        if (!C::kWide && m.kind == kItemGateUp && !a.xc4) {
             const TcItemInfo& inf = s.ring[m.ri];
             const int ntok = inf.ntok;
-            const uint32_t dst = smem_u32(s.slots + (size_t)slot * kTcSlotBytes + kSlotA);
+            const uint32_t dst = smem_u32(s.slots + (size_t)slot * C::kSlotBytes + kSlotA);
             for (int p = 0; p < ntok; ++p) {
                 const uint8_t* src = a.xb4 + ((size_t)inf.ids[p] * nst + m.stage) * 1024;
                 cp_async_16(dst + p * 1024 + lane * 16, src + lane * 16);
                 cp_async_16(dst + p * 1024 + 512 + lane * 16, src + 512 + lane * 16);
             }
             if (first) {   // the group's activation scales: per pair spb stages x 64 B, contiguous in xsf
-                const uint32_t sdst = smem_u32(s.scales + (m.sc % kTcScaleRing) * kTcScaleEntry + kScaleSfa);
+                const uint32_t sdst = smem_u32(s.scales + (m.sc % kTcScaleRing) * C::kScaleEntry + kScaleSfa);
                 const int per = m.pad * 4;   // 16-byte pieces per pair (spb x 64 B)
                 for (int i = lane; i < ntok * per; i += 32) {
                     const int p = i / per, q = i % per;
@@ -810,26 +869,29 @@ __device__ __forceinline__ void group4_reduce_scatter(const float (&v)[32], floa
     // out[i]: k = (lane & 3) | i << 2
 }
 
-// ---- epilogue warps (lane quarter q = warp % 4 < 2, column chunk c = warp / 4) -----
+// ---- epilogue warps (lane quarter q = warp % 4, 32-column chunks c) --------------
+// TcSmall: warps of quarters 0 and 1, c = warp / 4; TcWide: warps 0..7, c = warp / 4 and
+// warp / 4 + 2.  Each warp reads, per chunk c, columns 32c.. (gate rows / first down
+// block) and 128 + 32c.. (up rows / second down block) of its 32 lanes.
 // kDense = false: accumulator lane 32q + l is activation row 32q + l: pair slot 4q + l / 8,
 // term l % 8; after the reduce-scatter over groups of 8 lanes, lane l holds, for its pair,
 // the sums of columns 32c + 8s + (l % 8) and 128 + 32c + 8s + (l % 8), s = 0..3.
-// kDense = true (16 pairs x 4 terms): pair slot 8q + l / 4, term l % 4; lane l holds the
-// sums of columns 32c + 4s + (l % 4) and 128 + .., s = 0..7.
-// The warp reads columns 32c.. (gate rows / first down block) and 128 + 32c.. (up rows /
-// second down block).
+// kDense = true (4 terms): pair slot 8q + l / 4, term l % 4; lane l holds the sums of
+// columns 32c + 4s + (l % 4) and 128 + .., s = 0..7.
+// TcWide items carry their pairs' ids as 16-bit halves (two per word of the record).
 // kNorm (residual stack): the layer input's operand is r * w_norm without the per-token
 // factor 1 / rms(r), which the gate/up outputs take here, from the shared-memory routing
 // table: its tscale (a.rt set: the block was routed in shared memory) or tscale_g.
-template <bool kDense, bool kNorm>
+template <class C, bool kDense, bool kNorm>
 __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in, uint32_t tmem, TcRoleState& rs_in,
                                          int warp, int lane, unsigned long long deadline) {
     constexpr int kT = kDense ? 4 : kTcTerms;   // terms per activation: lanes (accumulator rows) per pair
     constexpr int kV = 32 / kT;                 // columns per lane of each 32-column chunk
+    constexpr int kCW = C::kChunksPerEpiWarp;   // 32-column chunks of this warp: c0, c0 + 2
     const TcArgs a = a_in;
     const TcSmem s = s_in;
     TcRoleState rs = rs_in;
-    const int q = warp & 3, c = warp >> 2;
+    const int q = warp & 3, c0 = warp >> 2;
     const int H = a.H, I = a.I;
     const int p = (32 / kT) * q + lane / kT, j = lane % kT;   // pair slot and term of this lane's row
     const int base = lane & ~(kT - 1);                        // first lane of the pair
@@ -850,23 +912,62 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
             break;
         }
         const int kind = s.ring[re].kind, chunk = s.ring[re].chunk, rb = s.ring[re].rb, ntok = s.ring[re].ntok;
-        const int my_id = s.ring[re].ids[p];   // this lane's pair: token (gate/up) or pair id (down)
+        // this lane's pair: token (gate/up) or pair id (down)
+        const int my_id = C::kWide ? (s.ring[re].ids[p >> 1] >> (16 * (p & 1))) & 0xFFFF : s.ring[re].ids[p];
         tc_fence_after();
         if (warp == 0 && lane == 0) tc_trace(a, 5, rs.n);
-        float G[kV], U[kV];
+        const bool mine = p < ntok;
+        // TcSmall: G, U = the column sums (gate / up, or the two down blocks), used after the
+        // accumulator is released.  TcWide: each chunk is finished as soon as it is read, so
+        // that only 8 values per chunk stay live: down items store their sums at once (the
+        // stores do not wait), gate/up items keep h = silu(g) * u in G.
+        float G[kCW][kV], U[kCW][kV];
         if (kind >= 0) {
-            uint32_t r0[32], r1[32];
-            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemAcc + 32 * c;
-            tc_ld_x32(ta, r0);
-            tc_ld_x32(ta + 128, r1);
-            tc_wait_ld();
-            float v[32];
+            if constexpr (kCW == 1) {   // both column blocks in flight at once
+                uint32_t r0[32], r1[32];
+                const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemAcc + 32 * c0;
+                tc_ld_x32(ta, r0);
+                tc_ld_x32(ta + 128, r1);
+                tc_wait_ld();
+                float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
-            if constexpr (kDense) group4_reduce_scatter(v, G, lane); else group8_reduce_scatter(v, G, lane);
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
+                if constexpr (kDense) group4_reduce_scatter(v, G[0], lane); else group8_reduce_scatter(v, G[0], lane);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r1[i]);
-            if constexpr (kDense) group4_reduce_scatter(v, U, lane); else group8_reduce_scatter(v, U, lane);
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r1[i]);
+                if constexpr (kDense) group4_reduce_scatter(v, U[0], lane); else group8_reduce_scatter(v, U[0], lane);
+            } else {
+                float sc = 1.0f;   // RMSNorm(r) = (r * w_norm) / rms(r): the per-token factor
+                if constexpr (kNorm)
+                    if (kind == kItemGateUp && mine) sc = a.rt ? a.rt->tscale[my_id] : __ldcg(s.rt->tscale_g + my_id);
+#pragma unroll
+                for (int h = 0; h < kCW; ++h) {
+                    const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemAcc + 32 * (c0 + 2 * h);
+                    uint32_t r[32];
+                    float v[32];
+                    tc_ld_x32(ta, r);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                    if constexpr (kDense) group4_reduce_scatter(v, G[h], lane); else group8_reduce_scatter(v, G[h], lane);
+                    tc_ld_x32(ta + 128, r);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                    if constexpr (kDense) group4_reduce_scatter(v, U[h], lane); else group8_reduce_scatter(v, U[h], lane);
+                    if (kind == kItemGateUp) {
+#pragma unroll
+                        for (int i = 0; i < kV; ++i) G[h][i] = silu(G[h][i] * sc) * (U[h][i] * sc);
+                    } else if (mine) {   // down: rows rb * 256 + 32c + kT s + j and + 128
+                        float* dst = a.partial + (size_t)my_id * H + (size_t)rb * kTcN + 32 * (c0 + 2 * h) + j;
+#pragma unroll
+                        for (int i = 0; i < kV; ++i) {
+                            dst[kT * i] = G[h][i];
+                            dst[128 + kT * i] = U[h][i];
+                        }
+                    }
+                }
+            }
         }
         tc_fence_before();
         __syncwarp();
@@ -876,64 +977,68 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
         }
         ++rs.n;
         if (kind < 0) break;
-        const bool mine = p < ntok;
         if (kind == kItemGateUp) {
             // h = silu(g) * u for rows 32c + kT s + j of the item's 128 (s < kV); the 32 rows
             // 32c.. are one MX block of the down projection's K.  Split into kT E2M1 terms
             // with block scales over the pair's kT lanes, stored as rows kT p + t of the
             // chunk's down operand at K = rb * 128 + 32c + kT s + j.
-            if constexpr (kNorm) {   // g and u of RMSNorm(r) = (g and u of r * w_norm) / rms(r), per token
+            if constexpr (kNorm && kCW == 1) {   // g and u of RMSNorm(r) = (g and u of r * w_norm) / rms(r), per token
                 const float sc = mine ? (a.rt ? a.rt->tscale[my_id] : __ldcg(s.rt->tscale_g + my_id)) : 1.0f;
 #pragma unroll
                 for (int i = 0; i < kV; ++i) {
-                    G[i] *= sc;
-                    U[i] *= sc;
+                    G[0][i] *= sc;
+                    U[0][i] *= sc;
                 }
             }
-            float hv[kV];
 #pragma unroll
-            for (int i = 0; i < kV; ++i) hv[i] = silu(G[i]) * U[i];
-            uint32_t codes[kV];   // per s: term t in bits 4t..4t+3
+            for (int h = 0; h < kCW; ++h) {
+                const int c = c0 + 2 * h;
+                float hv[kV];
 #pragma unroll
-            for (int i = 0; i < kV; ++i) codes[i] = 0u;
-            uint32_t sbt = 0;     // this lane's scale byte: term j
+                for (int i = 0; i < kV; ++i) hv[i] = kCW == 1 ? silu(G[0][i]) * U[0][i] : G[h][i];
+                uint32_t codes[kV];   // per s: term t in bits 4t..4t+3
 #pragma unroll
-            for (int t = 0; t < kT; ++t) {
-                float mx = 0.0f;
+                for (int i = 0; i < kV; ++i) codes[i] = 0u;
+                uint32_t sbt = 0;     // this lane's scale byte: term j
 #pragma unroll
-                for (int i = 0; i < kV; ++i) mx = fmaxf(mx, fabsf(hv[i]));
+                for (int t = 0; t < kT; ++t) {
+                    float mx = 0.0f;
 #pragma unroll
-                for (int o = 1; o < kT; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-                const uint32_t eb = __float_as_uint(mx) >> 23;
-                if (eb >= 8u && eb < 255u) {
-                    uint32_t xb = eb - 2u;
-                    if (mx > 6.0f * __uint_as_float(xb << 23)) ++xb;
-                    const float X = __uint_as_float(xb << 23);
-                    const float inv = __uint_as_float((254u - xb) << 23);
+                    for (int i = 0; i < kV; ++i) mx = fmaxf(mx, fabsf(hv[i]));
 #pragma unroll
-                    for (int i = 0; i < kV; ++i) {
-                        const uint32_t cd = f32_to_e2m1(hv[i] * inv);
-                        hv[i] = fmaf(-e2m1_code_to_f32(cd), X, hv[i]);
-                        codes[i] |= cd << (4 * t);
+                    for (int o = 1; o < kT; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+                    const uint32_t eb = __float_as_uint(mx) >> 23;
+                    if (eb >= 8u && eb < 255u) {
+                        uint32_t xb = eb - 2u;
+                        if (mx > 6.0f * __uint_as_float(xb << 23)) ++xb;
+                        const float X = __uint_as_float(xb << 23);
+                        const float inv = __uint_as_float((254u - xb) << 23);
+#pragma unroll
+                        for (int i = 0; i < kV; ++i) {
+                            const uint32_t cd = f32_to_e2m1(hv[i] * inv);
+                            hv[i] = fmaf(-e2m1_code_to_f32(cd), X, hv[i]);
+                            codes[i] |= cd << (4 * t);
+                        }
+                        if (t == j) sbt = xb;
                     }
-                    if (t == j) sbt = xb;
                 }
-            }
-            // lane j of the pair gathers term j's codes of the pair's kT lanes: column n (0..31)
-            // of the chunk is value n / kT of lane n % kT
-            uint32_t wd[4] = {0u, 0u, 0u, 0u};
+                // lane j of the pair gathers term j's codes of the pair's kT lanes: column n (0..31)
+                // of the chunk is value n / kT of lane n % kT
+                uint32_t wd[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int n = 0; n < 32; ++n) {
-                const uint32_t v = __shfl_sync(0xFFFFFFFFu, codes[n / kT], base + n % kT);
-                wd[n / 8] |= ((v >> (4 * j)) & 0xFu) << (4 * (n % 8));
-            }
-            if (mine) {
-                uint8_t* hb = a.hb4 + (size_t)chunk * hb4_chunk_bytes(I) + (size_t)(rb >> 1) * 8192;
-                const int n = kT * p + j;                    // operand row: pair slot p, term j
-                const int chunk16 = (rb & 1) * 4 + c;        // 16-byte chunk of K (rb&1)*128 + 32c .. +31
-                *reinterpret_cast<uint4*>(hb + n * 128 + ((chunk16 ^ (n & 7)) << 4)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-                a.hsf[(size_t)chunk * hsf_chunk_bytes(I) + (size_t)(rb >> 1) * 512 + n * 8 + 4 * (rb & 1) + c] =
-                    (uint8_t)sbt;
+                for (int n = 0; n < 32; ++n) {
+                    const uint32_t v = __shfl_sync(0xFFFFFFFFu, codes[n / kT], base + n % kT);
+                    wd[n / 8] |= ((v >> (4 * j)) & 0xFu) << (4 * (n % 8));
+                }
+                if (mine) {
+                    uint8_t* hb = a.hb4 + (size_t)chunk * hb4_chunk_bytes(I, C::kRowsA) + (size_t)(rb >> 1) * tc_a_tile<C>();
+                    const int n = kT * p + j;                    // operand row: pair slot p, term j
+                    const int chunk16 = (rb & 1) * 4 + c;        // 16-byte chunk of K (rb&1)*128 + 32c .. +31
+                    *reinterpret_cast<uint4*>(hb + n * 128 + ((chunk16 ^ (n & 7)) << 4)) =
+                        make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                    a.hsf[(size_t)chunk * hsf_chunk_bytes(I, C::kRowsA) + (size_t)(rb >> 1) * tc_sfa_stage<C>() + n * 8 +
+                          4 * (rb & 1) + c] = (uint8_t)sbt;
+                }
             }
             fence_proxy_async_global();   // read next by bulk copies
             if (!epi_sync()) { failed = true; break; }
@@ -942,12 +1047,12 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
                 fence_proxy_async_global();
                 red_release_add_gpu(a.done + chunk, 1);
             }
-        } else if (mine) {   // down: rows rb * 256 + 32c + kT s + j and + 128
-            float* dst = a.partial + (size_t)my_id * H + (size_t)rb * kTcN + 32 * c + j;
+        } else if (kCW == 1 && mine) {   // down: rows rb * 256 + 32c + kT s + j and + 128
+            float* dst = a.partial + (size_t)my_id * H + (size_t)rb * kTcN + 32 * c0 + j;
 #pragma unroll
             for (int i = 0; i < kV; ++i) {
-                dst[kT * i] = G[i];
-                dst[128 + kT * i] = U[i];
+                dst[kT * i] = G[0][i];
+                dst[128 + kT * i] = U[0][i];
             }
         }
     }
@@ -956,31 +1061,33 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
     return !failed;
 }
 
-// One expert phase, dispatched by warp role; every thread of the block calls it.
-template <bool kGathered, bool kNorm = false>
+// One expert phase of geometry C, dispatched by warp role; every thread of the block
+// calls it.
+template <class C, bool kNorm = false>
 __device__ __forceinline__ void tc_phase(const TcMaps& maps, const TcArgs& a, const TcSmem& s, uint32_t tmem,
                                          TcRoleState& rs, unsigned long long deadline) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == kTcWarpProducer) {
-        if (lane == 0) tc_produce<kGathered>(maps, a, s, rs, deadline);
-    } else if (warp == kTcWarpMma) {
-        if (lane == 0) tc_mma(a, s, tmem, rs, deadline);
-    } else if (tc_is_sf_warp(warp)) {
-        tc_sf<kGathered>(a, s, tmem, rs, (warp == 6) ? 0 : (warp == 7) ? 1 : 2, lane, deadline);
-    } else if (tc_loader_index(warp) >= 0) {
-        tc_load(a, s, rs, tc_loader_index(warp), lane, deadline);
-    } else if (tc_is_epi_warp(warp)) {
-        if (kGathered && a.dense) tc_epilogue<true, kNorm>(a, s, tmem, rs, warp, lane, deadline);
-        else tc_epilogue<false, kNorm>(a, s, tmem, rs, warp, lane, deadline);
+    if (warp == C::kProducer) {
+        if (lane == 0) tc_produce<C>(maps, a, s, rs, deadline);
+    } else if (warp == C::kMma) {
+        if (lane == 0) tc_mma<C>(a, s, tmem, rs, deadline);
+    } else if (C::sf_index(warp) >= 0) {
+        tc_sf<C>(a, s, tmem, rs, C::sf_index(warp), lane, deadline);
+    } else if (C::loader_index(warp) >= 0) {
+        tc_load<C>(a, s, rs, C::loader_index(warp), lane, deadline);
+    } else if (C::epi_warp(warp)) {
+        if (C::kWide && a.dense) tc_epilogue<C, true, kNorm>(a, s, tmem, rs, warp, lane, deadline);
+        else tc_epilogue<C, false, kNorm>(a, s, tmem, rs, warp, lane, deadline);
     }
 }
 
 // Setup shared by the standalone and persistent kernels: barriers (thread 0) and
 // the tensor-memory allocation (the MMA warp).  Ends with a block-wide barrier.
+template <class C>
 __device__ __forceinline__ uint32_t tc_setup(const TcSmem& s) {
     const int warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) tc_smem_init(s);
-    if (warp == kTcWarpMma) {
+    if (threadIdx.x == 0) tc_smem_init<C>(s);
+    if (warp == C::kMma) {
         tmem_alloc(s.tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -992,28 +1099,29 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& s) {
 
 // Teardown: every tcgen05 operation of the MMA thread has completed (bounded
 // wait), then the MMA warp frees the tensor memory.  All threads call it.
+template <class C>
 __device__ __forceinline__ void tc_teardown(const TcSmem& s, uint32_t tmem, unsigned long long timeout_ns) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == kTcWarpMma && lane == 0) {
+    if (warp == C::kMma && lane == 0) {
         tc_commit(s.drain);
         drain_phase(s.drain, 0, globaltimer_ns() + timeout_ns);
     }
-    if (tc_is_sf_warp(warp) && lane == 0) {   // the scale-factor warps' tensor-memory copies
+    if (C::sf_index(warp) >= 0 && lane == 0) {   // the scale-factor warps' tensor-memory copies
         tc_commit(s.drain2);
         drain_phase(s.drain2, 0, globaltimer_ns() + timeout_ns);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kTcWarpMma) tmem_dealloc(tmem, kTmemCols);
+    if (warp == C::kMma) tmem_dealloc(tmem, kTmemCols);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) expert_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs args) {
     extern __shared__ uint8_t smem_raw[];
-    const TcSmem s = tc_smem(smem_raw);
-    const uint32_t tmem = tc_setup(s);
+    const TcSmem s = tc_smem<TcSmall>(smem_raw);
+    const uint32_t tmem = tc_setup<TcSmall>(s);
     const unsigned long long deadline = globaltimer_ns() + args.timeout_ns;
-    if (threadIdx.x == kTcWarpProducer * 32) {
+    if (threadIdx.x == TcSmall::kProducer * 32) {
         prefetch_tensormap(&maps.gate_q);
         prefetch_tensormap(&maps.up_q);
         prefetch_tensormap(&maps.down_q);
@@ -1022,8 +1130,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) expert_tc_kernel(const __grid_c
         prefetch_tensormap(&maps.down_s);
     }
     TcRoleState rs{0u, 0u, 0u, 0u};
-    tc_phase<false>(maps, args, s, tmem, rs, deadline);
-    tc_teardown(s, tmem, args.timeout_ns);
+    tc_phase<TcSmall>(maps, args, s, tmem, rs, deadline);
+    tc_teardown<TcSmall>(s, tmem, args.timeout_ns);
 }
 
 // Input staging of one layer, one block of 1024 threads per token:

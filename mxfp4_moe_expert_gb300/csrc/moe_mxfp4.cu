@@ -93,19 +93,21 @@ WsLayout ws_layout(const moe_mxfp4_config& c, int T) {
     L.hbuf = take((size_t)T * k * I * 4);
     L.partial = take((size_t)T * k * H * 4);
     const size_t chunks = max_chunks(c, T);
+    // larger blocks (routed through the workspace): 128 operand rows per chunk (the wide
+    // expert phase) and the input operand gathered per chunk
+    const bool gathered = !((size_t)T * k <= 64 && (size_t)T * E <= 8192);
+    const int rows = gathered ? moe::TcWide::kRowsA : moe::TcSmall::kRowsA;
     L.xb4 = take(moe::xb4_bytes(T, (int)H));
     L.xsf = take(moe::xsf_bytes(T, (int)H));
     L.ss = take((size_t)T * (H / 256 + 1) * 4);
-    L.hb4 = take(chunks * moe::hb4_chunk_bytes((int)I));
-    L.hsf = take(chunks * moe::hsf_chunk_bytes((int)I));
+    L.hb4 = take(chunks * moe::hb4_chunk_bytes((int)I, rows));
+    L.hsf = take(chunks * moe::hsf_chunk_bytes((int)I, rows));
     L.items = take(max_items(c, T) * sizeof(moe::ItemRec));
     L.sync = take((8 + chunks) * 4);   // n_items[2], queue, abort, ..., done[chunks]
     L.rpart = take((size_t)(H / 256 + 1) * T * E * 4);   // router partials per column slice / block (>= 256 columns)
     L.chunk0 = take((E + 1) * 4);
-    // larger blocks (routed through the workspace): the input operand gathered per chunk
-    const bool gathered = !((size_t)T * k <= 64 && (size_t)T * E <= 8192);
-    L.xc4 = take(gathered ? chunks * (H / 256) * 8192 : 0);
-    L.xcs = take(gathered ? chunks * (H / 256) * 512 : 0);
+    L.xc4 = take(gathered ? chunks * (H / 256) * moe::tc_a_tile<moe::TcWide>() : 0);
+    L.xcs = take(gathered ? chunks * (H / 256) * moe::tc_sfa_stage<moe::TcWide>() : 0);
     L.tsc = take((size_t)T * 4);   // per-token 1 / rms of a residual stack (larger blocks)
     L.total = o;
     return L;
@@ -424,6 +426,8 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
     if (!small_block) {   // larger blocks: gathered input operand, dense unless disabled
         p.ta.xc4 = reinterpret_cast<uint8_t*>(ws + L.xc4);
         p.ta.xcs = reinterpret_cast<uint8_t*>(ws + L.xcs);
+        // chunks of 128 operand rows: 32 pairs x 4 terms, or 16 x 8 without the dense operand
+        p.chunk = moe::kWideTok;
         if (!(c.flags & MOE_FLAG_NO_DENSE)) {
             p.chunk = moe::kDenseTok;
             p.terms = 4;
@@ -641,7 +645,9 @@ int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens
     char* ws = static_cast<char*>(workspace_dev);
     const bool tma_fits = num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok;
     if (h->packed && !tma_fits) return MOE_ERR_UNSUPPORTED;   // the fallback path reads canonical experts
-    // the TMA work-item code holds up to 512 token chunks of 8 per expert
+    // the TMA work-item code holds up to 512 token chunks of 8 per expert (and the wide
+    // expert phase's records hold pair ids as 16-bit halves)
+    static_assert(512 * moe::kTmaTok <= 65536, "pair ids of the persistent path fit 16 bits");
     if (h->tma && num_tokens * h->cfg.top_k <= 512 * moe::kTmaTok) {
         const bool events = dbg && dbg->expert_events;
         if (h->persist_grid > 0 && !(h->cfg.flags & MOE_FLAG_MULTI_KERNEL) && !events)

@@ -77,8 +77,8 @@ struct PersistParams {
     float* rpart;      // [H / rslice, T, E] router slice partials
     int rslice;        // columns per router unit (256, 512 or 1024; divides H)
     int rfull;         // experts per whole-row router unit (router_full_unit), or 0: column-sliced units
-    int chunk;         // pairs per chunk of a block routed through the workspace (8, or 16 dense)
-    int terms;         // E2M1 terms per activation in those chunks (8, or 4 dense)
+    int chunk;         // pairs per chunk of a block routed through the workspace (32 dense, or 16)
+    int terms;         // E2M1 terms per activation in those chunks (4 dense, or 8): 128 operand rows
     int rtok;          // tokens per router unit (T for blocks routed in shared memory; else a multiple of 8 G)
     int* rcnt;         // [kMaxPersistLayers, 32] finished router units per expert group (0 at rest)
     unsigned long long* tstamp;   // CTA 0's %globaltimer at phase ends (or NULL)
@@ -1156,11 +1156,14 @@ __device__ __noinline__ void build_items_slice(const PersistParams& p, int* scra
         r.e = s_act[lo];
         r.beg = s_beg[lo] + tc * p.chunk;
         r.ntok = min(p.chunk, s_cnt[lo] - tc * p.chunk);
-        int pq[kMaxChunk];
+        // the pairs' ids as 16-bit halves (T * k <= 4096 on this path): word q holds pair
+        // slots 2q (low half) and 2q + 1
 #pragma unroll
-        for (int q = 0; q < kMaxChunk; ++q) pq[q] = q < r.ntok ? __ldcg(rb.perm + r.beg + q) : 0;
-#pragma unroll
-        for (int q = 0; q < kMaxChunk; ++q) r.tok[q] = q < r.ntok ? (down ? pq[q] : pq[q] / k) : 0;
+        for (int q = 0; q < kMaxChunk; ++q) {
+            const int p0 = 2 * q < r.ntok ? __ldcg(rb.perm + r.beg + 2 * q) : 0;
+            const int p1 = 2 * q + 1 < r.ntok ? __ldcg(rb.perm + r.beg + 2 * q + 1) : 0;
+            r.tok[q] = down ? (p0 | (p1 << 16)) : ((p0 / k) | ((p1 / k) << 16));
+        }
         r.chunk = s_c0[lo] + tc;
         r.pad[0] = nch;
         r.pad[1] = r.pad[2] = 0;
@@ -1168,34 +1171,42 @@ __device__ __noinline__ void build_items_slice(const PersistParams& p, int* scra
     }
 }
 
-constexpr uint32_t kGatherBufBase = 17408, kGatherBufBytes = 9216;   // per-warp staging buffers (slot area)
-static_assert(kGatherBufBase + 16 * kGatherBufBytes <= (uint32_t)kTcStages * kTcSlotBytes, "gather buffers in the slot area");
+// per-warp staging buffers of the gather: in the slot area and the scale ring, which are
+// one contiguous span and idle between expert phases
+constexpr uint32_t kGatherBufBase = 17408, kGatherBufBytes = 9216;
+static_assert(kGatherBufBase + 16 * kGatherBufBytes <=
+                  (uint32_t)(TcWide::kStages * TcWide::kSlotBytes + kTcScaleRing * TcWide::kScaleEntry),
+              "gather buffers in the slot area and the scale ring");
 static_assert(4 * (kMaxExperts + 1) * sizeof(int) <= kGatherBufBase, "routing arrays below the gather buffers");
 // The layer input's expert operand gathered per chunk (larger blocks, every CTA, after
-// the grouping is published): unit = (chunk, 256-wide stage), one warp per unit; pair
-// slot p of the chunk gets the first p.terms of its token's 8 term rows (rows
-// p.terms * p + j; the first 4 terms of the 8-term split are the 4-term split) and their
-// scales.
+// the grouping is published) into the 128-row layout of the wide expert phase: unit =
+// (chunk, 256-wide stage, half h), one warp per unit; pair slot p of the chunk gets the
+// first p.terms of its token's 8 term rows (rows p.terms * p + j; the first 4 terms of
+// the 8-term split are the 4-term split) and their scales; half h holds the pair slots
+// h * chunk / 2 .. (rows 64 h .. 64 h + 63).
 // scratch: the routing arrays staged by build_items_slice.
 __device__ __noinline__ void gather_chunk_operand(const PersistParams& p, const int* scratch, uint8_t* slots) {
+    constexpr int kTile = tc_a_tile<TcWide>(), kSfa = tc_sfa_stage<TcWide>();
     const int n_active = __ldcg(p.rb.active);
     const int* s_c0 = scratch;
     const int* s_beg = scratch + n_active + 1 + n_active;
     const int* s_cnt = s_beg + n_active;
     const int nst = p.H / kTcKS, total_chunks = s_c0[n_active];
+    const int half = p.chunk / 2;   // pair slots per half (64 rows)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     // this warp's staging buffer: 8 KB of rows + 512 B of scales, past the routing arrays
     const uint32_t buf = smem_u32(slots) + kGatherBufBase + (uint32_t)warp * kGatherBufBytes;
-    for (int u = blockIdx.x * nw + warp; u < total_chunks * nst; u += gridDim.x * nw) {
-        const int c = u / nst, st = u % nst;
+    for (int u = blockIdx.x * nw + warp; u < total_chunks * nst * 2; u += gridDim.x * nw) {
+        const int c = u / (2 * nst), st = (u >> 1) % nst, hh = u & 1;
         int lo = 0, hi = n_active - 1;   // the routed expert of chunk c
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (s_c0[mid] <= c) lo = mid; else hi = mid - 1;
         }
-        const int tc = c - s_c0[lo], beg = s_beg[lo] + tc * p.chunk, ntok = min(p.chunk, s_cnt[lo] - tc * p.chunk);
-        uint8_t* dst = const_cast<uint8_t*>(p.ta.xc4) + ((size_t)c * nst + st) * 8192;   // workspace memory
-        uint8_t* dsf = const_cast<uint8_t*>(p.ta.xcs) + ((size_t)c * nst + st) * 512;
+        const int tc = c - s_c0[lo], beg = s_beg[lo] + tc * p.chunk + hh * half;
+        const int ntok = min(half, s_cnt[lo] - tc * p.chunk - hh * half);   // <= 0: an empty half
+        uint8_t* dst = const_cast<uint8_t*>(p.ta.xc4) + ((size_t)c * nst + st) * kTile + hh * (kTile / 2);   // workspace
+        uint8_t* dsf = const_cast<uint8_t*>(p.ta.xcs) + ((size_t)c * nst + st) * kSfa + hh * (kSfa / 2);
         const int rows = p.terms, pp = rows * 8;   // term rows per pair; 16-byte pieces per pair
         // the chunk's tokens (lane q: pair q), then every pair's rows and scales into this
         // warp's shared-memory buffer (all copies in flight at once), then out in one run
@@ -1211,7 +1222,7 @@ __device__ __noinline__ void gather_chunk_operand(const PersistParams& p, const 
         __syncwarp();
         // rows are 128-byte swizzled by their row index mod 8 (the source by term j): with 4
         // terms an odd pair slot's rows 4q + j have phase j ^ 4, so their 16-byte pieces
-        // swap places c <-> c ^ 4
+        // swap places c <-> c ^ 4 (half is even: a slot's parity within the half is its own)
         for (int i = lane; i < ntok * pp; i += 32) {
             const int qq = i / pp, w = i % pp;
             const int o = (rows == 4 && (qq & 1)) ? (w ^ 4) : w;
@@ -1293,8 +1304,9 @@ __device__ __noinline__ void combine_elems(const PersistParams& p, int l, const 
 template <bool kGathered, bool kNorm>
 __device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMaps* maps, uint8_t* smem_raw,
                                                   uint32_t tmem, TcRoleState* rs, unsigned long long deadline) {
-    const TcSmem s = tc_smem(smem_raw);
-    if (threadIdx.x == kTcWarpProducer * 32) {
+    using C = typename TcGeom<kGathered>::type;
+    const TcSmem s = tc_smem<C>(smem_raw);
+    if (threadIdx.x == C::kProducer * 32) {
         fence_proxy_async_global();   // inputs written by other CTAs before the last barrier / flag
         prefetch_tensormap(&maps->gate_q);
         prefetch_tensormap(&maps->up_q);
@@ -1304,7 +1316,7 @@ __device__ __noinline__ void persist_expert_phase(const TcArgs args, const TcMap
         prefetch_tensormap(&maps->down_s);
     }
     TcRoleState r = *rs;
-    tc_phase<kGathered, kNorm>(*maps, args, s, tmem, r, deadline);
+    tc_phase<C, kNorm>(*maps, args, s, tmem, r, deadline);
     *rs = r;
 }
 
@@ -1355,7 +1367,8 @@ __device__ __forceinline__ void router_first_copies(const PersistParams& p, cons
 template <bool kLarge, bool kNorm>
 __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* smem_raw, uint32_t tmem,
                                             unsigned long long deadline) {
-    const TcSmem sm = tc_smem(smem_raw);
+    using C = typename TcGeom<kLarge>::type;
+    const TcSmem sm = tc_smem<C>(smem_raw);
     int* abort = p.wl.abort;
     int* status = p.ta.status;
     float* red = sm.red;                                   // block reductions (<= 32 floats)
@@ -1471,7 +1484,7 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
         // the loader warps are done with the phase before the other roles (once the producer
         // has no more items): they run the combine code once without storing, so this SM's
         // instruction cache holds it when the combine starts after the barrier
-        if (!kNorm && tc_loader_index((int)(threadIdx.x >> 5)) >= 0)
+        if (!kNorm && C::loader_index((int)(threadIdx.x >> 5)) >= 0)
             combine_elems(p, l, small ? sm.rt : nullptr, sm.slots, true);
         if (small && blockIdx.x == 0) publish_small(p, l, sm.rt);
         if (!grid_sync(p.bar, btok, deadline, abort, status)) return;
@@ -1511,13 +1524,14 @@ __device__ __noinline__ void persist_layers(const PersistParams& p, uint8_t* sme
 template <bool kLarge, bool kNorm>
 __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_constant__ PersistParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const TcSmem sm = tc_smem(smem_raw);
+    using C = typename TcGeom<kLarge>::type;
+    const TcSmem sm = tc_smem<C>(smem_raw);
     // every thread reads the tag and the abort flag (nothing in this launch writes either
     // before its first grid barrier, so all threads see the same values); used after the setup
     const unsigned long long tag = *reinterpret_cast<const volatile unsigned long long*>(p.state_tag);
     const int aborted_before = *reinterpret_cast<const volatile int*>(p.wl.abort);
     router_first_copies<kLarge>(p, sm, reinterpret_cast<int*>(sm.red + 40));   // in flight during the setup
-    const uint32_t tmem = tc_setup(sm);
+    const uint32_t tmem = tc_setup<C>(sm);
     const unsigned long long deadline = globaltimer_ns() + p.ta.timeout_ns;
     if (tag != p.tag) {
         if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -1532,7 +1546,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) persist_kernel(const __grid_con
     if (threadIdx.x == 0 && p.tstamp && blockIdx.x < 256)   // when each CTA finished (profiling)
         p.tstamp[56 + blockIdx.x] = globaltimer_ns();
     cp_async_wait_all();   // router-weight copies still in flight (a run cut short) land before exit
-    tc_teardown(sm, tmem, p.ta.timeout_ns);
+    tc_teardown<C>(sm, tmem, p.ta.timeout_ns);
 }
 
 }  // namespace moe

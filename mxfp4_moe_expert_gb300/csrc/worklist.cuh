@@ -1,6 +1,8 @@
 // Work items of the expert phase.  The routed pairs of a layer are grouped per
 // expert (perm order: each expert's pairs in (token, slot) order) and cut into
-// chunks of at most 8 pairs.  For every chunk there are I/128 gate/up items (a
+// chunks of at most 8 pairs (blocks routed through the workspace: 32 pairs with 4 E2M1
+// terms per activation, or 16 with 8, so that a chunk fills the MMA's 128 activation
+// rows).  For every chunk there are I/128 gate/up items (a
 // 128-row block of the gate and of the up matrix over all of K = H) and H/256 down
 // items (a 256-row block of the down matrix over all of K = I).  Within an expert the
 // items are ordered row block major, chunk minor: the chunks that read the same
@@ -16,8 +18,10 @@ namespace moe {
 constexpr int kTmaRows = 128;   // rows per gate/up item (of each of the two matrices)
 constexpr int kDownRows = 256;  // rows per down item
 constexpr int kTmaTok = 8;      // pairs per chunk (8 E2M1 terms per activation)
-constexpr int kDenseTok = 16;   // pairs per chunk of the dense operand (4 terms per activation)
-constexpr int kMaxChunk = 16;
+// blocks routed through the workspace: chunks fill the MMA's 128 activation rows
+constexpr int kDenseTok = 32;   // pairs per chunk of the dense operand (4 terms per activation)
+constexpr int kWideTok = 16;    // pairs per chunk with 8 terms per activation
+constexpr int kMaxChunk = 16;   // words of pair ids in a record
 
 enum : int { kItemGateUp = 0, kItemDown = 1 };
 
@@ -32,8 +36,10 @@ struct __align__(16) ItemRec {
     int code;            // item_code(kind, rb, tc, a)
     int e;               // expert id
     int beg;             // first position of the chunk's pairs in perm
-    int ntok;            // pairs in the chunk (1..8, or 1..16 with the dense operand)
-    int tok[kMaxChunk];  // gate/up items: token of each pair; down items: pair id (t*k + j)
+    int ntok;            // pairs in the chunk (1..8; blocks routed through the workspace: 1..32)
+    int tok[kMaxChunk];  // gate/up items: token of each pair; down items: pair id (t*k + j);
+                         // blocks routed through the workspace: 16-bit halves, pair slots
+                         // 2q and 2q + 1 in word q
     int chunk;           // chunk index within the layer
     int pad[3];          // pad[0]: chunks of the expert (the items of one row block are adjacent)
 };
