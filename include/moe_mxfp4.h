@@ -87,9 +87,9 @@ extern "C" {
 #define MOE_FLAG_NORM         (1u << 0) /* pre-norm residual stack (see above) */
 #define MOE_FLAG_OUT_BF16     (1u << 1) /* y is bf16 instead of fp32 */
 #define MOE_FLAG_MULTI_KERNEL (1u << 2) /* one launch per phase (comparison path) */
-#define MOE_FLAG_NO_DENSE     (1u << 3) /* blocks routed through the workspace (T*k > 64 or T*E > 8192) keep
-                                          * chunks of 8 pairs x 8 E2M1 terms per activation instead of the
-                                          * dense operand of 16 pairs x 4 terms (see moe_mxfp4_forward) */
+#define MOE_FLAG_NO_DENSE     (1u << 3) /* blocks routed through the workspace (T*k > 64 or T*E > 8192) use
+                                          * chunks of 16 pairs x 8 E2M1 terms per activation instead of the
+                                          * dense operand of 32 pairs x 4 terms (see moe_mxfp4_forward) */
 #define MOE_FLAG_DEBUG_STALL  (1u << 4) /* testing aid: the forward withholds one device-side signal (one
                                           * CTA's first grid-barrier arrival in the persistent forward; the
                                           * gate/up completions of the first routed expert in the one-launch-
@@ -192,9 +192,10 @@ int moe_mxfp4_workspace_bytes(const moe_mxfp4_handle* h, int32_t num_tokens, siz
  * encoding the residual of the previous ones.  A block of at most 64 (token, slot)
  * pairs (T*k <= 64, T*E <= 8192) works through chunks of at most 8 pairs of an expert
  * with 8 terms per activation (for N(0,1) inputs the sum stays within ~1e-7 of the
- * 32-block's maximum); larger blocks use chunks of up to 16 pairs with 4 terms (within
- * ~3e-4 of the block maximum; each weight tile then serves twice the pairs), unless
- * MOE_FLAG_NO_DENSE is set.  Products are summed in fp32. */
+ * 32-block's maximum); larger blocks use chunks of up to 32 pairs with 4 terms (within
+ * ~3e-4 of the block maximum; each weight tile then serves four times the pairs), or
+ * of up to 16 pairs with 8 terms when MOE_FLAG_NO_DENSE is set.  Products are summed
+ * in fp32. */
 int moe_mxfp4_forward(moe_mxfp4_handle* h, const void* x_dev, int32_t num_tokens, void* y_dev,
                       void* workspace_dev, size_t workspace_bytes, void* stream,
                       const moe_mxfp4_debug* dbg);

@@ -917,12 +917,15 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
         tc_fence_after();
         if (warp == 0 && lane == 0) tc_trace(a, 5, rs.n);
         const bool mine = p < ntok;
+        // TcWide: a warp whose lane quarter holds no pair of the chunk has nothing to read
+        // or store (its accumulator rows are never read back)
+        const bool used = !C::kWide || (32 / kT) * q < ntok;
         // TcSmall: G, U = the column sums (gate / up, or the two down blocks), used after the
         // accumulator is released.  TcWide: each chunk is finished as soon as it is read, so
         // that only 8 values per chunk stay live: down items store their sums at once (the
         // stores do not wait), gate/up items keep h = silu(g) * u in G.
         float G[kCW][kV], U[kCW][kV];
-        if (kind >= 0) {
+        if (kind >= 0 && used) {
             if constexpr (kCW == 1) {   // both column blocks in flight at once
                 uint32_t r0[32], r1[32];
                 const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemAcc + 32 * c0;
@@ -992,6 +995,7 @@ __device__ __noinline__ bool tc_epilogue(const TcArgs& a_in, const TcSmem& s_in,
             }
 #pragma unroll
             for (int h = 0; h < kCW; ++h) {
+                if (!used) break;
                 const int c = c0 + 2 * h;
                 float hv[kV];
 #pragma unroll

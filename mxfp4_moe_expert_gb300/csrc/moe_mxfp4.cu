@@ -509,11 +509,12 @@ int forward_persistent(moe_mxfp4_handle* h, const void* x, int T, void* y, char*
             p.layer[l].norm_w = reinterpret_cast<const __nv_bfloat16*>(ly.norm_w_dev);
         }
         void* kargs[] = {&p};
+        // blocks routed through the workspace run the wide instantiation
         const void* kern =
-            p.norm ? (p.ta.xc4 ? reinterpret_cast<const void*>(moe::persist_kernel<true, true>)
-                               : reinterpret_cast<const void*>(moe::persist_kernel<false, true>))
-                   : (p.ta.xc4 ? reinterpret_cast<const void*>(moe::persist_kernel<true, false>)
-                               : reinterpret_cast<const void*>(moe::persist_kernel<false, false>));
+            p.norm ? (!small_block ? reinterpret_cast<const void*>(moe::persist_kernel<true, true>)
+                                   : reinterpret_cast<const void*>(moe::persist_kernel<false, true>))
+                   : (!small_block ? reinterpret_cast<const void*>(moe::persist_kernel<true, false>)
+                                   : reinterpret_cast<const void*>(moe::persist_kernel<false, false>));
         if (cudaLaunchCooperativeKernel(kern, dim3(h->persist_grid),
                                         dim3(moe::kTcThreads), kargs, moe::kTcSmemBytes, st) != cudaSuccess)
             return MOE_ERR_CUDA;

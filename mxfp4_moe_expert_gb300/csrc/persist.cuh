@@ -998,7 +998,11 @@ __device__ __noinline__ void stack_prep_unit(const PersistParams& p, int u, floa
 // Grouping of a larger block by one CTA (after topk_tokens): counts, offsets, perm,
 // the routed-expert list and each routed expert's first chunk, published in the
 // workspace for the work-list builders (build_items_slice).
-// scratch: shared memory of at least (2 * E + 1 + 32 * E + 64 + 3 * E + T * k) ints.
+// scratch: shared memory of at least (2 * E + 1 + 32 * E + 64 + T * k + 2 * E) ints (the
+// pairs' experts, the counts and the active list are read from it, not from the workspace).
+static_assert((36 * kMaxExperts + 65 + 512 * kTmaTok) * sizeof(int) <=
+                  (size_t)TcWide::kStages * TcWide::kSlotBytes + kTcScaleRing * TcWide::kScaleEntry,
+              "the grouping's shared-memory arrays fit the slot area and the scale ring");
 __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLayer& ly, int l, int* scratch) {
     const int T = p.T, E = p.E, k = p.k, H = p.H;
     const RouteBufs& rb = p.rb;
@@ -1010,16 +1014,21 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
     sub(0);
     // (top-k and gates were written by topk_tokens)
     sub(1);
-    int* cnt = scratch;                  // [E]
+    const int npairs = T * k;
+    int* cnt = scratch;                  // [E] counts, then offsets
     int* flag = scratch + E;             // [E + 1]
     int* wcnt = scratch + 2 * E + 1;     // [32][E] (nw <= 32)
     int* misc = wcnt + 32 * E;           // [64]
+    int* sidx = misc + 64;               // [T * k] each pair's expert, -1 outside the shard
+    int* scnt = sidx + npairs;           // [E] counts
+    int* sact = scnt + E;                // [E] the active list
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
-    const int npairs = T * k;
     for (int s = threadIdx.x; s < npairs; s += blockDim.x) {
-        const int e = rb.idx[s];
-        if (e >= p.e_begin && e < p.e_end) atomicAdd(&cnt[e], 1);
+        int e = rb.idx[s];
+        if (e < p.e_begin || e >= p.e_end) e = -1;
+        sidx[s] = e;
+        if (e >= 0) atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
     sub(2);
@@ -1027,6 +1036,7 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
     if (warp == 0) {
         for (int e = lane; e < E; e += 32) {
             rb.counts[e] = cnt[e];
+            scnt[e] = cnt[e];
             flag[e] = cnt[e] > 0 ? 1 : 0;
         }
         __syncwarp();
@@ -1036,7 +1046,10 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
         __syncwarp();
         for (int e = lane; e < E; e += 32) {
             rb.offsets[e] = cnt[e];
-            if (rb.counts[e] > 0) rb.active[1 + flag[e]] = e;
+            if (scnt[e] > 0) {
+                rb.active[1 + flag[e]] = e;
+                sact[flag[e]] = e;
+            }
         }
         if (lane == 0) {
             rb.offsets[E] = total;
@@ -1050,14 +1063,7 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
     // in warp order (on top of the expert offsets), then each warp places its pairs in order.
     const int seg = (npairs + nw - 1) / nw;
     const int s_lo = min(npairs, warp * seg), s_hi = min(npairs, s_lo + seg);
-    auto pair_expert = [&](int s) {
-        int e = -1;
-        if (s < s_hi) {
-            e = rb.idx[s];
-            if (e < p.e_begin || e >= p.e_end) e = -1;
-        }
-        return e;
-    };
+    auto pair_expert = [&](int s) { return s < s_hi ? sidx[s] : -1; };
     for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wcnt[i] = 0;
     __syncthreads();
     for (int b = s_lo; b < s_hi; b += 32) {
@@ -1091,8 +1097,7 @@ __device__ __noinline__ void route_phase(const PersistParams& p, const PersistLa
     const int n_active = misc[0];
     const int rbu = p.I / kTmaRows, rbd = H / kDownRows;
     int* chunk0 = flag;                 // [n_active + 1]
-    for (int a = threadIdx.x; a < n_active; a += blockDim.x)
-        chunk0[a] = (__ldcg(rb.counts + __ldcg(rb.active + 1 + a)) + p.chunk - 1) / p.chunk;
+    for (int a = threadIdx.x; a < n_active; a += blockDim.x) chunk0[a] = (scnt[sact[a]] + p.chunk - 1) / p.chunk;
     __syncthreads();
     if (warp == 0) {
         const int total_chunks = warp_excl_scan(chunk0, n_active);
