@@ -11,26 +11,27 @@
 //                         item) in the 128-byte swizzled layout, as one 32 KB TMA box
 //                         from the packed layout (pack.cuh) or two [128 rows x 128 B]
 //                         boxes from the canonical one, and the activation operand of
-//                         down items and of gathered chunks (8 E2M1 terms per pair,
+//                         down items and of gathered chunks (E2M1 terms per pair,
 //                         below); the weights' E8M0 scales come per group of stages
 //                         through their own ring;
 //   activation loaders    (3 warps) the per-token activation rows and scales of gate/up
 //                         stages, by cp.async (see tc_load);
 //   MMA issuer (one lane) per stage 4 block-scaled MMAs (kind::mxf4, K = 64 each):
-//                         A = the activation terms (M = 128 rows, rows 8p + j of pair
-//                         slot p, term j; the dense operand: rows 4p + j, 16 pairs x 4
-//                         terms; rows 64.. unused), B = the weights (N = 256 rows), one
-//                         E8M0 scale per row and 32-element block, fp32 accumulator
+//                         A = the activation terms (M = 128 rows: rows 8p + j of pair
+//                         slot p, term j, 8 pairs with rows 64.. unused; blocks routed
+//                         through the workspace fill all 128: rows 4p + j of 32 pairs x
+//                         4 terms, or 8p + j of 16 x 8), B = the weights (N = 256 rows),
+//                         one E8M0 scale per row and 32-element block, fp32 accumulator
 //                         [128 x 256] in tensor memory;
 //   scale-factor warps    rearrange the stage's scales in shared memory into the
 //                         16-byte rows that tcgen05.cp puts into tensor memory, and
 //                         issue those copies (3 warps);
-//   epilogue warps (8)    lanes 0..63 of the accumulator (two lane quarters x four
-//                         column chunks): sum each pair's 8 term rows (shuffle
-//                         reduce-scatter over groups of 8 lanes), then gate/up items
-//                         apply SwiGLU and store h split into 8 E2M1 terms in the
-//                         down projection's operand layout; down items store fp32
-//                         per-pair partial outputs.
+//   epilogue warps (8)    the used lanes of the accumulator (lane quarters 0 and 1 x
+//                         four column chunks, or all four quarters x two): sum each
+//                         pair's term rows (shuffle reduce-scatter over the pair's
+//                         lanes), then gate/up items apply SwiGLU and store h split into
+//                         E2M1 terms in the down projection's operand layout; down items
+//                         store fp32 per-pair partial outputs (TcSmall / TcWide below).
 // One block-scaled MMA costs about the same for N = 64 as for N = 256, so the
 // weights take the wide operand: 8 KB of weights per MMA.  Every TMA request moves
 // whole 128-byte rows (narrower rows cost as much per request).

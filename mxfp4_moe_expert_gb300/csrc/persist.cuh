@@ -17,7 +17,8 @@
 //                      larger blocks: top-k on every warp, the grouping by CTA 0 while
 //                      the other CTAs wait on a release flag, then every CTA builds its
 //                      share of the work list and gathers the operand per chunk
-//   [experts]          the work-queue expert phase of expert_tc.cuh
+//                      (chunks of 32 pairs x 4 terms, all 128 rows of the MMA)
+//   [experts]          the work-queue expert phase of expert_tc.cuh (TcSmall or TcWide)
 //   -- grid barrier --
 //   [combine]          all CTAs: gate-weighted sum of the pair outputs (grid-stride
 //                      over (token, 4 columns))

@@ -391,15 +391,24 @@ def test_large_layer_all_rows():
     _layer_full_size("large")
 
 
+DENSE_CHUNK = 32   # pairs per chunk of a block routed through the workspace (4 E2M1 terms each)
+
+
 def batched_rows(wl, idx, n_hot=3, n_total=48, seed=7):
     """Rows of the 256-token Zipf block to compare: every token of the first and of the
-    last 8-pair chunk of the n_hot most popular experts (the chunks that reuse those
+    last chunk (DENSE_CHUNK pairs, the chunking the kernel uses) of the most popular expert,
+    the first and last 8 pairs of the next n_hot - 1 experts (the chunks that reuse those
     experts' weight rows most), tokens 0 and T-1, then seeded random tokens up to n_total."""
     counts, offsets, perm = O.assignment(idx, wl.E)
     rows = {0, wl.T - 1}
-    for e in np.argsort(-counts, kind="stable")[:n_hot]:
+    for rank, e in enumerate(np.argsort(-counts, kind="stable")[:n_hot]):
         pairs = perm[offsets[e]:offsets[e + 1]]
-        for chunk in (pairs[:8], pairs[-8:]):
+        if rank == 0:
+            last = (len(pairs) - 1) // DENSE_CHUNK * DENSE_CHUNK
+            ends = (pairs[:DENSE_CHUNK], pairs[last:])
+        else:
+            ends = (pairs[:8], pairs[-8:])
+        for chunk in ends:
             rows.update(int(p) // wl.k for p in chunk)
     rng = np.random.default_rng(seed)
     for t in rng.permutation(wl.T):
