@@ -281,6 +281,8 @@ def run_gpu(args):
         build.build()
 
     wl = WORKLOADS[args.workload]
+    if args.experts:
+        wl = wl.scaled(E=args.experts, name=f"{wl.name}_E{args.experts}")
     packed = args.layout == "packed" and moe_tma(wl)
     inputs, layers = device_layers(wl, device=dev, packed=packed)   # the one-time repack is outside the timed region
     flags = pkg.MOE_FLAG_NORM if wl.norm else 0
@@ -633,6 +635,9 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="multi-stream sweep of the 384-expert layer")
     ap.add_argument("--layout", default="packed", choices=["packed", "canonical"],
                     help="expert weights streamed from the packed (tile-major) copy or the canonical layout")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling aid: the workload with this many experts (a reduced layer for ncu captures "
+                         "that must hold a few GB at most); the line names it <workload>_E<n>")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

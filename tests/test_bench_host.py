@@ -62,6 +62,15 @@ def test_traffic_record_names_a_summary_and_a_source_hash(name):
     assert len(rec["source_sha256"]) == 64
 
 
+def test_traffic_records_are_keyed_to_the_current_kernel_sources():
+    """The committed DRAM counters describe the kernel as built from these sources (the bench
+    reports them only then): a kernel change without a new capture shows up here."""
+    import json
+    recs = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
+    h = _bench().kernel_sources_sha256()
+    assert all(recs[w]["source_sha256"] == h for w in ("large", "mid", "batched", "stack"))
+
+
 def test_reference_arm_prints_the_contract_line():
     """`bench.py --impl reference` (the oracle on the host cores) prints one JSON line with
     the keys the driver reads; run on the small workload so it takes a second."""
