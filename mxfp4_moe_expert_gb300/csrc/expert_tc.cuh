@@ -193,7 +193,7 @@ struct TcArgs {
     int debug_stall;          // testing aid: chunk 0 never signals its gate/up items
     const RouteTable* rt;     // shared-memory routing table, or NULL
     unsigned long long* trace;   // [6][256] per-stage timestamps of CTA 0 (profiling), or NULL
-    int dense;                // gathered chunks hold 16 pairs x 4 E2M1 terms (rows 4p + j) instead of 8 x 8
+    int dense;                // gathered chunks hold 32 pairs x 4 E2M1 terms (rows 4p + j) instead of 16 x 8
 };
 
 // Profiling aid: event `ev` of ring stage / item i of CTA 0.

@@ -55,7 +55,7 @@ def _crafted_bytes(wl):
                               "persistent_dense", "persistent_gathered_8x8"])
 def test_every_weight_byte_decodes_as_the_format_defines(flags, packed, T):
     """T = 40 (80 pairs) is routed through the workspace: its chunks take the dense operand
-    (16 pairs x 4 terms), or 8 pairs x 8 terms with MOE_FLAG_NO_DENSE."""
+    (32 pairs x 4 terms), or 16 pairs x 8 terms with MOE_FLAG_NO_DENSE."""
     wl = WL.scaled(T=T)
     assert (wl.H // 2) == 256 and (wl.I // 2) == 256   # one full byte cycle per row
     inputs = make_inputs(wl)

@@ -152,9 +152,9 @@ def test_layer_parity_packed_experts(wl):
 
 @pytest.mark.parametrize("wl", [w for w in SMALL if w.name in ("tma_many_tokens", "tma_max_pairs")], ids=lambda w: w.name)
 def test_gathered_blocks_with_and_without_the_dense_operand(wl):
-    """Blocks routed through the workspace run chunks of 16 pairs x 4 E2M1 terms (dense
-    operand) by default and of 8 pairs x 8 terms with MOE_FLAG_NO_DENSE: both against the
-    oracle on every row, and the 8 x 8 result nearer to it."""
+    """Blocks routed through the workspace run chunks of 32 pairs x 4 E2M1 terms (dense
+    operand) by default and of 16 pairs x 8 terms with MOE_FLAG_NO_DENSE: both against the
+    oracle on every row, and the 8-term result nearer to it."""
     inputs, layers = device_layers(wl, device=DEV, weights_device="cpu", quantizer=oracle_quantizer_to(DEV),
                                    packed=True)
     wr, b, _ = oracle_layer_args(inputs, 0)
